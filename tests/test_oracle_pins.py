@@ -1,0 +1,341 @@
+"""Pins for the CPU oracle: checks against what the pages and the mathematics
+fix, never against the oracle's own formulas retyped.
+
+* printed numbers of the pages (tests/golden/pages_numbers.json, cited);
+* the absorption identity of the DeepSeek MLA teardown page, §4 (path A,
+  decompress, equals path B, absorb) on brute-force inputs;
+* special cases with closed forms (one token, zero query);
+* reduction to a library routine (torch scaled_dot_product_attention);
+* a pure-Python loop restatement on tiny dimensions;
+* paging invariants and the split-KV merge;
+* planted mistakes, to show each pin catches a plausible slip.
+"""
+import json
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+import oracle
+from mla_latent_kv_02_gb300 import workloads as wl
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "pages_numbers.json")))
+SCALE = 1.0 / math.sqrt(128 + 64)
+
+
+def _rel(a, b):
+    return float(np.max(np.abs(np.asarray(a) - np.asarray(b))) / max(np.max(np.abs(b)), 1e-300))
+
+
+# ---------------------------------------------------------------- byte formula
+def test_kv_bytes_matches_printed_numbers():
+    per_layer = oracle.kv_bytes(1, 512, 64, 2, 1)
+    assert per_layer == GOLD["bytes_per_token_per_layer"]["value"]
+    per_tok = oracle.kv_bytes(60, 512, 64, 2, 1)
+    assert per_tok == GOLD["bytes_per_token_all_layers"]["value"]
+    assert Fraction(per_tok, 1024) == Fraction(GOLD["kib_per_token_all_layers"]["value"]).limit_denominator()
+    full = oracle.kv_bytes(60, 512, 64, 2, 128 * 1024)
+    g = GOLD["gib_per_128ki_token_sequence"]
+    assert oracle.gib(full) == Fraction(g["num"], g["den"])
+    assert float(oracle.gib(full)) == g["value"]
+    # elements per token per layer and its KiB size in bf16
+    assert 512 + 64 == GOLD["elements_per_token_per_layer"]["value"]
+    assert per_layer / 1024 == GOLD["kib_per_token_per_layer_bf16"]["value"]
+
+
+def test_kv_bytes_reductions_and_pages():
+    red = 1 - Fraction(576, 8192)
+    assert round(float(red * 100), 2) == GOLD["element_reduction_percent_8192_to_576"]["value"]
+    mha = 128 * 128 * 2 * 2          # K and V, 128 heads x 128 dims, 2 bytes
+    assert mha / 1024 == GOLD["mha_kib_per_token_per_layer_bf16"]["value"]
+    saving = 1 - Fraction(oracle.kv_bytes(1, 512, 64, 2, 1), mha)
+    assert round(float(saving * 100), 2) == GOLD["mla_vs_mha_saving_percent"]["value"]
+    page = oracle.kv_bytes(1, 512, 64, 2, GOLD["page_tokens"]["value"])
+    assert page == 73728 and page / 1024 == GOLD["page_kib_bf16"]["value"]
+    assert oracle.kv_bytes(1, 512, 64, 2, 16) / 1024 == GOLD["page16_kib_bf16"]["value"]
+
+
+def test_kv_bytes_64k_batch16_sizing():
+    """60 layers: MLA 67.5 GiB; the page's '~69 GB' is the 61-layer figure in
+    GiB (68.6), so only agreement to the printed precision of the rounded
+    number is asserted (a 3% band)."""
+    mla = oracle.kv_bytes(60, 512, 64, 2, 65536, 16)
+    assert oracle.gib(mla) == Fraction(135, 2)
+    approx = GOLD["mla_64k_b16_gb_approx"]["value"]
+    assert abs(float(oracle.gib(mla)) - approx) / approx < 0.03
+    mha = 60 * 128 * 128 * 2 * 2 * 65536 * 16
+    assert mha / 1024 ** 4 == GOLD["mha_64k_b16_tb_approx"]["value"]
+
+
+@pytest.mark.parametrize("args", [(0, 512, 64, 2, 1), (60, 0, 64, 2, 1), (60, 512, -1, 2, 1),
+                                  (60, 512, 64, 0, 1), (60, 512, 64, 2, 0), (60, 512, 64, 2, 1, 0)])
+def test_kv_bytes_invalid_dimension(args):
+    with pytest.raises(ValueError, match="invalid dimension"):
+        oracle.kv_bytes(*args)
+
+
+def test_kv_bytes_zero_rope_allowed():
+    assert oracle.kv_bytes(1, 512, 0, 2, 1) == 1024
+
+
+# ---------------------------------------------------------------- absorption identity
+def _tiny_inputs(n, seed, H=128, dhc=128, dc=512, dr=64):
+    rng = np.random.Generator(np.random.PCG64(seed))
+    q_c = rng.standard_normal((H, dhc))
+    q_r = rng.standard_normal((H, dr))
+    c = rng.standard_normal((n, dc))
+    k = rng.standard_normal((n, dr))
+    w_uk = rng.standard_normal((H, dhc, dc)) / math.sqrt(512)
+    w_uv = rng.standard_normal((H, dc, dhc)) / math.sqrt(512)
+    return q_c, q_r, c, k, w_uk, w_uv
+
+
+@pytest.mark.parametrize("n", [1, 5, 64, 65])
+def test_absorbed_equals_decompressed(n):
+    q_c, q_r, c, k, w_uk, w_uv = _tiny_inputs(n, seed=n)
+    naive_out, naive_lse = oracle.naive_attention_row(q_c, q_r, c, k, w_uk, w_uv, SCALE)
+    qa = oracle.absorb_q(q_c[None], w_uk)[0]
+    o_lat, lse = oracle.attention_row(qa, q_r, c, k, SCALE)
+    out = oracle.up_v(o_lat[None], w_uv)[0]
+    assert _rel(out, naive_out) < 1e-12
+    assert _rel(lse, naive_lse) < 1e-12
+
+
+def test_page_equivalence_script_setup_fp64():
+    """The teardown page's §4 script: seed 42, nh128/dhc128/dc512/dr64/S2048,
+    N(0,1) bf16 inputs and W_UK; in float64 the two paths agree far inside the
+    page's cosine bound."""
+    torch = pytest.importorskip("torch")
+    s = GOLD["absorption_setup"]
+    torch.manual_seed(s["seed"])
+    bf = torch.bfloat16
+    q_c = torch.randn(1, s["nh"], s["dhc"], dtype=bf)
+    q_r = torch.randn(1, s["nh"], s["dr"], dtype=bf)
+    w_uk = torch.randn(s["nh"], s["dhc"], s["dc"], dtype=bf)
+    c_kv = torch.randn(s["S"], s["dc"], dtype=bf)
+    k_r = torch.randn(s["S"], s["dr"], dtype=bf)
+    f = lambda t: t.double().numpy()
+    scale = oracle.default_scale(s["dhc"], s["dr"])
+    a = oracle.naive_scores(f(q_c)[0], f(q_r)[0], f(c_kv), f(k_r), f(w_uk), scale)
+    b = oracle.absorbed_scores(f(q_c)[0], f(q_r)[0], f(c_kv), f(k_r), f(w_uk), scale)
+    cos = float(np.dot(a.ravel(), b.ravel()) / (np.linalg.norm(a) * np.linalg.norm(b)))
+    assert cos > GOLD["absorption_cosine_min"]["value"]
+    assert _rel(b, a) < 1e-12
+
+
+# ---------------------------------------------------------------- closed forms
+def test_softmax_rows_sum_to_one_and_match_scipy():
+    sp = pytest.importorskip("scipy.special")
+    rng = np.random.Generator(np.random.PCG64(3))
+    s = rng.standard_normal((7, 33)) * 5
+    p, lse = oracle.softmax_lse(s)
+    assert np.max(np.abs(p.sum(-1) - 1)) < 1e-12
+    assert _rel(p, sp.softmax(s, axis=-1)) < 1e-12
+    assert _rel(lse, sp.logsumexp(s, axis=-1)) < 1e-12
+
+
+def test_single_token_gives_its_value():
+    q_c, q_r, c, k, w_uk, w_uv = _tiny_inputs(1, seed=11)
+    qa = oracle.absorb_q(q_c[None], w_uk)[0]
+    o_lat, lse = oracle.attention_row(qa, q_r, c, k, SCALE)
+    out = oracle.up_v(o_lat[None], w_uv)[0]
+    expect = np.stack([c[0] @ w_uv[h] for h in range(128)])
+    assert _rel(out, expect) < 1e-12
+    s0 = (qa @ c[0] + q_r @ k[0]) * SCALE
+    assert _rel(lse, s0) < 1e-12
+
+
+def test_zero_query_gives_mean_of_visible_latents():
+    n = 37
+    _, _, c, k, _, _ = _tiny_inputs(n, seed=5)
+    o_lat, lse = oracle.attention_row(np.zeros((128, 512)), np.zeros((128, 64)), c, k, SCALE)
+    assert _rel(o_lat, np.broadcast_to(c.mean(0), o_lat.shape)) < 1e-12
+    assert np.allclose(lse, math.log(n), rtol=0, atol=1e-12)
+
+
+def test_reduces_to_sdpa_with_identity_projections():
+    """With d_c = d_hc and W_UK = W_UV = I, absorbed MLA is single-KV-head
+    attention with keys [c | k_R] and values c: compare with torch SDPA (fp64),
+    including causal rows of a multi-token query."""
+    torch = pytest.importorskip("torch")
+    H, d, dr, n, q = 8, 32, 16, 45, 3
+    rng = np.random.Generator(np.random.PCG64(9))
+    q_c = rng.standard_normal((q, H, d))
+    q_r = rng.standard_normal((q, H, dr))
+    c = rng.standard_normal((n, d))
+    k = rng.standard_normal((n, dr))
+    eye = np.broadcast_to(np.eye(d), (H, d, d)).copy()
+    scale = 1 / math.sqrt(d + dr)
+    # paged cache of one sequence, identity pages of 8 tokens
+    page = 8
+    npg = (n + page - 1) // page
+    cache = np.zeros((npg, page, d + dr))
+    cache.reshape(-1, d + dr)[:n] = np.concatenate([c, k], 1)
+    bt = np.arange(npg)[None]
+    res = oracle.mla_step(q_c, q_r, eye, eye, cache, bt, [n], [q], scale, dc=d)
+    Q = torch.from_numpy(np.concatenate([q_c, q_r], -1)).permute(1, 0, 2)[None]   # [1,H,q,d+dr]
+    K = torch.from_numpy(np.concatenate([c, k], -1))[None, None].expand(1, H, n, d + dr)
+    V = torch.from_numpy(c)[None, None].expand(1, H, n, d)
+    vis = torch.tensor([[j <= n - q + i for j in range(n)] for i in range(q)])
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, attn_mask=vis, scale=scale)
+    ref = ref[0].permute(1, 0, 2).numpy()
+    assert _rel(res["out"], ref) < 1e-12
+    assert _rel(res["o_lat"], ref) < 1e-12
+
+
+def _python_loops_row(q_c, q_r, c, k, w_uk, w_uv, scale):
+    """MLA for one query written as explicit loops over the definition."""
+    H, dhc = len(q_c), len(q_c[0])
+    n, dc, dr = len(c), len(c[0]), len(k[0])
+    out = []
+    for h in range(H):
+        # K_h[j][d] = sum_c c[j][c] W_UK[h][d][c];  V_h[j][d] = sum_c c[j][c] W_UV[h][c][d]
+        s = []
+        for j in range(n):
+            acc = 0.0
+            for dd in range(dhc):
+                kk = 0.0
+                for cc in range(dc):
+                    kk += c[j][cc] * w_uk[h][dd][cc]
+                acc += q_c[h][dd] * kk
+            for rr in range(dr):
+                acc += q_r[h][rr] * k[j][rr]
+            s.append(acc * scale)
+        m = max(s)
+        e = [math.exp(x - m) for x in s]
+        z = sum(e)
+        row = []
+        for dd in range(w_uv.shape[2]):
+            v = 0.0
+            for j in range(n):
+                vj = 0.0
+                for cc in range(dc):
+                    vj += c[j][cc] * w_uv[h][cc][dd]
+                v += e[j] / z * vj
+            row.append(v)
+        out.append(row)
+    return np.array(out)
+
+
+def test_pure_python_loops_tiny_dims():
+    H, dhc, dc, dr, n = 2, 3, 4, 2, 3
+    rng = np.random.Generator(np.random.PCG64(21))
+    q_c = rng.standard_normal((1, H, dhc))
+    q_r = rng.standard_normal((1, H, dr))
+    c = rng.standard_normal((n, dc))
+    k = rng.standard_normal((n, dr))
+    w_uk = rng.standard_normal((H, dhc, dc))
+    w_uv = rng.standard_normal((H, dc, dhc + 1))       # d_out != d_hc exposes a transposed W_UV
+    page = 2
+    cache = np.zeros((2, page, dc + dr))
+    cache.reshape(-1, dc + dr)[:n] = np.concatenate([c, k], 1)
+    bt = np.array([[1, 0]])                             # non-identity page order
+    cache = cache[[1, 0]]
+    res = oracle.mla_step(q_c, q_r, w_uk, w_uv, cache, bt, [n], [1], 0.7, dc=dc)
+    ref = _python_loops_row(q_c[0].tolist(), q_r[0].tolist(), c.tolist(), k.tolist(), w_uk, w_uv, 0.7)
+    assert _rel(res["out"][0], ref) < 1e-12
+
+
+# ---------------------------------------------------------------- visibility / paging
+def test_visibility_rule_for_mtp_and_prefill():
+    assert oracle.visible_tokens(8194, 2, 0) == 8193
+    assert oracle.visible_tokens(8194, 2, 1) == 8194
+    assert oracle.visible_tokens(16896, 512, 0) == 16385
+    assert oracle.visible_tokens(16896, 512, 511) == 16896
+    assert oracle.visible_tokens(1024, 1, 0) == 1024
+
+
+def _cache_for(case):
+    seq, pos = case.positions()
+    slots = oracle.slot_mapping(case.block_table, seq, pos)
+    empty = np.zeros((case.num_pages, 64, 576), dtype=np.float32)
+    return oracle.append(empty, case.c_kv, case.k_r, slots)
+
+
+def test_slot_mapping_brute_force():
+    bt = np.array([[5, 2, 7], [0, 3, -1]])
+    seq = np.array([0, 0, 0, 1, 1, 1])
+    pos = np.array([0, 63, 64, 5, 64, 127])
+    assert list(oracle.slot_mapping(bt, seq, pos)) == [5 * 64, 5 * 64 + 63, 2 * 64, 5, 3 * 64, 3 * 64 + 63]
+
+
+def test_append_then_gather_roundtrip_exact():
+    case = wl.make_case([1, 130, 64, 200], [1, 2, 1, 3], seed=4, with_weights=False)
+    cache = _cache_for(case)
+    off = case.tok_off
+    for b in range(case.B):
+        n = int(case.seq_lens[b])
+        c, k = oracle.gather(cache, case.block_table, b, n)
+        assert np.array_equal(c, case.c_kv[off[b]:off[b] + n])
+        assert np.array_equal(k, case.k_r[off[b]:off[b] + n])
+
+
+def test_decode_invariant_under_page_permutation():
+    a = wl.make_case([70, 150], [1, 2], seed=6, page_order="identity", with_weights=False, with_q_abs=True)
+    b = wl.make_case([70, 150], [1, 2], seed=6, page_order="random", with_weights=False, with_q_abs=True)
+    assert not np.array_equal(a.block_table, b.block_table)
+    oa, la = oracle.decode(a.q_abs, a.q_r, _cache_for(a), a.block_table, a.seq_lens, a.q_lens, SCALE)
+    ob, lb = oracle.decode(b.q_abs, b.q_r, _cache_for(b), b.block_table, b.seq_lens, b.q_lens, SCALE)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+def test_causal_rows_use_exactly_their_prefix():
+    case = wl.make_case([100], [3], seed=8, with_weights=False, with_q_abs=True)
+    cache = _cache_for(case)
+    o, lse = oracle.decode(case.q_abs, case.q_r, cache, case.block_table, case.seq_lens, case.q_lens, SCALE)
+    for i in range(3):
+        n = 98 + i
+        ref_o, ref_l = oracle.attention_row(case.q_abs[i], case.q_r[i], case.c_kv[:n], case.k_r[:n], SCALE)
+        assert _rel(o[i], ref_o) < 1e-13 and _rel(lse[i], ref_l) < 1e-13
+
+
+@pytest.mark.parametrize("cuts", [[1], [64], [17, 90], [1, 2, 3, 150]])
+def test_split_and_combine_equals_single_pass(cuts):
+    n = 160
+    q_c, q_r, c, k, w_uk, _ = _tiny_inputs(n, seed=len(cuts))
+    qa = oracle.absorb_q(q_c[None], w_uk)[0]
+    full_o, full_l = oracle.attention_row(qa, q_r, c, k, SCALE)
+    edges = [0] + list(cuts) + [n]
+    parts = [oracle.attention_partial(qa, q_r, c[a:b], k[a:b], SCALE) for a, b in zip(edges, edges[1:])]
+    o, l = oracle.combine(parts)
+    assert _rel(o, full_o) < 1e-12 and _rel(l, full_l) < 1e-12
+
+
+# ---------------------------------------------------------------- planted mistakes
+def _pin_absorbed_vs_naive(absorb_fn=oracle.absorb_q, up_fn=oracle.up_v, scores_fn=oracle.scores):
+    q_c, q_r, c, k, w_uk, w_uv = _tiny_inputs(65, seed=99)
+    naive_out, _ = oracle.naive_attention_row(q_c, q_r, c, k, w_uk, w_uv, SCALE)
+    qa = absorb_fn(q_c[None], w_uk)[0]
+    s = scores_fn(qa, q_r, c, k, SCALE)
+    p, _ = oracle.softmax_lse(s)
+    out = up_fn((p @ c)[None], w_uv)[0]
+    return _rel(out, naive_out) < 1e-12
+
+
+def test_planted_mistakes_are_caught():
+    assert _pin_absorbed_vs_naive()
+    # dropped RoPE term
+    no_rope = lambda qa, qr, c, k, sc: (qa @ c.T) * sc
+    assert not _pin_absorbed_vs_naive(scores_fn=no_rope)
+    # wrong scale (1/sqrt(d_c + d_r))
+    bad_scale = lambda qa, qr, c, k, sc: (qa @ c.T + qr @ k.T) / math.sqrt(576)
+    assert not _pin_absorbed_vs_naive(scores_fn=bad_scale)
+    # W_UK used transposed per head (contract over c instead of d) — shapes
+    # only agree when d_hc == d_c, so plant it on a square slice
+    def bad_absorb(q, w):
+        sq = np.asarray(w)[:, :, :128]
+        out = np.zeros((q.shape[0], q.shape[1], w.shape[2]))
+        out[:, :, :128] = np.einsum("thd,hcd->thc", q, sq)
+        out[:, :, 128:] = np.einsum("thd,hdc->thc", q, np.asarray(w)[:, :, 128:])
+        return out
+    assert not _pin_absorbed_vs_naive(absorb_fn=bad_absorb)
+    # W_UV transposed within its square block
+    def bad_up(o, w):
+        w = np.array(w)
+        w[:, :128, :] = np.transpose(w[:, :128, :], (0, 2, 1))
+        return oracle.up_v(o, w)
+    assert not _pin_absorbed_vs_naive(up_fn=bad_up)
+    # off-by-one visibility would change the causal pin
+    assert oracle.visible_tokens(100, 3, 0) == 98
