@@ -1,0 +1,406 @@
+#!/usr/bin/env python3
+"""Benchmark of the absorbed paged MLA decode path on GB300.
+
+One step = one pass of the whole hot path over one batch:
+  A1 mla_kv_append (this step's new tokens) -> A2 mla_absorb_q ->
+  A3+A4 mla_decode_paged (split-KV + combine) -> A5 mla_up_v.
+
+Default workload: MTP-style decode, batch 64, 8192 cached tokens + 2 query
+tokens per sequence (128 query rows), 128 heads, d_c 512, d_r 64, page 64,
+random page tables, seed 0.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 2] [--impl mla|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from mla_latent_kv_02_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "MLA decode tokens/s and achieved KV HBM TB/s (% roofline), B=64 ctx 8K"
+SCALE = 1.0 / math.sqrt(192)
+FLOPS_PER_VISIBLE = 128 * (2 * 576 + 2 * 512)   # per (query row, visible token), all heads
+
+
+def workload_stats(case):
+    """Algorithmic work of one decode step (A3): flops and bytes."""
+    visible = 0
+    for b in range(case.B):
+        n, q = int(case.seq_lens[b]), int(case.q_lens[b])
+        visible += sum(n - q + i + 1 for i in range(q))
+    kv_tokens = int(case.seq_lens[case.q_lens > 0].astype(np.int64).sum())
+    T = case.T
+    flops = visible * FLOPS_PER_VISIBLE
+    bytes_ = kv_tokens * 1152 + T * 128 * 576 * 2 + T * 128 * 512 * 2
+    return dict(T=T, visible=visible, kv_tokens=kv_tokens, flops=flops, bytes=bytes_,
+                kv_bytes=kv_tokens * 1152)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=float(d["hbm_gbs"]), bf16_tflops=float(d["bf16_tflops"]),
+                    bf16_tflops_sustained=float(d.get("bf16_tflops_sustained", d["bf16_tflops"])),
+                    source="measured")
+    return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ distributed helpers
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def reduce_max(value: float, ws: int, device=None) -> float:
+    """Max of a float over all ranks (identity when not distributed)."""
+    if ws <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ clocks
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap",
+               0x8: "hw_slowdown", 0x10: "sync_boost", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, index: int, path: str):
+        self.path = path
+        self.proc = None
+        try:
+            self.f = open(path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={index}",
+                 "--query-gpu=index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 5:
+                continue
+            try:
+                s, m = float(parts[1]), float(parts[2])
+                r = int(parts[4], 16)
+            except ValueError:
+                continue
+            sm.append(s)
+            mx.append(m)
+            for bit, name in REASON_BITS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def cpu_baseline(case, budget_s: float, max_rows: int = 128):
+    """The oracle as it stands on a bounded sample of rows of the same workload."""
+    import oracle  # test infrastructure: only the CPU-baseline leg imports it
+    t0 = time.perf_counter()
+    cache = None
+    seq, pos = case.positions()
+    slots = oracle.slot_mapping(case.block_table, seq, pos)
+    cache = oracle.append(np.zeros((case.num_pages, 64, 576), dtype=np.float32), case.c_kv, case.k_r, slots)
+    setup = time.perf_counter() - t0
+    rows_done = 0
+    t1 = time.perf_counter()
+    order = list(range(case.T))
+    while rows_done < min(max_rows, case.T):
+        r = order[rows_done]
+        oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table,
+                        case.seq_lens, case.q_lens, SCALE, rows=[r])
+        rows_done += 1
+        if time.perf_counter() - t1 > budget_s:
+            break
+    el = time.perf_counter() - t1
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    blas = None
+    try:
+        from threadpoolctl import threadpool_info
+        blas = sum(int(x.get("num_threads", 0)) for x in threadpool_info() if x.get("user_api") == "blas") or None
+    except Exception:
+        pass
+    return dict(value=rows_done / el, unit="tokens/s", cores=int(blas or cores), kind="oracle",
+                sample=f"{rows_done} of {case.T} query rows (A2+A3+A5 in float64 NumPy, all 128 heads); "
+                       f"cache placement {setup:.1f}s untimed", seconds=el)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_mla(args):
+    import torch
+    from mla_latent_kv_02_gb300 import api
+
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+
+    case = wl.workload(args.workload, seed=0)
+    st = workload_stats(case)
+    T = case.T
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device=dev, dtype=torch.bfloat16)
+
+    dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = torch.empty((case.num_pages, 64, 576), dtype=torch.bfloat16, device=dev)
+    api.mla_cache_init(kv)
+    bt = torch.from_numpy(case.block_table).to(dev)
+    seq, pos = case.positions()
+    slots_all = api.mla_slot_mapping(case.block_table, seq, pos)
+    new_idx = case.new_token_index()
+    old_mask = np.ones(slots_all.shape[0], dtype=bool)
+    old_mask[new_idx] = False
+    old_idx = np.nonzero(old_mask)[0]
+    if old_idx.size:
+        api.mla_kv_append(bf(case.c_kv[old_idx]), bf(case.k_r[old_idx]),
+                          torch.from_numpy(slots_all[old_idx]).to(dev), kv, dev_err)
+    c_new, k_new = bf(case.c_kv[new_idx]), bf(case.k_r[new_idx])
+    slots_new = torch.from_numpy(slots_all[new_idx]).to(dev)
+    q_c, q_r = bf(case.q_c), bf(case.q_r)
+    w_uk, w_uv = bf(case.w_uk), bf(case.w_uv)
+    q_abs = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
+    o_lat = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, 128), dtype=torch.float32, device=dev)
+    out = torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev)
+    plan = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev)
+    launches_per_step = 4 + (1 if plan.info.num_split_rows > 0 else 0)
+
+    def step(ev=None):
+        api.mla_kv_append(c_new, k_new, slots_new, kv, dev_err)
+        api.mla_absorb_q(q_c, w_uk, q_abs, dev_err)
+        if ev is not None:
+            ev[0].record(stream)
+        api.mla_decode_paged(q_abs, q_r, kv, bt, plan, o_lat, dev_err, lse=lse, scale=SCALE)
+        if ev is not None:
+            ev[1].record(stream)
+        api.mla_up_v(o_lat, w_uv, out, dev_err)
+
+    for _ in range(args.warmup):
+        step()
+    if api.mla_check(dev_err) != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    K = args.steps
+    dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv")) \
+        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/mla_bench_clocks.csv")
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(K):
+        step(dec_ev[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    ms_total = reduce_max(ms_total, ws, dev)
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ev]
+    dec_avg = sum(dec_ms) / len(dec_ms)
+    if api.mla_check(dev_err) != 0:
+        raise RuntimeError("device error word set during the timed steps")
+
+    # ---- end to end through the API: pinned host inputs in, result out, plan rebuilt each step
+    h_q_c = torch.from_numpy(case.q_c).to(torch.bfloat16).pin_memory()
+    h_q_r = torch.from_numpy(case.q_r).to(torch.bfloat16).pin_memory()
+    h_c_new = c_new.cpu().pin_memory()
+    h_k_new = k_new.cpu().pin_memory()
+    h_slots = slots_new.cpu().pin_memory()
+    h_out = torch.empty((T, 128, 128), dtype=torch.bfloat16).pin_memory()
+    d_q_c, d_q_r = torch.empty_like(q_c), torch.empty_like(q_r)
+    d_c_new, d_k_new, d_slots = torch.empty_like(c_new), torch.empty_like(k_new), torch.empty_like(slots_new)
+    h2d = sum(t.numel() * t.element_size() for t in (h_q_c, h_q_r, h_c_new, h_k_new, h_slots))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        d_q_c.copy_(h_q_c, non_blocking=True)
+        d_q_r.copy_(h_q_r, non_blocking=True)
+        d_c_new.copy_(h_c_new, non_blocking=True)
+        d_k_new.copy_(h_k_new, non_blocking=True)
+        d_slots.copy_(h_slots, non_blocking=True)
+        p = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, num_clusters=plan.num_clusters)
+        api.mla_kv_append(d_c_new, d_k_new, d_slots, kv, dev_err)
+        api.mla_absorb_q(d_q_c, w_uk, q_abs, dev_err)
+        api.mla_decode_paged(q_abs, d_q_r, kv, bt, p, o_lat, dev_err, lse=lse, scale=SCALE)
+        api.mla_up_v(o_lat, w_uv, out, dev_err)
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream(dev).synchronize()
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
+    if api.mla_check(dev_err) != 0:
+        raise RuntimeError("device error word set during the end-to-end steps")
+
+    peaks = load_peaks()
+    step_s = ms_total / 1e3 / K
+    tokens = T * ws
+    value = tokens / step_s
+    dec_s = dec_avg / 1e3
+    t_flops = st["flops"] / (peaks["bf16_tflops"] * 1e12)
+    t_bytes = st["bytes"] / (peaks["hbm_gbs"] * 1e9)
+    bound = "tensor" if t_flops >= t_bytes else "hbm"
+    if bound == "tensor":
+        achieved, peak, unit = st["flops"] / dec_s / 1e12, peaks["bf16_tflops"], "TFLOP/s"
+    else:
+        achieved, peak, unit = st["bytes"] / dec_s / 1e9, peaks["hbm_gbs"], "GB/s"
+
+    line = {
+        "metric": METRIC,
+        "value": round(value, 1),
+        "unit": "tokens/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_total / K, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, N(0,1/512) weights, random page tables)",
+        "config": {
+            "workload": case.name,
+            "batch": case.B, "query_tokens_per_seq": int(case.q_lens.max()),
+            "context_tokens": int(case.seq_lens.max()), "rows": T, "heads": 128, "d_c": 512, "d_r": 64,
+            "page_size": 64, "kv_bytes_per_step": st["kv_bytes"],
+            "l2": "inputs larger than L2 (%.0f MB of KV streamed per step)" % (st["kv_bytes"] / 1e6),
+            "parallelism": f"replicas x{ws}" if ws > 1 else "single GPU",
+            "decode_clusters": plan.num_clusters, "split_rows": int(plan.info.num_split_rows),
+        },
+        "kv_tb_per_s": round(st["kv_bytes"] / dec_s / 1e12, 4),
+        "decode_us": round(dec_avg * 1e3, 2),
+        "roofline": {
+            "kernel": "mla_decode_paged (decode + combine launches)",
+            "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+            "frac": round(achieved / peak, 4), "traffic": None,
+            "peak_source": peaks["source"] + " (burst)",
+            "t_roof_us": round(max(t_flops, t_bytes) * 1e6, 2),
+            "frac_of_t_roof": round(max(t_flops, t_bytes) / dec_s, 4),
+            "algorithmic": {"flops": st["flops"], "bytes": st["bytes"]},
+        },
+        "e2e": {"value": round(tokens * K / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_budget)
+        line["cpu_baseline"].pop("seconds", None)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ reference arm: the CPU oracle
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    case = wl.workload(args.workload, seed=0)
+    import oracle
+    seq, pos = case.positions()
+    slots = oracle.slot_mapping(case.block_table, seq, pos)
+    cache = oracle.append(np.zeros((case.num_pages, 64, 576), dtype=np.float32), case.c_kv, case.k_r, slots)
+    rows_per_step = max(1, min(case.T, args.ref_rows))
+
+    def step(i):
+        rows = [(i * rows_per_step + k) % case.T for k in range(rows_per_step)]
+        oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table,
+                        case.seq_lens, case.q_lens, SCALE, rows=rows)
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    el = time.perf_counter() - t0
+    value = rows_per_step * args.steps / el
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)",
+        "config": {"workload": case.name, "batch": case.B, "rows": case.T},
+        "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{rows_per_step} query rows per step of {case.T}"},
+        "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=2, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=2, help="query rows per reference-arm step")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and args.impl == "mla":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_mla(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,269 @@
+/*
+ * mla.h — C ABI of the GB300 (sm_103a) absorbed paged MLA decode library.
+ *
+ * The operation is DeepSeek Multi-Head Latent Attention decode with matrix
+ * absorption over a paged latent KV cache, as described by:
+ *
+ *   [P1] "撕开 DeepSeek MLA 源码：C++ 与 TensorRT-LLM 算子设计优化全景与 TaoToken 实践"
+ *        (sheratonhq.com/news/189140): §1 the cached token (512-d latent c_KV
+ *        plus 64-d decoupled RoPE key k_R, 576 bf16 elements), §3 the
+ *        dimension constants and the plugin config (128 heads, content head
+ *        dim 128, page_size 64, absorption on, bf16 cache), §4 the absorbed
+ *        score (path B) and its scale, §5 the shared-memory and 16-byte
+ *        alignment pitfalls.
+ *   [P2] "DeepSeek的推理为什么比别人便宜一个数量级？——MLA、MoE、MTP技术拆解"
+ *        (leslieaibin.github.io): the MLA section (K = c·W_UK, V = c·W_UV),
+ *        the MTP section (two query tokens per decode step) and the closing
+ *        inference-flow summary (the new latent is appended every step).
+ *   [P3] bjbfmj.com/news/60700: the KV-byte formula and its calculator.
+ *
+ * Conventions
+ *   - Every call returns an mla_status; on failure mla_last_error() gives a
+ *     thread-local message.  Host-side validation runs before anything is
+ *     enqueued: a failing call enqueues nothing.
+ *   - Device buffers are owned by the caller.  Only the page pool (a host
+ *     object) is allocated by the library; no entry point allocates or frees
+ *     device memory.
+ *   - bf16 tensors are passed as untyped pointers to IEEE bfloat16 values
+ *     (uint16 bit patterns), row-major, contiguous, 16-byte aligned.
+ *   - Device work is enqueued asynchronously on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream) on the current CUDA device.
+ *   - Anomalies seen on the device (a page id or slot outside the pool, an
+ *     internal wait that exceeded its time limit) are OR-ed into the caller's
+ *     int32 device error word `dev_err` as MLA_DEVERR_* bits; the kernel then
+ *     skips or redirects the offending access instead of faulting.
+ *     mla_check() reads that word.
+ *   - Dimensions are fixed at the [P1] §3 constants: H = 128 heads, d_hc = 128,
+ *     d_c = 512, d_r = 64, page_size = 64.  Anything else is
+ *     MLA_ERR_UNSUPPORTED.
+ */
+#ifndef MLA_H_
+#define MLA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MLA_NUM_HEADS 128
+#define MLA_HEAD_DIM_C 128
+#define MLA_LATENT_DIM 512
+#define MLA_ROPE_DIM 64
+#define MLA_PAGE_SIZE 64
+#define MLA_TOKEN_ELEMS 576          /* d_c + d_r per cached token */
+#define MLA_PAGE_BYTES (64 * 576 * 2) /* 73 728 B: one 64-token bf16 page */
+
+typedef enum mla_status {
+  MLA_OK = 0,
+  MLA_ERR_INVALID_ARG = 1, /* null pointer, bad size or inconsistent arguments */
+  MLA_ERR_MISALIGNED = 2,  /* a device pointer is not 16-byte aligned ([P1] §5) */
+  MLA_ERR_UNSUPPORTED = 3, /* dimensions other than the [P1] §3 constants */
+  MLA_ERR_CUDA = 4,        /* a CUDA runtime/driver call failed */
+  MLA_ERR_DEVICE = 5,      /* mla_check: the device error word is non-zero */
+  MLA_ERR_TIMEOUT = 6,     /* mla_check: a kernel wait gave up (MLA_DEVERR_TIMEOUT) */
+  MLA_ERR_NO_SPACE = 7     /* the page pool has fewer free pages than requested */
+} mla_status;
+
+/* Bits of the device error word. */
+#define MLA_DEVERR_PAGE_OOB 1u /* block-table entry outside [0, num_pages): page 0 read instead */
+#define MLA_DEVERR_SLOT_OOB 2u /* append/gather slot outside the pool: that token skipped */
+#define MLA_DEVERR_TIMEOUT 4u  /* an mbarrier wait exceeded its limit; the kernel stopped early */
+#define MLA_DEVERR_PLAN 8u     /* the plan buffer is not a valid decode plan */
+
+/* Thread-local message of the last failing call (never NULL). */
+const char* mla_last_error(void);
+/* Static name of a status code. */
+const char* mla_status_string(mla_status s);
+/* Library ABI version (major * 100 + minor). */
+int32_t mla_version(void);
+
+/*
+ * Model dimensions of [P1] §3 (mla_config.h constants and the plugin JSON),
+ * plus the score scale 1/sqrt(d_hc + d_r) of [P1] §4.
+ */
+typedef struct mla_config {
+  int32_t num_heads;  /* 128 */
+  int32_t head_dim_c; /* 128 */
+  int32_t latent_dim; /* 512 */
+  int32_t rope_dim;   /* 64 */
+  int32_t page_size;  /* 64 */
+  float scale;        /* 1/sqrt(192) */
+} mla_config;
+
+mla_config mla_config_default(void);
+/* MLA_OK if `cfg` holds the supported dimensions and a finite positive scale;
+ * MLA_ERR_UNSUPPORTED for other dimensions; MLA_ERR_INVALID_ARG for NULL or a bad scale. */
+mla_status mla_config_validate(const mla_config* cfg);
+
+/*
+ * [P3] KV-byte formula: *out = layers * (dc + dr) * elem_bytes * tokens * seqs.
+ * MLA_ERR_INVALID_ARG if layers, dc, elem_bytes, tokens or seqs <= 0, dr < 0,
+ * `out` is NULL, or the product overflows uint64.
+ */
+mla_status mla_kv_bytes(int64_t layers, int64_t dc, int64_t dr, int64_t elem_bytes,
+                        int64_t tokens, int64_t seqs, uint64_t* out);
+
+/* ---------------------------------------------------------------------------
+ * Page pool and page tables (host objects).  Pages of 64 tokens, [P1] §3.
+ * ------------------------------------------------------------------------- */
+typedef struct mla_pool mla_pool;
+
+/* Create a pool of page ids [0, num_pages).  num_pages >= 1. */
+mla_status mla_pool_create(int32_t num_pages, mla_pool** out);
+/* Take `n` free page ids (lowest first) into page_ids_out[n].  MLA_ERR_NO_SPACE
+ * (nothing taken) if fewer than n are free. */
+mla_status mla_pool_alloc(mla_pool* pool, int32_t n, int32_t* page_ids_out);
+/* Return ids to the pool.  MLA_ERR_INVALID_ARG (nothing returned) if an id is
+ * out of range, not allocated, or repeated. */
+mla_status mla_pool_free(mla_pool* pool, const int32_t* ids, int32_t n);
+mla_status mla_pool_available(const mla_pool* pool, int32_t* out);
+void mla_pool_destroy(mla_pool* pool);
+
+/*
+ * Physical slot of token (seq_ids[i], positions[i]):
+ *   slots_out[i] = block_table[b * max_pages + pos / 64] * 64 + pos % 64.
+ * block_table is host int32 [batch, max_pages].  MLA_ERR_INVALID_ARG if a
+ * sequence id or page index is out of range or the table entry is negative.
+ */
+mla_status mla_slot_mapping(const int32_t* block_table, int32_t batch, int32_t max_pages,
+                            const int32_t* seq_ids, const int32_t* positions, int32_t n,
+                            int64_t* slots_out);
+
+/* ---------------------------------------------------------------------------
+ * Device steps
+ * ------------------------------------------------------------------------- */
+
+/* Zero-fill the pool kv_cache [num_pages, 64, 576] bf16 (every slot must hold
+ * finite values: a masked token still enters the P·V product with weight 0). */
+mla_status mla_cache_init(void* kv_cache, int64_t num_pages, void* stream);
+
+/*
+ * Step A1 — append ([P2] inference-flow summary: each step's new latent joins
+ * the cache; [P1] §3 page_size 64).  For i < n:
+ *   kv_cache[slots[i]] = [c_kv_new[i, 0:512] | k_r_new[i, 0:64]]
+ * c_kv_new bf16 [n, 512], k_r_new bf16 [n, 64], slots int64 [n] (device),
+ * kv_cache bf16 [num_pages * 64, 576].  A slot outside [0, num_pages*64) sets
+ * MLA_DEVERR_SLOT_OOB and that token is skipped.  n == 0 is a no-op.
+ */
+mla_status mla_kv_append(const void* c_kv_new, const void* k_r_new, const int64_t* slots,
+                         int32_t n, void* kv_cache, int64_t num_pages, int32_t* dev_err,
+                         void* stream);
+
+/*
+ * Copy the first n_tokens cached tokens of sequence b, in position order, to
+ * out bf16 [n_tokens, 576] (device).  A bit-exact view of what the decode
+ * kernel reads.  Bad page ids set MLA_DEVERR_PAGE_OOB and leave rows unwritten.
+ */
+mla_status mla_gather_paged(const void* kv_cache, int64_t num_pages, const int32_t* block_table,
+                            int32_t max_pages, int32_t b, int32_t n_tokens, void* out,
+                            int32_t* dev_err, void* stream);
+
+/*
+ * Step A2 — query absorption ([P1] §4 path B, einsum 'qhd,hdc->qhc'):
+ *   q_abs[t, h, c] = sum_d q_c[t, h, d] * W_UK[h, d, c]
+ * q_c bf16 [T, 128, 128], w_uk bf16 [128, 128, 512], q_abs bf16 [T, 128, 512];
+ * fp32 accumulation, one bf16 rounding.  T == 0 is a no-op.  dev_err (device
+ * int32, required) receives MLA_DEVERR_TIMEOUT if an internal wait gives up.
+ */
+mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t T, int32_t* dev_err,
+                        void* stream);
+
+/*
+ * Step A5 — V up-projection ([P2] MLA section, V = c·W_UV, applied after the
+ * attention by associativity):
+ *   out[t, h, d] = sum_c o_lat[t, h, c] * W_UV[h, c, d]
+ * o_lat bf16 [T, 128, 512], w_uv bf16 [128, 512, 128], out bf16 [T, 128, 128];
+ * fp32 accumulation.  T == 0 is a no-op.  dev_err as for mla_absorb_q.
+ */
+mla_status mla_up_v(const void* o_lat, const void* w_uv, void* out, int32_t T, int32_t* dev_err,
+                    void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Step A3 + A4 — absorbed paged attention with split-KV and combine.
+ *
+ * Rows: query token i of sequence b is row t = sum_{b'<b} q_lens[b'] + i.  Its
+ * sequence holds seq_lens[b] tokens (this step's q_lens[b] tokens already
+ * appended), it sits at position seq_lens[b] - q_lens[b] + i and sees the
+ * positions [0, that position] (causal within a multi-token query: the MTP
+ * two-token decode of [P2] and chunked prefill of [P1]).
+ *
+ * Per row t and head h, over the visible tokens j ([P1] §4 path B):
+ *   s_j   = (q_abs[t,h,:]·c_KV[j] + q_r[t,h,:]·k_R[j]) * scale
+ *   o_lat[t,h,:] = sum_j softmax(s)_j c_KV[j]          (bf16 out)
+ *   lse[t,h]     = ln sum_j exp(s_j)                    (fp32 out, optional)
+ * ------------------------------------------------------------------------- */
+
+/* Largest number of co-resident 2-CTA clusters the decode kernel can use on
+ * the current device (the split plan's parallelism). */
+mla_status mla_decode_max_clusters(int32_t* out);
+
+/* Bytes of the plan buffer for T rows and num_clusters clusters. */
+mla_status mla_decode_plan_bytes(int32_t T, int32_t num_clusters, size_t* bytes);
+
+/* Bytes of the split-KV workspace for num_clusters clusters (fp32 partial
+ * outputs and their log-sum-exp). */
+mla_status mla_decode_workspace_size(int32_t num_clusters, size_t* bytes);
+
+/* Summary of a plan, filled by the planner and passed back to mla_decode_paged. */
+typedef struct mla_plan_info {
+  uint32_t magic;         /* MLA_PLAN_MAGIC */
+  int32_t T;              /* rows */
+  int32_t B;              /* sequences */
+  int32_t num_clusters;   /* clusters launched (<= requested) */
+  int32_t num_segments;   /* (row, page range) work pieces */
+  int32_t num_partials;   /* split pieces written to the workspace */
+  int32_t num_split_rows; /* rows merged by the combine kernel */
+  int32_t max_pages_needed; /* block-table columns the plan reads */
+  int64_t total_tiles;    /* 64-token tiles over all rows */
+  size_t plan_bytes;      /* bytes of plan data written */
+} mla_plan_info;
+
+#define MLA_PLAN_MAGIC 0x504C4D41u /* "AMLP" */
+
+/*
+ * Build the split-KV schedule on the host into plan_host (plan_bytes from
+ * mla_decode_plan_bytes).  seq_lens/q_lens are host int32 [B] with
+ * seq_lens[b] >= 1 and 0 <= q_lens[b] <= seq_lens[b].  Work (64-token tiles of
+ * every row, in row order) is cut into equal contiguous ranges, one per
+ * cluster; a row cut by a range boundary is computed in pieces and merged by
+ * the combine step.
+ */
+mla_status mla_decode_plan_host(const int32_t* seq_lens, const int32_t* q_lens, int32_t B,
+                                int32_t num_clusters, void* plan_host, size_t plan_bytes,
+                                mla_plan_info* info);
+
+/* As mla_decode_plan_host, then copies the plan to plan_dev on `stream`. */
+mla_status mla_decode_plan(const int32_t* seq_lens_host, const int32_t* q_lens_host, int32_t B,
+                           int32_t num_clusters, void* plan_dev, size_t plan_bytes,
+                           mla_plan_info* info, void* stream);
+
+/*
+ * Run steps A3 and A4.
+ *   q_abs bf16 [T, 128, 512]; q_r bf16 [T, 128, 64];
+ *   kv_cache bf16 [num_pages, 64, 576]; block_table int32 [B, max_pages] (device);
+ *   plan_dev / info from mla_decode_plan; workspace of ws_bytes >=
+ *   mla_decode_workspace_size(info->num_clusters) (device, 16-B aligned);
+ *   o_lat bf16 [T, 128, 512] out; lse fp32 [T, 128] out or NULL;
+ *   dev_err int32 device word (required).
+ * Every cache slot read must hold finite values (see mla_cache_init).
+ */
+mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_cache,
+                            int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                            const void* plan_dev, const mla_plan_info* info, float scale,
+                            void* workspace, size_t ws_bytes, void* o_lat, float* lse,
+                            int32_t* dev_err, void* stream);
+
+/*
+ * Synchronise `stream`, read the device error word into *word_out (may be
+ * NULL) and map it: 0 -> MLA_OK, MLA_DEVERR_TIMEOUT set -> MLA_ERR_TIMEOUT,
+ * other bits -> MLA_ERR_DEVICE.  The word is not cleared.
+ */
+mla_status mla_check(void* stream, const int32_t* dev_err, int32_t* word_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_H_ */

@@ -1,0 +1,254 @@
+"""Python binding of the C ABI (include/mla.h), same names, torch tensors in.
+
+Only argument marshalling happens here: shapes, dtypes and devices are
+checked, raw pointers and the current CUDA stream are passed to libmla, and a
+non-zero status raises :class:`MlaError`.  Every step of the path runs in the
+library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from ._lib import lib, mla_plan_info
+
+H, D_HC, D_C, D_R, PAGE = 128, 128, 512, 64, 64
+D_QK = D_C + D_R
+
+STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_MISALIGNED", 3: "MLA_ERR_UNSUPPORTED",
+          4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE", 6: "MLA_ERR_TIMEOUT", 7: "MLA_ERR_NO_SPACE"}
+DEVERR_PAGE_OOB, DEVERR_SLOT_OOB, DEVERR_TIMEOUT, DEVERR_PLAN = 1, 2, 4, 8
+
+
+class MlaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+def _check(status: int) -> None:
+    if status != 0:
+        raise MlaError(status, lib().mla_last_error().decode())
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> C.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return C.c_void_p(stream.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None, cuda: bool = True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+# ------------------------------------------------------------------ host-only calls
+def mla_version() -> int:
+    return int(lib().mla_version())
+
+
+def mla_config_default():
+    return lib().mla_config_default()
+
+
+def mla_kv_bytes(layers: int, dc: int, dr: int, elem_bytes: int, tokens: int, seqs: int = 1) -> int:
+    out = C.c_uint64()
+    _check(lib().mla_kv_bytes(layers, dc, dr, elem_bytes, tokens, seqs, C.byref(out)))
+    return int(out.value)
+
+
+class MlaPool:
+    """Host page pool (mla_pool_*)."""
+
+    def __init__(self, num_pages: int):
+        self._h = C.c_void_p()
+        _check(lib().mla_pool_create(int(num_pages), C.byref(self._h)))
+
+    def alloc(self, n: int) -> np.ndarray:
+        ids = np.zeros(max(n, 1), dtype=np.int32)
+        _check(lib().mla_pool_alloc(self._h, int(n), ids.ctypes.data_as(C.POINTER(C.c_int32))))
+        return ids[:n]
+
+    def free(self, ids) -> None:
+        ids = np.ascontiguousarray(ids, dtype=np.int32)
+        _check(lib().mla_pool_free(self._h, ids.ctypes.data_as(C.POINTER(C.c_int32)), int(ids.size)))
+
+    def available(self) -> int:
+        out = C.c_int32()
+        _check(lib().mla_pool_available(self._h, C.byref(out)))
+        return int(out.value)
+
+    def close(self) -> None:
+        if self._h:
+            lib().mla_pool_destroy(self._h)
+            self._h = C.c_void_p()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def mla_slot_mapping(block_table: np.ndarray, seq_ids: np.ndarray, positions: np.ndarray) -> np.ndarray:
+    bt = np.ascontiguousarray(block_table, dtype=np.int32)
+    sid = np.ascontiguousarray(seq_ids, dtype=np.int32)
+    pos = np.ascontiguousarray(positions, dtype=np.int32)
+    n = int(sid.size)
+    out = np.zeros(max(n, 1), dtype=np.int64)
+    P32 = C.POINTER(C.c_int32)
+    _check(lib().mla_slot_mapping(bt.ctypes.data_as(P32), int(bt.shape[0]), int(bt.shape[1]),
+                                  sid.ctypes.data_as(P32), pos.ctypes.data_as(P32), n,
+                                  out.ctypes.data_as(C.POINTER(C.c_int64))))
+    return out[:n]
+
+
+# ------------------------------------------------------------------ device steps
+def mla_cache_init(kv_cache: torch.Tensor, stream=None) -> None:
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _check(lib().mla_cache_init(_ptr(kv_cache), kv_cache.shape[0], _stream(stream)))
+
+
+def mla_kv_append(c_kv_new, k_r_new, slots, kv_cache, dev_err, stream=None) -> None:
+    n = c_kv_new.shape[0]
+    _need(c_kv_new, "c_kv_new", torch.bfloat16, (n, D_C))
+    _need(k_r_new, "k_r_new", torch.bfloat16, (n, D_R))
+    _need(slots, "slots", torch.int64, (n,))
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_kv_append(_ptr(c_kv_new), _ptr(k_r_new), _ptr(slots), int(n), _ptr(kv_cache),
+                               kv_cache.shape[0], _ptr(dev_err), _stream(stream)))
+
+
+def mla_gather_paged(kv_cache, block_table, b: int, n_tokens: int, out, dev_err, stream=None) -> None:
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(out, "out", torch.bfloat16, (n_tokens, D_QK))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_gather_paged(_ptr(kv_cache), kv_cache.shape[0], _ptr(block_table), block_table.shape[1],
+                                  int(b), int(n_tokens), _ptr(out), _ptr(dev_err), _stream(stream)))
+
+
+def mla_absorb_q(q_c, w_uk, q_abs, dev_err, stream=None) -> None:
+    T = q_c.shape[0]
+    _need(q_c, "q_c", torch.bfloat16, (T, H, D_HC))
+    _need(w_uk, "w_uk", torch.bfloat16, (H, D_HC, D_C))
+    _need(q_abs, "q_abs", torch.bfloat16, (T, H, D_C))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_absorb_q(_ptr(q_c), _ptr(w_uk), _ptr(q_abs), int(T), _ptr(dev_err), _stream(stream)))
+
+
+def mla_up_v(o_lat, w_uv, out, dev_err, stream=None) -> None:
+    T = o_lat.shape[0]
+    _need(o_lat, "o_lat", torch.bfloat16, (T, H, D_C))
+    _need(w_uv, "w_uv", torch.bfloat16, (H, D_C, D_HC))
+    _need(out, "out", torch.bfloat16, (T, H, D_HC))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_up_v(_ptr(o_lat), _ptr(w_uv), _ptr(out), int(T), _ptr(dev_err), _stream(stream)))
+
+
+def mla_decode_max_clusters() -> int:
+    out = C.c_int32()
+    _check(lib().mla_decode_max_clusters(C.byref(out)))
+    return int(out.value)
+
+
+def mla_decode_plan_bytes(T: int, num_clusters: int) -> int:
+    out = C.c_size_t()
+    _check(lib().mla_decode_plan_bytes(int(T), int(num_clusters), C.byref(out)))
+    return int(out.value)
+
+
+def mla_decode_workspace_size(num_clusters: int) -> int:
+    out = C.c_size_t()
+    _check(lib().mla_decode_workspace_size(int(num_clusters), C.byref(out)))
+    return int(out.value)
+
+
+def mla_decode_plan_host(seq_lens: Sequence[int], q_lens: Sequence[int], num_clusters: int):
+    """Host planner only (no GPU): returns (plan int32 array, info)."""
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    T = int(ql.sum()) if ql.size else 0
+    nbytes = mla_decode_plan_bytes(T, num_clusters)
+    buf = np.zeros(nbytes // 4, dtype=np.int32)
+    info = mla_plan_info()
+    P32 = C.POINTER(C.c_int32)
+    _check(lib().mla_decode_plan_host(sl.ctypes.data_as(P32), ql.ctypes.data_as(P32), int(sl.size),
+                                      int(num_clusters), buf.ctypes.data_as(C.c_void_p), nbytes, C.byref(info)))
+    return buf, info
+
+
+@dataclass
+class DecodePlan:
+    """A plan on the device plus its host summary (mla_decode_plan)."""
+    plan: torch.Tensor          # int32 device buffer
+    info: mla_plan_info
+    workspace: torch.Tensor     # uint8 device buffer
+
+    @property
+    def num_clusters(self) -> int:
+        return int(self.info.num_clusters)
+
+
+def mla_decode_plan(seq_lens: Sequence[int], q_lens: Sequence[int], device=None, num_clusters: Optional[int] = None,
+                    stream=None) -> DecodePlan:
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    T = int(ql.sum()) if ql.size else 0
+    if num_clusters is None:
+        num_clusters = mla_decode_max_clusters()
+    nbytes = mla_decode_plan_bytes(T, num_clusters)
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    plan = torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.int32, device=device)
+    info = mla_plan_info()
+    P32 = C.POINTER(C.c_int32)
+    _check(lib().mla_decode_plan(sl.ctypes.data_as(P32), ql.ctypes.data_as(P32), int(sl.size), int(num_clusters),
+                                 _ptr(plan), nbytes, C.byref(info), _stream(stream)))
+    ws_bytes = mla_decode_workspace_size(num_clusters)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
+    return DecodePlan(plan=plan, info=info, workspace=ws)
+
+
+def mla_decode_paged(q_abs, q_r, kv_cache, block_table, plan: DecodePlan, o_lat, dev_err, lse=None,
+                     scale: float = 1.0 / (192 ** 0.5), stream=None) -> None:
+    T = q_abs.shape[0]
+    _need(q_abs, "q_abs", torch.bfloat16, (T, H, D_C))
+    _need(q_r, "q_r", torch.bfloat16, (T, H, D_R))
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    if kv_cache.dim() != 3 or tuple(kv_cache.shape[1:]) != (PAGE, D_QK):
+        raise ValueError("kv_cache must be [num_pages, 64, 576]")
+    _need(block_table, "block_table", torch.int32)
+    _need(o_lat, "o_lat", torch.bfloat16, (T, H, D_C))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (T, H))
+    if int(plan.info.T) != T:
+        raise ValueError(f"plan has {plan.info.T} rows, q_abs has {T}")
+    _check(lib().mla_decode_paged(_ptr(q_abs), _ptr(q_r), _ptr(kv_cache), kv_cache.shape[0], _ptr(block_table),
+                                  block_table.shape[1], _ptr(plan.plan), C.byref(plan.info), float(scale),
+                                  _ptr(plan.workspace), plan.workspace.numel(), _ptr(o_lat), _ptr(lse),
+                                  _ptr(dev_err), _stream(stream)))
+
+
+def mla_check(dev_err, stream=None) -> int:
+    """Synchronise and return the device error word; raises on a non-zero word."""
+    word = C.c_int32()
+    _check(lib().mla_check(_stream(stream), _ptr(dev_err), C.byref(word)))
+    return int(word.value)

@@ -1,0 +1,176 @@
+// Steps A2 (query absorption) and A5 (V up-projection) as per-head GEMMs on
+// the tcgen05 tensor cores:
+//   A2  q_abs[t, h, :] = q_c[t, h, :] · W_UK[h]     (K = 128 -> N = 512)
+//       ([P1] "撕开 DeepSeek MLA 源码…" §4 path B, einsum 'qhd,hdc->qhc')
+//   A5  out[t, h, :]   = o_lat[t, h, :] · W_UV[h]   (K = 512 -> N = 128)
+//       ([P2] "DeepSeek的推理为什么比别人便宜一个数量级？…", MLA section: V = c·W_UV)
+//
+// One CTA computes a 128-row tile of tokens for one head: D[128 x N] fp32 in
+// TMEM, A (activation rows, K-major) and W (row-major [K x N], read as an
+// MN-major operand) staged by TMA with 128-byte swizzle through a K-chunk
+// ring.  Rows past T are zero-filled by TMA and never stored.  For small T
+// the kernel streams the 16 MiB of weights once (HBM bound).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace gemm {
+
+using namespace mla::dev;
+
+template <int N, int K, int STAGES>
+struct Cfg {
+  static constexpr int kKCh = K / 64;
+  static constexpr int kABytes = 128 * 64 * 2;
+  static constexpr int kBBytes = 64 * N * 2;
+  static constexpr int kStage = kABytes + kBBytes;
+  static constexpr int kOffBar = STAGES * kStage;
+  static constexpr int kOffMisc = kOffBar + 8 * (2 * STAGES + 1);
+  static constexpr int kSmem = kOffMisc + 16 + 1024;
+  static constexpr int kMmaN = N < 256 ? N : 256;
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN, false, true);
+  static_assert(kSmem <= 232448, "head GEMM exceeds shared memory");
+};
+
+template <int N, int K, int STAGES>
+__global__ void __launch_bounds__(128, 1)
+    head_gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
+                     uint16_t* __restrict__ c, int32_t T, int32_t* err) {
+  using C = Cfg<N, K, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + C::kOffBar;
+  const uint32_t full0 = bars, empty0 = bars + 8 * STAGES, done = bars + 16 * STAGES;
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + C::kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + C::kOffMisc + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int m0 = blockIdx.x * 128;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_slot), N);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&a_map);
+      prefetch_tmap(&w_map);
+      int issued = 0;
+      for (int kc = 0; kc < C::kKCh; ++kc) {
+        const int st = kc % STAGES, use = kc / STAGES;
+        if (use > 0 && !wait_phase(empty0 + 8 * st, (use - 1) & 1, err, abort_flag)) break;
+        const uint32_t dst = base + st * C::kStage;
+        mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::kStage);
+        tma_load_3d(dst, &a_map, kc * 64, h, m0, full0 + 8 * st);
+#pragma unroll
+        for (int nb = 0; nb < N / 64; ++nb)
+          tma_load_3d(dst + C::kABytes + nb * 8192, &w_map, nb * 64, kc * 64, h, full0 + 8 * st);
+        ++issued;
+      }
+      for (int k = (issued > STAGES ? issued - STAGES : 0); k < issued; ++k)
+        wait_phase_drain(full0 + 8 * (k % STAGES), (k / STAGES) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int kc = 0; kc < C::kKCh; ++kc) {
+        const int st = kc % STAGES;
+        if (!wait_phase(full0 + 8 * st, (kc / STAGES) & 1, err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = base + st * C::kStage;
+        const uint32_t sb = sa + C::kABytes;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+#pragma unroll
+          for (int nh = 0; nh < N / C::kMmaN; ++nh)
+            mma_ss(tmem + nh * C::kMmaN, sdesc_sw128(sa + kk * 32, 16, 1024),
+                   sdesc_sw128(sb + nh * (C::kMmaN / 64) * 8192 + kk * 2048, 8192, 1024), C::kIdesc,
+                   (kc | kk) ? 1u : 0u);
+        tc_commit(empty0 + 8 * st);
+      }
+      tc_commit(done);  // also fires (after in-flight MMAs) when the loop stopped early
+      if (!ok) wait_phase_drain(done, 0);
+    }
+    __syncwarp();
+  }
+
+  // Epilogue: thread = output row (TMEM lane), all four warps.
+  bool w = wait_phase(done, 0, err, abort_flag) && !*abort_flag;
+  w = __all_sync(0xffffffffu, w);
+  tc_fence_after();
+  if (w) {
+    const int t = m0 + warp * 32 + lane;
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    uint4* dst = reinterpret_cast<uint4*>(c + ((size_t)t * 128 + h) * N);
+#pragma unroll 1
+    for (int col = 0; col < N; col += 32) {
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32_sync(tl + col, r);
+      if (t < T) {
+#pragma unroll
+        for (int v = 0; v < 4; ++v)
+          dst[col / 8 + v] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
+                                        pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                        pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                        pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, N);
+  }
+}
+
+template <int N, int K, int STAGES>
+cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c, int32_t T, int32_t* err,
+                cudaStream_t stream) {
+  using C = Cfg<N, K, STAGES>;
+  auto* kern = head_gemm_kernel<N, K, STAGES>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((T + 127) / 128, 128);
+  kern<<<grid, 128, C::kSmem, stream>>>(a_map, w_map, c, T, err);
+  return cudaGetLastError();
+}
+
+}  // namespace gemm
+
+cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
+                             int32_t T, int32_t* err, cudaStream_t stream) {
+  if (kind == HeadGemm::kAbsorbQ) return gemm::run<512, 128, 2>(a_map, w_map, c, T, err, stream);
+  return gemm::run<128, 512, 4>(a_map, w_map, c, T, err, stream);
+}
+
+}  // namespace mla

@@ -1,0 +1,89 @@
+// Internal interface between the C-ABI entry points (mla_api.cu) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+namespace mla {
+
+// Layout of the decode plan (int32 words).  Written by the host planner,
+// read by the decode and combine kernels.
+//   [0] magic  [1] T  [2] B  [3] num_clusters  [4] num_segments
+//   [5] num_partials  [6] num_split_rows  [7] max_pages_needed
+//   [8..15] reserved
+//   seg_off   at kPlanHeader, num_clusters + 1 entries
+//   segments  at seg_base, num_segments x 8: {row, b, page_begin, page_end,
+//             visible, out_slot (-1 = final), 0, 0}
+//   split rows at split_base, num_split_rows x 4: {row, slot_begin, n_slots, 0}
+constexpr int kPlanHeader = 16;
+constexpr int kSegWords = 8;
+constexpr int kSplitWords = 4;
+
+struct PlanLayout {
+  int64_t seg_off;  // word offsets
+  int64_t seg_base;
+  int64_t split_base;
+  int64_t words;
+};
+PlanLayout plan_layout(int64_t num_clusters, int64_t num_segments, int64_t num_split_rows);
+// Upper bounds used to size the plan buffer.
+inline int64_t plan_max_segments(int64_t T, int64_t num_clusters) { return T + num_clusters; }
+inline int64_t plan_max_split_rows(int64_t T, int64_t num_clusters) {
+  return T < num_clusters ? T : num_clusters;
+}
+inline int64_t plan_max_partials(int64_t num_clusters) { return 2 * num_clusters; }
+
+struct DecodeArgs {
+  const uint16_t* q_abs;  // bf16 [T, 128, 512]
+  const uint16_t* q_r;    // bf16 [T, 128, 64]
+  const int32_t* block_table;
+  int32_t max_pages;
+  int32_t pad_;
+  int64_t num_pages;
+  const int32_t* seg_off;
+  const int32_t* segs;
+  float scale_log2;  // scale * log2(e)
+  int32_t pad2_;
+  uint16_t* o_lat;     // bf16 [T, 128, 512]
+  float* lse;          // [T, 128] or null
+  float* part_o;       // fp32 [partials, 128, 512]
+  float* part_lse;     // fp32 [partials, 128] (log2 domain)
+  int32_t* dev_err;
+  // plan summary, used to validate every segment before any access
+  int32_t T;
+  int32_t B;
+  int32_t num_segments;
+  int32_t num_partials;
+};
+
+struct CombineArgs {
+  const int32_t* split_rows;
+  const float* part_o;
+  const float* part_lse;
+  uint16_t* o_lat;
+  float* lse;
+  int32_t T;
+  int32_t num_partials;
+  int32_t* dev_err;
+};
+
+int decode_smem_bytes();
+int decode_threads();
+cudaError_t decode_max_clusters(int* out);
+cudaError_t launch_decode(const CUtensorMap& kv_map, const DecodeArgs& args, int num_clusters, cudaStream_t stream);
+cudaError_t launch_combine(const CombineArgs& args, int num_split_rows, cudaStream_t stream);
+
+cudaError_t launch_kv_append(const uint16_t* c_kv_new, const uint16_t* k_r_new, const int64_t* slots, int32_t n,
+                             uint16_t* kv_cache, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                          int32_t b, int32_t n_tokens, uint16_t* out, int32_t* dev_err, cudaStream_t stream);
+
+// Per-head GEMM C[t, h, :] = A[t, h, :] · W[h] (bf16 in, fp32 accumulate, bf16 out).
+enum class HeadGemm { kAbsorbQ, kUpV };
+cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
+                             int32_t T, int32_t* err, cudaStream_t stream);
+
+}  // namespace mla
