@@ -179,7 +179,7 @@ def run_mla(args):
     dev = torch.device("cuda", local)
     stream = torch.cuda.current_stream(dev)
 
-    case = wl.workload(args.workload, seed=0)
+    case = wl.workload(args.workload, seed=0, batch=args.batch)
     st = workload_stats(case)
     T = case.T
 
@@ -389,6 +389,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=2, choices=sorted(wl.WORKLOADS))
+    ap.add_argument("--batch", type=int, default=None, help="keep only the first N sequences (profiling cases)")
     ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -5,7 +5,7 @@
 //   s_j = (q_abs[t,h]·c_KV[j] + q_R[t,h]·k_R[j]) · scale,
 //   o_lat[t,h] = Σ_j softmax(s)_j · c_KV[j],   lse[t,h] = ln Σ_j e^{s_j}.
 //
-// GB300 design (one CTA pair = one 2-CTA cluster per work range):
+// GB300 design (one 2-CTA cluster per work range):
 //  * The fp32 latent accumulator O[128 heads × 512] is exactly one SM's TMEM
 //    (128 lanes × 512 columns), so the pair splits the latent columns: CTA r
 //    owns O[:, 256r : 256r+256) and streams only its columns of each 64-token
@@ -13,17 +13,27 @@
 //  * The score contraction (576 = 9 chunks of 64) is split the same way: CTA 0
 //    takes latent chunks 0-3, CTA 1 latent chunks 4-7 plus the RoPE chunk.  Each
 //    CTA computes a partial S = Q_r·K_r^T (tcgen05, M = 128 heads, N = 64
-//    tokens, A = Q from TMEM, B = the page tile in shared memory) and the two
-//    partials are exchanged through distributed shared memory (st.async into
-//    the peer, completing on the peer's mbarrier).  Both CTAs then hold the
-//    same full S (fp32 addition is commutative), run the same online softmax,
-//    write P (bf16) into TMEM and accumulate O_r += P·V_r (tcgen05, N = 256,
-//    B = the same page tile read as an MN-major operand).
+//    tokens, A = Q from TMEM, B = the page tile in shared memory).  The
+//    partials, scaled to log2 units, are exchanged as fp16 (each warp stages
+//    its rows in shared memory; one bulk copy per warp pushes them into the
+//    peer CTA, completing on the peer's mbarrier).  Both CTAs add the two
+//    rounded halves in the same order-free way, so they hold bit-identical S,
+//    run the same online softmax, write P (bf16) into TMEM and accumulate
+//    O_r += P·V_r (tcgen05, N = 256, B = the same page tile read as an
+//    MN-major operand).
+//  * Software pipeline: the scores of tile g+1 are read and pushed to the peer
+//    before tile g's softmax runs, so the exchange overlaps the softmax; the
+//    MMA warp issues each QK^T as soon as its inputs are ready, independently
+//    of the P·V order.
+//  * Two softmax warpgroups split the 64 tokens of a tile (32 each, thread =
+//    head row = TMEM lane); the row maximum is combined through shared memory.
 //  * Online softmax with lazy rescaling: the running reference max only moves
 //    when a tile's max exceeds it by more than 8 (log2 units), so P stays
 //    below 256 and O in TMEM is rescaled only on those rare tiles.
 //  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + MMA issue,
-//    warps 2-5 softmax/epilogue (thread = head row = TMEM lane).
+//    warps 2-9 softmax/epilogue, warp 10 tells the peer when a receive buffer
+//    has been read (a cluster-scope release arrive stalls its thread for
+//    hundreds of cycles, so it is kept off the softmax warps).
 //  * Work: the plan cuts all rows' 64-token tiles into equal contiguous ranges,
 //    one per cluster; a row cut by a boundary is written as fp32 partials
 //    (normalised O and log2-sum-exp) and merged by the combine kernel.
@@ -47,16 +57,28 @@ constexpr int kChunkBytes = kPage * kChunk * 2;           // [64 tokens x 64] bf
 constexpr int kMaxQKChunks = 5;
 constexpr int kStageBytes = kMaxQKChunks * kChunkBytes;   // 40 KB
 constexpr int kStages = 4;
-constexpr int kXBytes = kH * kPage * 4;                   // one CTA's fp32 partial S
+constexpr int kXBytes = kH * kPage * 2;                   // one CTA's fp16 partial S (16 KB)
+constexpr int kXHalf = kXBytes / 2;                       // one warpgroup's 32 tokens
+constexpr int kXWarp = kXHalf / 4;                        // one warp's 32 rows (2 KB)
+
+// Shared memory: a small region (barriers, row reductions, flags) at the
+// start, then the 1024-byte aligned region (page ring, 2 send + 2 receive
+// exchange buffers).
+constexpr int kNumBars = 32;
+constexpr int kSmallBar = 0;
+constexpr int kSmallRed = kSmallBar + 8 * kNumBars;       // float [2 parity][2 wg][128]
+constexpr int kSmallMisc = kSmallRed + 2 * 2 * kH * 4;
+constexpr int kSmallBytes = kSmallMisc + 64;
 constexpr int kOffKV = 0;
-constexpr int kOffX = kStages * kStageBytes;
-constexpr int kOffBar = kOffX + 2 * kXBytes;
-constexpr int kOffMisc = kOffBar + 8 * 32;
-constexpr int kSmemBytes = kOffMisc + 64 + 1024;          // + slack to align the base to 1024 B
-static_assert(kSmemBytes <= 232448, "decode kernel exceeds 227 KB of shared memory");
+constexpr int kOffSend = kStages * kStageBytes;
+constexpr int kOffRecv = kOffSend + 2 * kXBytes;
+constexpr int kAlignedBytes = kOffRecv + 2 * kXBytes;
+constexpr int kSmemBytes = 232448;                        // the per-block maximum
+static_assert(kSmallBytes + kAlignedBytes <= kSmemBytes, "shared memory layout does not fit");
 
 constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320, kColP = 480, kTmemCols = 512;
-constexpr int kThreads = 192;
+constexpr int kThreads = 352;
+constexpr uint32_t kSoftmaxThreads = 256;
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
@@ -70,23 +92,55 @@ enum : int {
   B_O_DONE,
   B_Q_READY,
   B_O_FREE,
-  B_X_FULL0,
+  B_X_FULL0,   // receive buffer 0 / 1 filled by the peer
   B_X_FULL1,
+  B_X_EMPTY0,  // the peer has read what this CTA pushed into its buffer 0 / 1
+  B_X_EMPTY1,
+  B_X_READ0,   // this CTA has read receive buffer 0 / 1 (local, for the signaller)
+  B_X_READ1,
   B_DRAIN,
+  B_GROUP,
   B_COUNT
 };
-static_assert(B_COUNT <= 32, "barrier area too small");
+static_assert(B_COUNT <= kNumBars, "barrier area too small");
+
+// Walks the 64-token tiles of a cluster's segments in order.
+struct TileCursor {
+  const int32_t* segs;
+  int s, s_end, pg, pb, pe;
+  __device__ __forceinline__ void init(const int32_t* sg, int sb, int se) {
+    segs = sg;
+    s = sb;
+    s_end = se;
+    if (s < s_end) load();
+  }
+  __device__ __forceinline__ void load() {
+    pb = segs[8 * s + 2];
+    pe = segs[8 * s + 3];
+    pg = pb;
+  }
+  __device__ __forceinline__ bool valid() const { return s < s_end; }
+  __device__ __forceinline__ bool first() const { return pg == pb; }
+  __device__ __forceinline__ bool last() const { return pg == pe - 1; }
+  __device__ __forceinline__ void next() {
+    if (++pg == pe) {
+      ++s;
+      if (s < s_end) load();
+    }
+  }
+};
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
-  extern __shared__ uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + kOffMisc);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc + 8);
-  int32_t* seg_range = reinterpret_cast<int32_t*>(gbase + kOffMisc + 16);
-  const uint32_t bars = base + kOffBar;
+  const uint32_t bars = raw + kSmallBar;
+  float* red = reinterpret_cast<float*>(smem_raw + kSmallRed);
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem_raw + kSmallMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + kSmallMisc + 8);
+  int32_t* seg_range = reinterpret_cast<int32_t*>(smem_raw + kSmallMisc + 16);
+  const uint32_t base = (raw + kSmallBytes + 1023u) & ~1023u;
+  const bool layout_fits = base + kAlignedBytes <= raw + kSmemBytes;
 #define BAR(i) (bars + 8u * (uint32_t)(i))
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -104,21 +158,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(BAR(B_KV_EMPTY + i), 1);
     }
     mbar_init(BAR(B_S_FULL), 1);
-    mbar_init(BAR(B_S_FREE), 128);
-    mbar_init(BAR(B_P_FULL), 128);
+    mbar_init(BAR(B_S_FREE), kSoftmaxThreads);
+    mbar_init(BAR(B_P_FULL), kSoftmaxThreads);
     mbar_init(BAR(B_O_DONE), 1);
-    mbar_init(BAR(B_Q_READY), 128);
-    mbar_init(BAR(B_O_FREE), 128);
+    mbar_init(BAR(B_Q_READY), kSoftmaxThreads);
+    mbar_init(BAR(B_O_FREE), kSoftmaxThreads);
     mbar_init(BAR(B_X_FULL0), 1);
     mbar_init(BAR(B_X_FULL1), 1);
+    mbar_init(BAR(B_X_EMPTY0), 1);
+    mbar_init(BAR(B_X_EMPTY1), 1);
+    mbar_init(BAR(B_X_READ0), 1);
+    mbar_init(BAR(B_X_READ1), 1);
     mbar_init(BAR(B_DRAIN), 1);
+    mbar_init(BAR(B_GROUP), kSoftmaxThreads);
     fence_mbar_init();
   }
-  if (threadIdx.x == 32) {
-    // Validate this cluster's plan range; an inconsistent plan is skipped whole
-    // (by every role alike) and reported instead of being dereferenced.
+  if (threadIdx.x == 64) {
+    // Validate this cluster's plan range; an inconsistent plan (or a shared
+    // memory window that cannot hold the aligned layout) is skipped whole, by
+    // every role alike, and reported instead of being dereferenced.
     int32_t sb = a.seg_off[cid], se = a.seg_off[cid + 1];
-    bool good = sb >= 0 && se >= sb && se <= a.num_segments;
+    bool good = layout_fits && sb >= 0 && se >= sb && se <= a.num_segments;
     for (int s = sb; good && s < se; ++s) {
       const int32_t* sg = a.segs + 8 * s;
       const int32_t row = sg[0], b = sg[1], pb = sg[2], pe = sg[3], vis = sg[4], slot = sg[5];
@@ -141,7 +201,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // the peer's barriers exist before any st.async reaches them
+  cluster_sync();  // the peer's barriers exist before any copy or arrive reaches them
   const uint32_t tmem = *tmem_slot;
 
   const int s_begin = seg_range[0];
@@ -158,7 +218,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t* bt = a.block_table + (int64_t)b * a.max_pages;
         for (int pg = pb; pg < pe; ++pg) {
           const uint32_t st = g % kStages, use = g / kStages;
-          if (use > 0 && !wait_phase(BAR(B_KV_EMPTY + st), (use - 1) & 1u, err, abort_flag)) {
+          if (use > 0 && !wait_phase<false, true>(BAR(B_KV_EMPTY + st), (use - 1) & 1u, err, abort_flag)) {
             ok = false;
             break;
           }
@@ -181,258 +241,350 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issue
+    // Two in-order streams, QK^T(t) and P·V(t); whichever is ready is issued,
+    // QK^T first, so the tensor pipe runs the next scores while the softmax
+    // of the current tile is still in flight.
     if (lane == 0) {
-      uint32_t g = 0;
-      int segi = 0;
-      bool ok = true, pend = false, pend_first = false;
-      uint32_t pend_g = 0;
-      int pend_seg = 0;
-      auto issue_pv = [&](uint32_t gp, bool first, int si) -> bool {
-        if (!wait_phase(BAR(B_P_FULL), gp & 1u, err, abort_flag)) return false;
-        if (first && !wait_phase(BAR(B_O_FREE), (uint32_t)si & 1u, err, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t v = base + kOffKV + (gp % kStages) * kStageBytes;
-        // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
-        // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, sdesc_sw128(v + kk * 2048, 8192, 1024), kIdescPV,
-                 (first && kk == 0) ? 0u : 1u);
-        tc_commit(BAR(B_KV_EMPTY + gp % kStages));
-        tc_commit(BAR(B_O_DONE));
-        return true;
-      };
-      for (int s = s_begin; s < s_end && ok; ++s, ++segi) {
-        const int32_t* sg = a.segs + 8 * s;
-        const int pb = sg[2], pe = sg[3];
-        if (!wait_phase(BAR(B_Q_READY), (uint32_t)segi & 1u, err, abort_flag)) {
-          ok = false;
-          break;
+      TileCursor cq, cp;
+      cq.init(a.segs, s_begin, s_end);
+      cp.init(a.segs, s_begin, s_end);
+      uint32_t tq = 0, tp = 0, spins = 0;
+      uint64_t t_stall = 0;
+      while (cp.valid()) {
+        bool progressed = false;
+        if (cq.valid()) {
+          const uint32_t st = tq % kStages;
+          const bool ready = mbar_test_wait(BAR(B_KV_FULL + st), (tq / kStages) & 1u) &&
+                             (tq == 0 || mbar_test_wait(BAR(B_S_FREE), (tq - 1) & 1u)) &&
+                             (!cq.first() || mbar_test_wait(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u));
+          if (ready) {
+            tc_fence_after();
+            const uint32_t kv = base + kOffKV + st * kStageBytes;
+            // S_partial[128 x 64] = Q_r[128 x 64*nq] · K_r^T, K-major, 16 per step.
+            for (int i = 0; i < nq; ++i)
+              for (int kk = 0; kk < 4; ++kk)
+                mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8,
+                       sdesc_sw128(kv + i * kChunkBytes + kk * 32, 16, 1024), kIdescQK, (i | kk) ? 1u : 0u);
+            tc_commit(BAR(B_S_FULL));
+            cq.next();
+            ++tq;
+            progressed = true;
+          }
         }
-        for (int pg = pb; pg < pe; ++pg) {
-          const uint32_t st = g % kStages;
-          if (!wait_phase(BAR(B_KV_FULL + st), (g / kStages) & 1u, err, abort_flag) ||
-              (g > 0 && !wait_phase(BAR(B_S_FREE), (g - 1) & 1u, err, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kv = base + kOffKV + st * kStageBytes;
-          // S_partial[128 x 64] = Q_r[128 x 64*nq] · K_r^T, K-major, 16 per step.
-          for (int i = 0; i < nq; ++i)
+        if (!progressed && tp < tq) {
+          const bool first = cp.first();
+          const bool ready = mbar_test_wait(BAR(B_P_FULL), tp & 1u) &&
+                             (!first || mbar_test_wait(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u));
+          if (ready) {
+            tc_fence_after();
+            const uint32_t v = base + kOffKV + (tp % kStages) * kStageBytes;
+            // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
+            // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
             for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8,
-                     sdesc_sw128(kv + i * kChunkBytes + kk * 32, 16, 1024), kIdescQK, (i | kk) ? 1u : 0u);
-          tc_commit(BAR(B_S_FULL));
-          if (pend && !issue_pv(pend_g, pend_first, pend_seg)) {
-            ok = false;
-            break;
+              mma_ts(tmem + kColO, tmem + kColP + kk * 8, sdesc_sw128(v + kk * 2048, 8192, 1024), kIdescPV,
+                     (first && kk == 0) ? 0u : 1u);
+            tc_commit(BAR(B_KV_EMPTY + tp % kStages));
+            tc_commit(BAR(B_O_DONE));
+            cp.next();
+            ++tp;
+            progressed = true;
           }
-          pend = true;
-          pend_g = g;
-          pend_first = (pg == pb);
-          pend_seg = segi;
-          ++g;
+        }
+        if (progressed) {
+          spins = 0;
+        } else {
+          __nanosleep(20);  // poll gently: this SM sub-partition also runs softmax warps
+          if (spins == 0) t_stall = globaltimer();
+          if ((++spins & 255u) == 0u) {
+            if (*abort_flag) break;
+            if (globaltimer() - t_stall > kWaitLimitNs) {
+              atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              break;
+            }
+          }
         }
       }
-      if (ok && pend) ok = issue_pv(pend_g, pend_first, pend_seg);
       // Every MMA must be finished before TMEM is released.
       tc_commit(BAR(B_DRAIN));
       wait_phase_drain(BAR(B_DRAIN), 0);
     }
     __syncwarp();
+  } else if (warp == 10) {
+    // ---------------------------------------------------------------- signaller
+    if (lane == 0) {
+      uint32_t G = 0;
+      for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
+      for (uint32_t g = 0; g < G; ++g) {
+        const uint32_t xb = g & 1u;
+        if (!wait_phase<false, true>(BAR(B_X_READ0 + xb), (g >> 1) & 1u, err, abort_flag)) break;
+        mbar_arrive_remote(mapa(BAR(B_X_EMPTY0 + xb), peer));
+      }
+    }
+    __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
-    const int q4 = warp & 3;
-    const int h = q4 * 32 + lane;
-    const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);  // this warp's TMEM lane quarter
-    const uint32_t xrow = base + kOffX + (uint32_t)h * 256u;
-    const uint32_t swz = (uint32_t)(h & 7);
-    const float scale_log2 = a.scale_log2;
+    const int sw = warp - 2;                 // 0..7
+    const int wg = sw >> 2;                  // warpgroup: tokens [32 wg, 32 wg + 32) of each tile
+    const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
+    const int h = q4 * 32 + lane;            // head row = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
+    const uint32_t swz = (uint32_t)((h >> 1) & 3);
+    const uint32_t row_off = (uint32_t)(wg * kXHalf + h * 64);
+    const uint32_t warp_off = (uint32_t)(wg * kXHalf + q4 * kXWarp);
+    const bool leader = (sw == 0 && lane == 0);
+    const float c2 = a.scale_log2;
+    // Barrier over the 256 softmax threads with a bounded wait (a hardware
+    // named barrier would hang if one warp stopped early on a timeout).
+    uint32_t grp = 0;
+    auto group_sync = [&]() -> bool {
+      mbar_arrive(BAR(B_GROUP));
+      const bool w = wait_phase(BAR(B_GROUP), grp & 1u, err, abort_flag);
+      ++grp;
+      return __all_sync(0xffffffffu, w);
+    };
     __syncwarp();
 
+    // Q_r of a row into TMEM: this warpgroup's chunks (2 latent chunks, plus the
+    // RoPE chunk for CTA 1's first warpgroup), all loads issued before any store.
     auto load_q = [&](int s) {
       const int row = a.segs[8 * s];
-      const uint4* src = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256);
-      uint32_t r[32];
+      const uint4* lat = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256) + wg * 16;
+      const bool rope = (rank == 1 && wg == 0);
+      uint4 v[24];
 #pragma unroll
-      for (int part = 0; part < 4; ++part) {
+      for (int j = 0; j < 16; ++j) v[j] = __ldg(lat + j);
+      if (rope) {
+        const uint4* rp = reinterpret_cast<const uint4*>(a.q_r + ((size_t)row * kH + h) * kDR);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = __ldg(src + part * 8 + v);
-          r[4 * v] = x.x;
-          r[4 * v + 1] = x.y;
-          r[4 * v + 2] = x.z;
-          r[4 * v + 3] = x.w;
-        }
-        tmem_st32(tl + kColQ + part * 32, r);
+        for (int j = 0; j < 8; ++j) v[16 + j] = __ldg(rp + j);
       }
-      if (rank == 1) {
-        const uint4* srr = reinterpret_cast<const uint4*>(a.q_r + ((size_t)row * kH + h) * kDR);
 #pragma unroll
-        for (int v = 0; v < 8; ++v) {
-          const uint4 x = __ldg(srr + v);
-          r[4 * v] = x.x;
-          r[4 * v + 1] = x.y;
-          r[4 * v + 2] = x.z;
-          r[4 * v + 3] = x.w;
+      for (int ci = 0; ci < 3; ++ci) {
+        if (ci == 2 && !rope) break;
+        uint32_t r[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          r[4 * j] = v[ci * 8 + j].x;
+          r[4 * j + 1] = v[ci * 8 + j].y;
+          r[4 * j + 2] = v[ci * 8 + j].z;
+          r[4 * j + 3] = v[ci * 8 + j].w;
         }
-        tmem_st32(tl + kColQ + 128, r);
+        const int chunk = ci < 2 ? wg * 2 + ci : 4;
+        tmem_st32(tl + kColQ + chunk * 32, r);
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(BAR(B_Q_READY));
     };
 
+    // Read this warpgroup's 32 columns of tile t's partial scores, free the S
+    // buffer, load the next segment's Q if tile t ends a segment, and push the
+    // fp16 log2-scaled partial to the peer.  `own` keeps the rounded values.
+    auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[16]) -> bool {
+      bool w = wait_phase(BAR(B_S_FULL), t & 1u, err, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) return false;
+      tc_fence_after();
+      uint32_t r[32];
+      tmem_ld32_sync(tl + kColS + wg * 32, r);
+      tc_fence_before();
+      mbar_arrive(BAR(B_S_FREE));
+      if (c.last() && c.s + 1 < c.s_end) load_q(c.s + 1);  // every QK^T of this segment is done
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        own[j] = pack_f16x2_sat(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
+      const uint32_t xb = t & 1u;
+      if (t >= 2) {  // the peer has read what was pushed into this buffer two tiles ago
+        w = wait_phase<true>(BAR(B_X_EMPTY0 + xb), ((t - 2) >> 1) & 1u, err, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) return false;
+      }
+      const uint32_t send = base + kOffSend + xb * kXBytes;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        st_shared_v4(send + row_off + (((uint32_t)k ^ swz) << 4), own[4 * k], own[4 * k + 1], own[4 * k + 2],
+                     own[4 * k + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0)
+        bulk_copy_to_peer(mapa(base + kOffRecv + xb * kXBytes + warp_off, peer), send + warp_off, (uint32_t)kXWarp,
+                          mapa(BAR(B_X_FULL0 + xb), peer));
+      return true;
+    };
+
+    // tile count of this cluster
+    uint32_t G = 0;
+    for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
+
     mbar_arrive(BAR(B_O_FREE));  // O is free for the first segment
-    if (s_begin < s_end) load_q(s_begin);
-    uint32_t g = 0;
+    TileCursor cf;               // the tile being finished
+    cf.init(a.segs, s_begin, s_end);
+    uint32_t own_cur[16], own_nxt[16];
     bool ok = true;
-    for (int s = s_begin; s < s_end && ok; ++s) {
-      const int32_t* sg = a.segs + 8 * s;
-      const int row = sg[0], pb = sg[2], pe = sg[3], vis = sg[4], slot = sg[5];
-      float m = -INFINITY, l = 0.f;
-      for (int pg = pb; pg < pe; ++pg, ++g) {
-        bool w = wait_phase(BAR(B_S_FULL), g & 1u, err, abort_flag);
+    if (G > 0) {
+      load_q(s_begin);
+      ok = fetch_push(0, cf, own_cur);
+    }
+    float m = -INFINITY, l = 0.f;
+    for (uint32_t g = 0; g < G && ok; ++g) {
+      TileCursor cn = cf;
+      cn.next();
+      if (g + 1 < G && !fetch_push(g + 1, cn, own_nxt)) {
+        ok = false;
+        break;
+      }
+      const int32_t* sg = a.segs + 8 * cf.s;
+      const int pg = cf.pg, vis = sg[4];
+
+      // ---- tile g: the peer's half, full scores (log2 units)
+      const uint32_t xb = g & 1u;
+      if (leader) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
+      bool w = wait_phase<true>(BAR(B_X_FULL0 + xb), (g >> 1) & 1u, err, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+        break;
+      }
+      const uint32_t recv = base + kOffRecv + xb * kXBytes + row_off;
+      float sv[32];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        const float4 v = ld_shared_v4(recv + (((uint32_t)k ^ swz) << 4));
+        const uint32_t pv[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
+                                __float_as_uint(v.w)};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 o2 = unpack_f16x2(own_cur[4 * k + i]);
+          const float2 p2 = unpack_f16x2(pv[i]);
+          sv[8 * k + 2 * i] = o2.x + p2.x;
+          sv[8 * k + 2 * i + 1] = o2.y + p2.y;
+        }
+      }
+
+      // ---- causal/length mask, row max over both warpgroups
+      const int valid = vis - pg * kPage - wg * 32;
+      if (valid < 32) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+          if (j >= valid) sv[j] = -INFINITY;
+      }
+      float mx[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(sv[4 * j], sv[4 * j + 1]), fmaxf(sv[4 * j + 2], sv[4 * j + 3]));
+      const float mloc =
+          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+      float* redp = red + xb * (2 * kH);
+      redp[wg * kH + h] = mloc;
+      if (!group_sync()) {
+        ok = false;
+        break;
+      }
+      if (leader) mbar_arrive(BAR(B_X_READ0 + xb));  // all have read this buffer; warp 10 tells the peer
+      const float mt = fmaxf(mloc, redp[(wg ^ 1) * kH + h]);
+
+      float factor = 1.f;
+      bool resc = false;
+      if (cf.first()) {
+        m = mt;
+        l = 0.f;
+      } else if (mt > m + 8.f) {
+        factor = ex2_approx(m - mt);
+        m = mt;
+        l *= factor;
+        resc = true;
+      }
+      // P (single TMEM buffer) and an O rescale both need P·V of the previous tile done.
+      if (g > 0) {
+        w = wait_phase(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float sv[64];
-        {
-          uint32_t r[32];
-          tmem_ld32_sync(tl + kColS, r);
+      }
+      if (__any_sync(0xffffffffu, resc)) {
+#pragma unroll 1
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t o[32];
+          tmem_ld32_sync(tl + kColO + wg * 128 + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) sv[i] = __uint_as_float(r[i]);
-          tmem_ld32_sync(tl + kColS + 32, r);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) sv[32 + i] = __uint_as_float(r[i]);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
+          tmem_st32(tl + kColO + wg * 128 + c, o);
         }
-        tc_fence_before();
-        mbar_arrive(BAR(B_S_FREE));
-        if (pg == pe - 1 && s + 1 < s_end) load_q(s + 1);  // all QK of this segment are done
-
-        // ---- exchange partial scores with the peer CTA
-        const uint32_t xb = g & 1u;
-        if (h == 0) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
-        const uint32_t my_row = xrow + xb * (uint32_t)kXBytes;
-        const uint32_t rrow = mapa(my_row, peer);
-        const uint32_t rbar = mapa(BAR(B_X_FULL0 + xb), peer);
+      }
+      uint32_t pk[16];
+      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int k = 0; k < 16; ++k)
-          st_async_v4(rrow + (((uint32_t)k ^ swz) << 4), sv[4 * k], sv[4 * k + 1], sv[4 * k + 2], sv[4 * k + 3], rbar);
-        w = wait_phase<true>(BAR(B_X_FULL0 + xb), (g >> 1) & 1u, err, abort_flag);
+      for (int j = 0; j < 16; ++j) {
+        const __nv_bfloat162 v = __floats2bfloat162_rn(ex2_approx(sv[2 * j] - m), ex2_approx(sv[2 * j + 1] - m));
+        pk[j] = *reinterpret_cast<const uint32_t*>(&v);
+        rs[j & 3] += __low2float(v) + __high2float(v);
+      }
+      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
+      tmem_st16(tl + kColP + wg * 16, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(BAR(B_P_FULL));
+
+      if (cf.last()) {
+        // ---- epilogue of this segment: wait for its last P·V, normalise, store
+        const int row = sg[0], slot = sg[5];
+        w = wait_phase(BAR(B_O_DONE), g & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const float4 v = ld_shared_v4(my_row + (((uint32_t)k ^ swz) << 4));
-          sv[4 * k] += v.x;
-          sv[4 * k + 1] += v.y;
-          sv[4 * k + 2] += v.z;
-          sv[4 * k + 3] += v.w;
+        tc_fence_after();
+        float* redl = red + ((g + 1) & 1u) * (2 * kH);
+        redl[wg * kH + h] = l;
+        if (!group_sync()) {
+          ok = false;
+          break;
         }
-
-        // ---- scale (log2 domain), causal/length mask, online softmax
-        const int valid = vis - pg * kPage;
-        float mt = -INFINITY;
-#pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const float x = (j < valid) ? sv[j] * scale_log2 : -INFINITY;
-          sv[j] = x;
-          mt = fmaxf(mt, x);
+        const float lt = l + redl[(wg ^ 1) * kH + h];
+        if (!group_sync()) {  // both halves read before the next tile reuses this buffer
+          ok = false;
+          break;
         }
-        float factor = 1.f;
-        bool resc = false;
-        if (pg == pb) {
-          m = mt;
-        } else if (mt > m + 8.f) {
-          factor = exp2f(m - mt);
-          m = mt;
-          l *= factor;
-          resc = true;
-        }
-        // P (single TMEM buffer) and an O rescale both need PV of the previous tile done.
-        if (g > 0) {
-          w = wait_phase(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
-          if (!__all_sync(0xffffffffu, w)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-        }
-        if (__any_sync(0xffffffffu, resc)) {
-#pragma unroll 1
-          for (int c = 0; c < 256; c += 32) {
-            uint32_t r[32];
-            tmem_ld32_sync(tl + kColO + c, r);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) * factor);
-            tmem_st32(tl + kColO + c, r);
-          }
-        }
-        uint32_t pk[32];
-        float rs = 0.f;
-#pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const __nv_bfloat162 v = __floats2bfloat162_rn(exp2f(sv[2 * jj] - m), exp2f(sv[2 * jj + 1] - m));
-          pk[jj] = *reinterpret_cast<const uint32_t*>(&v);
-          rs += __low2float(v) + __high2float(v);
-        }
-        l += rs;
-        tmem_st32(tl + kColP, pk);
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(BAR(B_P_FULL));
-      }
-      if (!ok) break;
-
-      // ---- epilogue of this segment: wait for the last P·V, normalise, store
-      bool w = wait_phase(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const float inv = 1.f / l;
-      if (slot < 0) {
-        uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256);
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t r[32];
-          tmem_ld32_sync(tl + kColO + c, r);
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[c / 8 + v] = make_uint4(
-                pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv, __uint_as_float(r[8 * v + 1]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv, __uint_as_float(r[8 * v + 3]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv, __uint_as_float(r[8 * v + 5]) * inv),
-                pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv, __uint_as_float(r[8 * v + 7]) * inv));
-        }
-      } else {
-        float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * kH + h) * kDC + rank * 256);
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t r[32];
-          tmem_ld32_sync(tl + kColO + c, r);
-#pragma unroll
-          for (int v = 0; v < 8; ++v)
-            dst[c / 4 + v] = make_float4(__uint_as_float(r[4 * v]) * inv, __uint_as_float(r[4 * v + 1]) * inv,
-                                         __uint_as_float(r[4 * v + 2]) * inv, __uint_as_float(r[4 * v + 3]) * inv);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(BAR(B_O_FREE));
-      if (rank == 0) {
-        const float lse2 = m + log2f(l);
+        const float inv = 1.f / lt;
         if (slot < 0) {
-          if (a.lse) a.lse[(size_t)row * kH + h] = lse2 * 0.6931471805599453f;
+          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256 + wg * 128);
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t o[32];
+            tmem_ld32_sync(tl + kColO + wg * 128 + c, o);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+              dst[c / 8 + v] = make_uint4(
+                  pack_bf16x2(__uint_as_float(o[8 * v + 0]) * inv, __uint_as_float(o[8 * v + 1]) * inv),
+                  pack_bf16x2(__uint_as_float(o[8 * v + 2]) * inv, __uint_as_float(o[8 * v + 3]) * inv),
+                  pack_bf16x2(__uint_as_float(o[8 * v + 4]) * inv, __uint_as_float(o[8 * v + 5]) * inv),
+                  pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
+          }
         } else {
-          a.part_lse[(size_t)slot * kH + h] = lse2;
+          float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * kH + h) * kDC + rank * 256 + wg * 128);
+#pragma unroll 1
+          for (int c = 0; c < 128; c += 32) {
+            uint32_t o[32];
+            tmem_ld32_sync(tl + kColO + wg * 128 + c, o);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              dst[c / 4 + v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                           __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(BAR(B_O_FREE));
+        if (rank == 0 && wg == 0) {
+          const float lse2 = m + log2f(lt);
+          if (slot < 0) {
+            if (a.lse) a.lse[(size_t)row * kH + h] = lse2 * 0.6931471805599453f;
+          } else {
+            a.part_lse[(size_t)slot * kH + h] = lse2;
+          }
         }
       }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) own_cur[j] = own_nxt[j];
+      cf = cn;
     }
   }
 

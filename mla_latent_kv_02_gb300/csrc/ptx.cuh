@@ -6,6 +6,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "../../include/mla.h"
 
@@ -64,17 +65,49 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
   return ok != 0;
 }
 
-// Bounded wait.  On timeout: sets MLA_DEVERR_TIMEOUT in *err, raises the
-// CTA's abort flag and returns false.  Returns false at once when another
-// thread already raised the abort flag.
-template <bool kCluster = false>
+// Non-blocking probes of a phase (the thread is never suspended, so it sees
+// the completion as soon as it polls).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Bounded wait by polling.  On timeout: sets MLA_DEVERR_TIMEOUT in *err,
+// raises the CTA's abort flag and returns false.  Returns false at once when
+// another thread already raised the abort flag.
+// kSuspend: the thread may be suspended inside the probe (mbarrier.try_wait),
+// which frees issue slots for other warps at the cost of a later wake-up; for
+// roles that run ahead of the critical path.
+template <bool kCluster = false, bool kSuspend = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_t* err,
                                            volatile int32_t* abort_flag) {
-  if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  auto probe = [&]() -> bool {
+    if (kSuspend) return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
+    return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
+  };
+  if (probe()) return true;
   const uint64_t t0 = globaltimer();
   for (uint32_t i = 1;; ++i) {
-    if (kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0u) {
+    if (probe()) return true;
+    if ((i & 255u) == 0u) {
       if (*abort_flag) return false;
       if (globaltimer() - t0 > kWaitLimitNs) {
         atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
@@ -89,7 +122,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_
 // are still in flight before the CTA exits.
 __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) {
   const uint64_t t0 = globaltimer();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_test_wait(bar, parity)) {
     if (globaltimer() - t0 > kWaitLimitNs) return;
   }
 }
@@ -128,6 +161,37 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
                : "r"(addr)
                : "memory");
   return v;
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// Make this thread's generic-proxy shared-memory writes visible to the async
+// proxy (bulk copies, tensor core) before they are signalled.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory into a
+// peer CTA's shared memory, completing on the peer's mbarrier `rbar`.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t rdst, uint32_t src, uint32_t bytes, uint32_t rbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   rdst),
+               "r"(src), "r"(bytes), "r"(rbar)
+               : "memory");
+}
+// Arrive on a peer CTA's mbarrier, releasing this thread's prior accesses at cluster scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
+}
+// Named barrier over `count` threads (whole warps).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+// 2^x with the hardware approximation (flush-to-zero); 2^-inf = +0.
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // ------------------------------------------------------------------ TMA
@@ -237,6 +301,13 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
       MLA_W8(r, 0), MLA_W8(r, 8), MLA_W8(r, 16), MLA_W8(r, 24)
       : "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+      MLA_W8(r, 0), MLA_W8(r, 8)
+      : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 #define MLA_RW8(p, i) "+r"(p[i]), "+r"(p[i + 1]), "+r"(p[i + 2]), "+r"(p[i + 3]), "+r"(p[i + 4]), "+r"(p[i + 5]), "+r"(p[i + 6]), "+r"(p[i + 7])
@@ -251,6 +322,16 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// fp16x2 of two values clamped to the finite fp16 range (no infinities).
+__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
+  lo = fminf(fmaxf(lo, -65504.f), 65504.f);
+  hi = fminf(fmaxf(hi, -65504.f), 65504.f);
+  __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
+  return __half22float2(*reinterpret_cast<const __half2*>(&u));
+}
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
   return *reinterpret_cast<uint32_t*>(&v);

@@ -30,11 +30,17 @@ PAGE = 64        # tokens per page
 
 
 def bf16_round(x: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bf16 (ties to even); returns float32."""
-    x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
-    return (u.astype(np.uint32) << 16).view(np.float32)
+    """Round finite float32 values to the nearest bf16 (ties to even); returns float32.
+
+    In uint32 arithmetic: for finite inputs u + 0x8000 cannot wrap.
+    """
+    x = np.array(x, dtype=np.float32, copy=True, order="C")
+    u = x.view(np.uint32)
+    lsb = (u >> np.uint32(16)) & np.uint32(1)
+    u += np.uint32(0x7FFF)
+    u += lsb
+    u &= np.uint32(0xFFFF0000)
+    return x
 
 
 def bf16_bits(x: np.ndarray) -> np.ndarray:
@@ -182,9 +188,20 @@ WORKLOADS = {
 }
 
 
-def workload(idx: int, seed: int = 0, with_q_abs: bool = False, with_weights: bool = True) -> Case:
+def workload(idx: int, seed: int = 0, with_q_abs: bool = False, with_weights: bool = True,
+             batch: Optional[int] = None) -> Case:
+    """Workload ``idx``; ``batch`` keeps only its first sequences (a smaller
+    case of the same shape, e.g. for profiler captures)."""
     w = dict(WORKLOADS[idx])
     name = w.pop("name")
+    if batch is not None:
+        name = f"{name}_first{batch}"
+        if "draw_lens" in w:
+            B, lo, hi = w["draw_lens"]
+            w["draw_lens"] = (min(B, batch), lo, hi)
+        else:
+            w["seq_lens"] = w["seq_lens"][:batch]
+            w["q_lens"] = w["q_lens"][:batch]
     page_order = w.pop("page_order", "random")
     if "draw_lens" in w:
         return make_case(seq_lens=[], q_lens=w["q_lens"], seed=seed, page_order=page_order,
