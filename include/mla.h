@@ -255,6 +255,44 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
                             void* workspace, size_t ws_bytes, void* o_lat, float* lse,
                             int32_t* dev_err, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * Allocation-free decode (no counterpart in the source pages: it exists for
+ * callers that cannot allocate device memory).
+ * ------------------------------------------------------------------------- */
+
+/* Size of the scratch that mla_decode_paged_noalloc keeps in a device array
+ * of the library (plan area + split-KV workspace, 16.5 MiB in all). */
+#define MLA_NOALLOC_PLAN_BYTES (512u * 1024u)
+#define MLA_NOALLOC_WORKSPACE_BYTES (16u * 1024u * 1024u)
+
+/*
+ * mla_decode_paged for callers that cannot allocate device memory: a plugin
+ * that its host framework hands only input and output tensors, an engine
+ * whose memory pool already holds all free device memory, or a runtime that
+ * forbids allocation after initialisation.  The caller passes only inputs and
+ * outputs; the split plan and the split-KV workspace live in a file-scope
+ * device array of the library (MLA_NOALLOC_PLAN_BYTES +
+ * MLA_NOALLOC_WORKSPACE_BYTES, held on every device that loads the library
+ * until the process exits).  No cudaMalloc, cudaFree or other allocating call
+ * is made.
+ *
+ * Arguments as for mla_decode_paged, except that the sequence lengths are
+ * given on the host (seq_lens_host / q_lens_host, int32 [B]) and the plan is
+ * built internally.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress) and the cluster count; make that first call
+ * before capturing any stream.  When the plan for all clusters needs more
+ * workspace than the array holds, fewer clusters are used; a batch whose plan
+ * exceeds MLA_NOALLOC_PLAN_BYTES (about 16 000 query rows) is rejected with
+ * MLA_ERR_INVALID_ARG.  Nothing in the array needs to start at zero: every
+ * call writes the plan and every workspace slot before reading them.  All
+ * calls share the one array, so calls that may overlap on the GPU (different
+ * streams, or host threads racing on one device) race on it: serialise them.
+ */
+mla_status mla_decode_paged_noalloc(const void* q_abs, const void* q_r, const void* kv_cache,
+                                    int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                    const int32_t* seq_lens_host, const int32_t* q_lens_host, int32_t B,
+                                    float scale, void* o_lat, float* lse, int32_t* dev_err, void* stream);
+
 /*
  * Synchronise `stream`, read the device error word into *word_out (may be
  * NULL) and map it: 0 -> MLA_OK, MLA_DEVERR_TIMEOUT set -> MLA_ERR_TIMEOUT,

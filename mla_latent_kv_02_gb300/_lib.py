@@ -57,6 +57,7 @@ SIGNATURES = {
     "mla_decode_plan": (C.c_int, [PI32, PI32, I32, I32, P, SZ, C.POINTER(mla_plan_info), P]),
     "mla_decode_paged": (C.c_int, [P, P, P, I64, P, I32, P, C.POINTER(mla_plan_info), C.c_float, P, SZ, P, P, P, P]),
     "mla_check": (C.c_int, [P, P, PI32]),
+    "mla_decode_paged_noalloc": (C.c_int, [P, P, P, I64, P, I32, PI32, PI32, I32, C.c_float, P, P, P, P]),
 }
 
 

@@ -252,3 +252,28 @@ def mla_check(dev_err, stream=None) -> int:
     word = C.c_int32()
     _check(lib().mla_check(_stream(stream), _ptr(dev_err), C.byref(word)))
     return int(word.value)
+
+
+def mla_decode_paged_noalloc(q_abs, q_r, kv_cache, block_table, seq_lens, q_lens, o_lat, dev_err, lse=None,
+                             scale: float = 1.0 / (192 ** 0.5), stream=None) -> None:
+    """mla_decode_paged without caller-provided plan or workspace: for callers
+    that cannot allocate device memory (the library keeps both in a device
+    array of its own).  Calls that may overlap on the GPU must be serialised."""
+    T = q_abs.shape[0]
+    _need(q_abs, "q_abs", torch.bfloat16, (T, H, D_C))
+    _need(q_r, "q_r", torch.bfloat16, (T, H, D_R))
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(o_lat, "o_lat", torch.bfloat16, (T, H, D_C))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (T, H))
+    sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    ql = np.ascontiguousarray(q_lens, dtype=np.int32)
+    if int(ql.sum()) != T:
+        raise ValueError(f"q_lens sum to {int(ql.sum())} rows, q_abs has {T}")
+    P32 = C.POINTER(C.c_int32)
+    _check(lib().mla_decode_paged_noalloc(_ptr(q_abs), _ptr(q_r), _ptr(kv_cache), kv_cache.shape[0],
+                                          _ptr(block_table), block_table.shape[1], sl.ctypes.data_as(P32),
+                                          ql.ctypes.data_as(P32), int(sl.size), float(scale), _ptr(o_lat),
+                                          _ptr(lse), _ptr(dev_err), _stream(stream)))

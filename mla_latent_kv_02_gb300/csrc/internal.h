@@ -7,7 +7,12 @@
 
 #include <cstdint>
 
+#include "../../include/mla.h"
+
 namespace mla {
+
+// Records `message` as this thread's mla_last_error() and returns `s`.
+mla_status set_last_error(mla_status s, const char* message);
 
 // Layout of the decode plan (int32 words).  Written by the host planner,
 // read by the decode and combine kernels.

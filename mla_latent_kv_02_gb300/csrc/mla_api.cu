@@ -207,6 +207,8 @@ size_t workspace_bytes_for(int64_t partials) {
 }  // namespace
 
 namespace mla {
+mla_status set_last_error(mla_status s, const char* message) { return fail(s, "%s", message); }
+
 PlanLayout plan_layout(int64_t num_clusters, int64_t num_segments, int64_t num_split_rows) {
   PlanLayout L;
   L.seg_off = kPlanHeader;
