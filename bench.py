@@ -48,6 +48,25 @@ def workload_stats(case):
                 kv_bytes=kv_tokens * 1152)
 
 
+# DRAM traffic (read + write) per decode launch from an ncu capture, keyed by
+# the sha1 prefix of the decode kernel source it was taken on and the
+# workload.  Captured at half batch and scaled by the query rows (see
+# profiles/decode_kernel_mtp2_b32_ncu.md); any other source reads as null.
+MEASURED_TRAFFIC = {("946a5b8359ed", 2): 1170.0e6}
+
+
+def decode_traffic(workload: int, batch):
+    import hashlib
+    src = os.path.join(ROOT, "mla_latent_kv_02_gb300", "csrc", "decode_paged.cu")
+    try:
+        sha = hashlib.sha1(open(src, "rb").read()).hexdigest()[:12]
+    except OSError:
+        return None
+    if batch is not None:
+        return None
+    return MEASURED_TRAFFIC.get((sha, workload))
+
+
 def load_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -324,7 +343,7 @@ def run_mla(args):
         "roofline": {
             "kernel": "mla_decode_paged (decode + combine launches)",
             "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-            "frac": round(achieved / peak, 4), "traffic": None,
+            "frac": round(achieved / peak, 4), "traffic": decode_traffic(args.workload, args.batch),
             "peak_source": peaks["source"] + " (burst)",
             "t_roof_us": round(max(t_flops, t_bytes) * 1e6, 2),
             "frac_of_t_roof": round(max(t_flops, t_bytes) / dec_s, 4),
