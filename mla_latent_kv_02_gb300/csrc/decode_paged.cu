@@ -10,26 +10,29 @@
 //    (128 lanes × 512 columns), so the pair splits the latent columns: CTA r
 //    owns O[:, 256r : 256r+256) and streams only its columns of each 64-token
 //    page by TMA — no byte of the cache is read twice.
-//  * The score contraction (576 = 9 chunks of 64) is split the same way: CTA 0
-//    takes latent chunks 0-3, CTA 1 latent chunks 4-7 plus the RoPE chunk.  Each
-//    CTA computes a partial S = Q_r·K_r^T (tcgen05, M = 128 heads, N = 64
-//    tokens, A = Q from TMEM, B = the page tile in shared memory).  The
-//    partials, scaled to log2 units, are exchanged as fp16 (each warp stages
-//    its rows in shared memory; one bulk copy per warp pushes them into the
-//    peer CTA, completing on the peer's mbarrier).  Both CTAs add the two
-//    rounded halves in the same order-free way, so they hold bit-identical S,
-//    run the same online softmax, write P (bf16) into TMEM and accumulate
-//    O_r += P·V_r (tcgen05, N = 256, B = the same page tile read as an
-//    MN-major operand).
+//  * The score contraction (576) is split evenly: CTA r takes latent chunks
+//    4r..4r+3 (64 columns each, 128-byte swizzle) and RoPE dims [32r, 32r+32)
+//    (64-byte swizzle).  Each CTA computes a partial S = Q_r·K_r^T (tcgen05,
+//    M = 128 heads, N = 64 tokens, A = Q from TMEM, B = the page tile in shared
+//    memory).  The partials, scaled to log2 units, are exchanged as fp16: each
+//    warp stages its rows and one bulk copy per warp pushes them into the peer
+//    CTA, completing on the peer's mbarrier.  Both CTAs add the same two
+//    rounded halves, so they hold bit-identical S and take identical softmax
+//    decisions.
+//  * Softmax in packed fp16 (add, max, subtract, 2^x with one MUFU issue per
+//    pair), P converted to bf16 and written to TMEM; O_r += P·V_r (tcgen05,
+//    N = 256, B = the same page tile read as an MN-major operand) and the row
+//    sums l += P·1 (N = 16 against a tile of ones), so l matches exactly the
+//    bf16 P the tensor core accumulated.
 //  * Software pipeline: the scores of tile g+1 are read and pushed to the peer
-//    before tile g's softmax runs, so the exchange overlaps the softmax; the
-//    MMA warp issues each QK^T as soon as its inputs are ready, independently
-//    of the P·V order.
+//    before tile g's softmax runs; the MMA warp issues each QK^T as soon as
+//    its inputs are ready, independently of the P·V order.
 //  * Two softmax warpgroups split the 64 tokens of a tile (32 each, thread =
-//    head row = TMEM lane); the row maximum is combined through shared memory.
+//    head row = TMEM lane); the two threads of a row swap their maxima through
+//    a tagged shared-memory slot.
 //  * Online softmax with lazy rescaling: the running reference max only moves
 //    when a tile's max exceeds it by more than 8 (log2 units), so P stays
-//    below 256 and O in TMEM is rescaled only on those rare tiles.
+//    below 256 and O and l in TMEM are rescaled only on those rare tiles.
 //  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + MMA issue,
 //    warps 2-9 softmax/epilogue, warp 10 tells the peer when a receive buffer
 //    has been read (a cluster-scope release arrive stalls its thread for
@@ -54,34 +57,38 @@ using namespace mla::dev;
 constexpr int kH = 128, kDC = 512, kDR = 64, kPage = 64;
 constexpr int kChunk = 64;                                // elements in one 128-byte swizzled row
 constexpr int kChunkBytes = kPage * kChunk * 2;           // [64 tokens x 64] bf16 = 8 KB
-constexpr int kMaxQKChunks = 5;
-constexpr int kStageBytes = kMaxQKChunks * kChunkBytes;   // 40 KB
+constexpr int kRopeHalf = 32;                             // RoPE dims per CTA
+constexpr int kRopeBytes = kPage * kRopeHalf * 2;         // [64 tokens x 32] bf16 = 4 KB, 64-byte rows
+constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes; // 36 KB
 constexpr int kStages = 4;
 constexpr int kXBytes = kH * kPage * 2;                   // one CTA's fp16 partial S (16 KB)
 constexpr int kXHalf = kXBytes / 2;                       // one warpgroup's 32 tokens
 constexpr int kXWarp = kXHalf / 4;                        // one warp's 32 rows (2 KB)
+constexpr int kOnesBytes = 16 * kChunk * 2;               // [16 x 64] bf16 ones for the row sums
 
-// Shared memory: a small region (barriers, row reductions, flags) at the
+// Shared memory: a small region (barriers, row-max slots, flags) at the
 // start, then the 1024-byte aligned region (page ring, 2 send + 2 receive
-// exchange buffers).
+// exchange buffers, the ones tile).
 constexpr int kNumBars = 32;
 constexpr int kSmallBar = 0;
-constexpr int kSmallRed = kSmallBar + 8 * kNumBars;       // float [2 parity][2 wg][128]
-constexpr int kSmallMisc = kSmallRed + 2 * 2 * kH * 4;
+constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [2 parity][2 wg][128]: {max bits, tile}
+constexpr int kSmallMisc = kSmallPair + 2 * 2 * kH * 8;
 constexpr int kSmallBytes = kSmallMisc + 64;
 constexpr int kOffKV = 0;
 constexpr int kOffSend = kStages * kStageBytes;
 constexpr int kOffRecv = kOffSend + 2 * kXBytes;
-constexpr int kAlignedBytes = kOffRecv + 2 * kXBytes;
-constexpr int kSmemBytes = 232448;                        // the per-block maximum
-static_assert(kSmallBytes + kAlignedBytes <= kSmemBytes, "shared memory layout does not fit");
+constexpr int kOffOnes = kOffRecv + 2 * kXBytes;
+constexpr int kAlignedBytes = kOffOnes + kOnesBytes;
+constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320, kColP = 480, kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 480, kTmemCols = 512;
 constexpr int kThreads = 352;
 constexpr uint32_t kSoftmaxThreads = 256;
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
+constexpr uint32_t kIdescSum = idesc_bf16_f32(128, 16, false, false);
 
 enum : int {
   B_KV_FULL = 0,
@@ -96,10 +103,9 @@ enum : int {
   B_X_FULL1,
   B_X_EMPTY0,  // the peer has read what this CTA pushed into its buffer 0 / 1
   B_X_EMPTY1,
-  B_X_READ0,   // this CTA has read receive buffer 0 / 1 (local, for the signaller)
+  B_X_READ0,   // every softmax warp of this CTA has read receive buffer 0 / 1
   B_X_READ1,
   B_DRAIN,
-  B_GROUP,
   B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier area too small");
@@ -130,12 +136,16 @@ struct TileCursor {
   }
 };
 
+__device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
+__device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const DecodeArgs a) {
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap rope_map,
+                  const DecodeArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t bars = raw + kSmallBar;
-  float* red = reinterpret_cast<float*>(smem_raw + kSmallRed);
+  const uint32_t pair = raw + kSmallPair;  // uint2 slots, accessed with volatile ld/st
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem_raw + kSmallMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + kSmallMisc + 8);
   int32_t* seg_range = reinterpret_cast<int32_t*>(smem_raw + kSmallMisc + 16);
@@ -147,8 +157,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const uint32_t rank = cluster_ctarank();
   const uint32_t peer = rank ^ 1u;
   const int cid = blockIdx.x >> 1;
-  const int nq = rank ? 5 : 4;      // score-contraction chunks held by this CTA
-  const int chunk0 = rank ? 4 : 0;  // first of them within the 576-wide token row
   int32_t* err = a.dev_err;
 
   if (threadIdx.x == 0) {
@@ -167,10 +175,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_X_FULL1), 1);
     mbar_init(BAR(B_X_EMPTY0), 1);
     mbar_init(BAR(B_X_EMPTY1), 1);
-    mbar_init(BAR(B_X_READ0), 1);
-    mbar_init(BAR(B_X_READ1), 1);
+    mbar_init(BAR(B_X_READ0), 8);
+    mbar_init(BAR(B_X_READ1), 8);
     mbar_init(BAR(B_DRAIN), 1);
-    mbar_init(BAR(B_GROUP), kSoftmaxThreads);
     fence_mbar_init();
   }
   if (threadIdx.x == 64) {
@@ -192,7 +199,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     seg_range[0] = sb;
     seg_range[1] = se;
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&kv_map);
+  // Row-max slots start with an impossible tile tag; the ones tile feeds the
+  // row-sum MMA (written by the generic proxy, read by the tensor core).
+  for (int i = threadIdx.x; i < 2 * 2 * kH; i += kThreads) st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
+  if (layout_fits) {
+    uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + kOffOnes);
+    for (int i = threadIdx.x; i < kOnesBytes / 4; i += kThreads) ones[i] = 0x3F803F80u;  // bf16 1.0 pairs
+    fence_proxy_async_smem();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&kv_map);
+    prefetch_tmap(&rope_map);
+  }
   if (warp == 1) {
     __syncwarp();
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -228,9 +246,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pid = 0;
           }
           const uint32_t dst = base + kOffKV + st * kStageBytes;
-          mbar_arrive_expect_tx(BAR(B_KV_FULL + st), (uint32_t)(nq * kChunkBytes));
-          for (int i = 0; i < nq; ++i)
-            tma_load_2d(dst + i * kChunkBytes, &kv_map, (chunk0 + i) * kChunk, pid * kPage, BAR(B_KV_FULL + st));
+          mbar_arrive_expect_tx(BAR(B_KV_FULL + st), (uint32_t)kStageBytes);
+          for (int i = 0; i < 4; ++i)
+            tma_load_2d(dst + i * kChunkBytes, &kv_map, (int)(4 * rank + i) * kChunk, pid * kPage,
+                        BAR(B_KV_FULL + st));
+          tma_load_2d(dst + 4 * kChunkBytes, &rope_map, kDC + (int)rank * kRopeHalf, pid * kPage, BAR(B_KV_FULL + st));
           ++g;
         }
       }
@@ -248,6 +268,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       TileCursor cq, cp;
       cq.init(a.segs, s_begin, s_end);
       cp.init(a.segs, s_begin, s_end);
+      const uint32_t ones = base + kOffOnes;
       uint32_t tq = 0, tp = 0, spins = 0;
       uint64_t t_stall = 0;
       while (cp.valid()) {
@@ -260,11 +281,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           if (ready) {
             tc_fence_after();
             const uint32_t kv = base + kOffKV + st * kStageBytes;
-            // S_partial[128 x 64] = Q_r[128 x 64*nq] · K_r^T, K-major, 16 per step.
-            for (int i = 0; i < nq; ++i)
+            // S_partial[128 x 64] = Q_r[128 x 288] · K_r^T, K-major, 16 per step:
+            // 4 latent chunks (128-byte swizzle) then the RoPE half (64-byte swizzle).
+            for (int i = 0; i < 4; ++i)
               for (int kk = 0; kk < 4; ++kk)
                 mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8,
                        sdesc_sw128(kv + i * kChunkBytes + kk * 32, 16, 1024), kIdescQK, (i | kk) ? 1u : 0u);
+            for (int kk = 0; kk < 2; ++kk)
+              mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, sdesc_sw64(kv + 4 * kChunkBytes + kk * 32, 16, 512),
+                     kIdescQK, 1u);
             tc_commit(BAR(B_S_FULL));
             cq.next();
             ++tq;
@@ -282,6 +307,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
             for (int kk = 0; kk < 4; ++kk)
               mma_ts(tmem + kColO, tmem + kColP + kk * 8, sdesc_sw128(v + kk * 2048, 8192, 1024), kIdescPV,
+                     (first && kk == 0) ? 0u : 1u);
+            // l[128 x 16] += P · 1: every column holds the row sum of P.
+            for (int kk = 0; kk < 4; ++kk)
+              mma_ts(tmem + kColSum, tmem + kColP + kk * 8, sdesc_sw128(ones + kk * 32, 16, 1024), kIdescSum,
                      (first && kk == 0) ? 0u : 1u);
             tc_commit(BAR(B_KV_EMPTY + tp % kStages));
             tc_commit(BAR(B_O_DONE));
@@ -334,34 +363,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t warp_off = (uint32_t)(wg * kXHalf + q4 * kXWarp);
     const bool leader = (sw == 0 && lane == 0);
     const float c2 = a.scale_log2;
-    // Barrier over the 256 softmax threads with a bounded wait (a hardware
-    // named barrier would hang if one warp stopped early on a timeout).
-    uint32_t grp = 0;
-    auto group_sync = [&]() -> bool {
-      mbar_arrive(BAR(B_GROUP));
-      const bool w = wait_phase(BAR(B_GROUP), grp & 1u, err, abort_flag);
-      ++grp;
-      return __all_sync(0xffffffffu, w);
-    };
     __syncwarp();
 
-    // Q_r of a row into TMEM: this warpgroup's chunks (2 latent chunks, plus the
-    // RoPE chunk for CTA 1's first warpgroup), all loads issued before any store.
+    // Q_r of a row into TMEM: warpgroup 0 loads latent chunks 0-1, warpgroup 1
+    // latent chunks 2-3 and the RoPE half; all loads issued before any store.
     auto load_q = [&](int s) {
       const int row = a.segs[8 * s];
       const uint4* lat = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256) + wg * 16;
-      const bool rope = (rank == 1 && wg == 0);
-      uint4 v[24];
+      uint4 v[20];
 #pragma unroll
       for (int j = 0; j < 16; ++j) v[j] = __ldg(lat + j);
-      if (rope) {
-        const uint4* rp = reinterpret_cast<const uint4*>(a.q_r + ((size_t)row * kH + h) * kDR);
+      if (wg == 1) {
+        const uint4* rp = reinterpret_cast<const uint4*>(a.q_r + ((size_t)row * kH + h) * kDR + rank * kRopeHalf);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[16 + j] = __ldg(rp + j);
+        for (int j = 0; j < 4; ++j) v[16 + j] = __ldg(rp + j);
       }
 #pragma unroll
-      for (int ci = 0; ci < 3; ++ci) {
-        if (ci == 2 && !rope) break;
+      for (int ci = 0; ci < 2; ++ci) {
         uint32_t r[32];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -370,8 +388,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           r[4 * j + 2] = v[ci * 8 + j].z;
           r[4 * j + 3] = v[ci * 8 + j].w;
         }
-        const int chunk = ci < 2 ? wg * 2 + ci : 4;
-        tmem_st32(tl + kColQ + chunk * 32, r);
+        tmem_st32(tl + kColQ + (wg * 2 + ci) * 32, r);
+      }
+      if (wg == 1) {
+        uint32_t r[16];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          r[4 * j] = v[16 + j].x;
+          r[4 * j + 1] = v[16 + j].y;
+          r[4 * j + 2] = v[16 + j].z;
+          r[4 * j + 3] = v[16 + j].w;
+        }
+        tmem_st16(tl + kColQ + 128, r);
       }
       tmem_st_wait();
       tc_fence_before();
@@ -392,7 +420,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (c.last() && c.s + 1 < c.s_end) load_q(c.s + 1);  // every QK^T of this segment is done
 #pragma unroll
       for (int j = 0; j < 16; ++j)
-        own[j] = pack_f16x2_sat(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
+        own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
       const uint32_t xb = t & 1u;
       if (t >= 2) {  // the peer has read what was pushed into this buffer two tiles ago
         w = wait_phase<true>(BAR(B_X_EMPTY0 + xb), ((t - 2) >> 1) & 1u, err, abort_flag);
@@ -424,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       load_q(s_begin);
       ok = fetch_push(0, cf, own_cur);
     }
-    float m = -INFINITY, l = 0.f;
+    float m = -INFINITY;
     for (uint32_t g = 0; g < G && ok; ++g) {
       TileCursor cn = cf;
       cn.next();
@@ -435,7 +463,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int32_t* sg = a.segs + 8 * cf.s;
       const int pg = cf.pg, vis = sg[4];
 
-      // ---- tile g: the peer's half, full scores (log2 units)
+      // ---- tile g: add the peer's half (fp16, log2 units)
       const uint32_t xb = g & 1u;
       if (leader) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
       bool w = wait_phase<true>(BAR(B_X_FULL0 + xb), (g >> 1) & 1u, err, abort_flag);
@@ -444,54 +472,69 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
       const uint32_t recv = base + kOffRecv + xb * kXBytes + row_off;
-      float sv[32];
+      uint32_t sv[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         const float4 v = ld_shared_v4(recv + (((uint32_t)k ^ swz) << 4));
-        const uint32_t pv[4] = {__float_as_uint(v.x), __float_as_uint(v.y), __float_as_uint(v.z),
-                                __float_as_uint(v.w)};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 o2 = unpack_f16x2(own_cur[4 * k + i]);
-          const float2 p2 = unpack_f16x2(pv[i]);
-          sv[8 * k + 2 * i] = o2.x + p2.x;
-          sv[8 * k + 2 * i + 1] = o2.y + p2.y;
-        }
+        sv[4 * k] = as_u32(__hadd2(as_h2(own_cur[4 * k]), as_h2(__float_as_uint(v.x))));
+        sv[4 * k + 1] = as_u32(__hadd2(as_h2(own_cur[4 * k + 1]), as_h2(__float_as_uint(v.y))));
+        sv[4 * k + 2] = as_u32(__hadd2(as_h2(own_cur[4 * k + 2]), as_h2(__float_as_uint(v.z))));
+        sv[4 * k + 3] = as_u32(__hadd2(as_h2(own_cur[4 * k + 3]), as_h2(__float_as_uint(v.w))));
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_X_READ0 + xb));  // this warp has read the buffer
 
-      // ---- causal/length mask, row max over both warpgroups
+      // ---- causal/length mask and this half's row max
       const int valid = vis - pg * kPage - wg * 32;
       if (valid < 32) {
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
-          if (j >= valid) sv[j] = -INFINITY;
+        for (int j = 0; j < 16; ++j) {
+          if (2 * j >= valid) sv[j] = (sv[j] & 0xFFFF0000u) | 0xFC00u;          // low half -> -inf
+          if (2 * j + 1 >= valid) sv[j] = (sv[j] & 0x0000FFFFu) | 0xFC000000u;  // high half -> -inf
+        }
       }
-      float mx[8];
+      __half2 mx[4];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) mx[j] = fmaxf(fmaxf(sv[4 * j], sv[4 * j + 1]), fmaxf(sv[4 * j + 2], sv[4 * j + 3]));
-      const float mloc =
-          fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])), fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-      float* redp = red + xb * (2 * kH);
-      redp[wg * kH + h] = mloc;
-      if (!group_sync()) {
+      for (int j = 0; j < 4; ++j)
+        mx[j] = __hmax2(__hmax2(as_h2(sv[4 * j]), as_h2(sv[4 * j + 1])), __hmax2(as_h2(sv[4 * j + 2]), as_h2(sv[4 * j + 3])));
+      const __half2 mh = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
+      const float mloc = fmaxf(__low2float(mh), __high2float(mh));
+
+      // ---- swap maxima with the other thread of this row (tagged slot)
+      st_shared_v2_volatile(pair + 8u * ((xb * 2 + wg) * kH + h), __float_as_uint(mloc), g);
+      float mo;
+      {
+        const uint32_t slot = pair + 8u * ((xb * 2 + (wg ^ 1)) * kH + h);
+        uint2 v = ld_shared_v2_volatile(slot);
+        if (v.y != g) {
+          const uint64_t t0 = globaltimer();
+          for (uint32_t it = 1; (v = ld_shared_v2_volatile(slot)).y != g; ++it) {
+            if ((it & 255u) == 0u && (*abort_flag || globaltimer() - t0 > kWaitLimitNs)) {
+              if (!*abort_flag) atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              break;
+            }
+          }
+        }
+        mo = __uint_as_float(v.x);
+        w = (v.y == g);
+      }
+      if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
       }
-      if (leader) mbar_arrive(BAR(B_X_READ0 + xb));  // all have read this buffer; warp 10 tells the peer
-      const float mt = fmaxf(mloc, redp[(wg ^ 1) * kH + h]);
+      const float mt = fmaxf(mloc, mo);
 
       float factor = 1.f;
       bool resc = false;
       if (cf.first()) {
         m = mt;
-        l = 0.f;
       } else if (mt > m + 8.f) {
-        factor = ex2_approx(m - mt);
+        factor = exp2f(m - mt);
         m = mt;
-        l *= factor;
         resc = true;
       }
-      // P (single TMEM buffer) and an O rescale both need P·V of the previous tile done.
+      // P (single TMEM buffer) and a rescale both need P·V of the previous tile done.
       if (g > 0) {
         w = wait_phase(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
@@ -509,16 +552,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
           tmem_st32(tl + kColO + wg * 128 + c, o);
         }
+        if (wg == 0) tmem_st1(tl + kColSum, __float_as_uint(__uint_as_float(tmem_ld1_sync(tl + kColSum)) * factor));
       }
+      // P = 2^(s - m) in fp16 pairs, stored as bf16 for the tensor core.
+      const __half2 m2 = __float2half2_rn(m);  // m is a max of fp16 values: exact
       uint32_t pk[16];
-      float rs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < 16; ++j) {
-        const __nv_bfloat162 v = __floats2bfloat162_rn(ex2_approx(sv[2 * j] - m), ex2_approx(sv[2 * j + 1] - m));
-        pk[j] = *reinterpret_cast<const uint32_t*>(&v);
-        rs[j & 3] += __low2float(v) + __high2float(v);
+        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hsub2(as_h2(sv[j]), m2)))));
+        pk[j] = pack_bf16x2(p.x, p.y);
       }
-      l += (rs[0] + rs[1]) + (rs[2] + rs[3]);
       tmem_st16(tl + kColP + wg * 16, pk);
       tmem_st_wait();
       tc_fence_before();
@@ -533,17 +576,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         tc_fence_after();
-        float* redl = red + ((g + 1) & 1u) * (2 * kH);
-        redl[wg * kH + h] = l;
-        if (!group_sync()) {
-          ok = false;
-          break;
-        }
-        const float lt = l + redl[(wg ^ 1) * kH + h];
-        if (!group_sync()) {  // both halves read before the next tile reuses this buffer
-          ok = false;
-          break;
-        }
+        const float lt = __uint_as_float(tmem_ld1_sync(tl + kColSum));
         const float inv = 1.f / lt;
         if (slot < 0) {
           uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256 + wg * 128);
@@ -655,11 +688,11 @@ cudaError_t decode_max_clusters(int* out) {
   return cudaOccupancyMaxActiveClusters(out, (const void*)decode::decode_kernel, &cfg);
 }
 
-cudaError_t launch_decode(const CUtensorMap& kv_map, const DecodeArgs& args, int num_clusters,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& rope_map, const DecodeArgs& args,
+                          int num_clusters, cudaStream_t stream) {
   cudaError_t e = decode_prepare();
   if (e != cudaSuccess) return e;
-  decode::decode_kernel<<<2 * num_clusters, decode::kThreads, decode::kSmemBytes, stream>>>(kv_map, args);
+  decode::decode_kernel<<<2 * num_clusters, decode::kThreads, decode::kSmemBytes, stream>>>(kv_map, rope_map, args);
   return cudaGetLastError();
 }
 

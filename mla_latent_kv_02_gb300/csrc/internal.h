@@ -78,7 +78,10 @@ struct CombineArgs {
 int decode_smem_bytes();
 int decode_threads();
 cudaError_t decode_max_clusters(int* out);
-cudaError_t launch_decode(const CUtensorMap& kv_map, const DecodeArgs& args, int num_clusters, cudaStream_t stream);
+// kv_map: 128-byte swizzled boxes of 64 columns x 64 tokens (latent chunks);
+// rope_map: 64-byte swizzled boxes of 32 columns x 64 tokens (RoPE halves).
+cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& rope_map, const DecodeArgs& args,
+                          int num_clusters, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& args, int num_split_rows, cudaStream_t stream);
 
 cudaError_t launch_kv_append(const uint16_t* c_kv_new, const uint16_t* k_r_new, const int64_t* slots, int32_t n,

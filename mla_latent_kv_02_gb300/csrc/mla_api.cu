@@ -65,17 +65,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// bf16 tensor map with 128-byte swizzle; dims innermost first, strides in
-// bytes for dims 1..rank-1.
+// bf16 tensor map (128-byte swizzle unless told otherwise); dims innermost
+// first, strides in bytes for dims 1..rank-1.
 mla_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
-                    const uint32_t* box, const char* what) {
+                    const uint32_t* box, const char* what,
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
   auto fn = encode_fn();
   if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
                   reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides),
-                  reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                  reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled(%s) failed with %d", what, (int)r);
   return MLA_OK;
 }
@@ -532,11 +533,14 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
       return fail(MLA_ERR_INVALID_ARG, "workspace holds %zu bytes, the plan needs %zu", ws_bytes, need_ws);
   }
 
-  CUtensorMap kv_map;
+  CUtensorMap kv_map, rope_map;
   const uint64_t dims[2] = {MLA_TOKEN_ELEMS, (uint64_t)num_pages * MLA_PAGE_SIZE};
   const uint64_t str[1] = {(uint64_t)kRowBytes};
   const uint32_t box[2] = {64, 64};
+  const uint32_t rope_box[2] = {32, 64};
   mla_status s = make_map(&kv_map, kv_cache, 2, dims, str, box, "kv_cache");
+  if (s != MLA_OK) return s;
+  s = make_map(&rope_map, kv_cache, 2, dims, str, rope_box, "kv_cache RoPE halves", CU_TENSOR_MAP_SWIZZLE_64B);
   if (s != MLA_OK) return s;
 
   const mla::PlanLayout L = mla::plan_layout(info->num_clusters, info->num_segments, info->num_split_rows);
@@ -562,7 +566,7 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
   a.B = info->B;
   a.num_segments = info->num_segments;
   a.num_partials = info->num_partials;
-  cudaError_t e = mla::launch_decode(kv_map, a, info->num_clusters, (cudaStream_t)stream);
+  cudaError_t e = mla::launch_decode(kv_map, rope_map, a, info->num_clusters, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (info->num_split_rows > 0) {
     mla::CombineArgs c = {};

@@ -166,6 +166,15 @@ __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
+// Volatile 8-byte shared-memory access (a tagged slot polled by another warp).
+__device__ __forceinline__ void st_shared_v2_volatile(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.volatile.shared.v2.u32 [%0], {%1, %2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ uint2 ld_shared_v2_volatile(uint32_t addr) {
+  uint2 v;
+  asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
+  return v;
+}
 // Make this thread's generic-proxy shared-memory writes visible to the async
 // proxy (bulk copies, tensor core) before they are signalled.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -259,13 +268,19 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       : "memory");
 }
 
-// Shared-memory matrix descriptor, 128-byte swizzle (atoms of 8 rows x 128 B,
-// 1024-byte aligned).  lbo/sbo in bytes.  Bits: [0,14) start >> 4,
+// Shared-memory matrix descriptor.  lbo/sbo in bytes.  Bits: [0,14) start >> 4,
 // [16,30) leading byte offset >> 4, [32,46) stride byte offset >> 4,
-// [46,48) descriptor version 1, [61,64) layout 2 = 128-byte swizzle.
-__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// [46,48) descriptor version 1, [61,64) layout: 2 = 128-byte swizzle (atoms
+// of 8 rows x 128 B, 1024-byte aligned), 4 = 64-byte swizzle (8 rows x 64 B).
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo, uint32_t layout) {
   return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
-         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+         ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)layout << 61);
+}
+__device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return sdesc(saddr, lbo, sbo, 2u);
+}
+__device__ __forceinline__ uint64_t sdesc_sw64(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return sdesc(saddr, lbo, sbo, 4u);
 }
 
 // Instruction descriptor for kind::f16 with bf16 A/B and fp32 D.
@@ -308,6 +323,15 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16
       MLA_W8(r, 0), MLA_W8(r, 8)
       : "memory");
 }
+__device__ __forceinline__ uint32_t tmem_ld1_sync(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : "+r"(r) : : "memory");
+  return r;
+}
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 #define MLA_RW8(p, i) "+r"(p[i]), "+r"(p[i + 1]), "+r"(p[i + 2]), "+r"(p[i + 3]), "+r"(p[i + 4]), "+r"(p[i + 5]), "+r"(p[i + 6]), "+r"(p[i + 7])
@@ -322,6 +346,18 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// fp16x2 of two values, saturating to the finite fp16 range (no infinities).
+__device__ __forceinline__ uint32_t cvt_f16x2_satfinite(float lo, float hi) {
+  uint32_t d;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// 2^x on both halves of an fp16x2 (hardware approximation, one MUFU issue).
+__device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
+  uint32_t y;
+  asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
 // fp16x2 of two values clamped to the finite fp16 range (no infinities).
 __device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
   lo = fminf(fmaxf(lo, -65504.f), 65504.f);

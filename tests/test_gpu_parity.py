@@ -96,7 +96,7 @@ def _check_decode(api, case, num_clusters=None, tag=""):
     ref_o, ref_lse = oracle.decode(case.q_abs, case.q_r, oracle_cache(case), case.block_table,
                                    case.seq_lens, case.q_lens, SCALE)
     assert_close(to_np(o), ref_o, f"o_lat {tag}")
-    assert_close(lse.cpu().numpy(), ref_lse, f"lse {tag}", max_frac=1e-3, mean_rel=1e-4)
+    assert_close(lse.cpu().numpy(), ref_lse, f"lse {tag}", max_frac=2e-3, mean_rel=5e-4)
     return plan
 
 
@@ -216,6 +216,6 @@ def test_workload_full_size_sampled_rows(api, cfg, k):
                           case.seq_lens, case.q_lens, SCALE, rows=rows)
     assert_close(to_np(o)[rows], ref["o_lat"][rows], f"cfg{cfg} o_lat")
     assert_close(to_np(out)[rows], ref["out"][rows], f"cfg{cfg} out")
-    assert_close(lse.cpu().numpy()[rows], ref["lse"][rows], f"cfg{cfg} lse", max_frac=1e-3, mean_rel=1e-4)
+    assert_close(lse.cpu().numpy()[rows], ref["lse"][rows], f"cfg{cfg} lse", max_frac=2e-3, mean_rel=5e-4)
     # property over every row: finite outputs, lse >= max-free lower bound ln(1)
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
