@@ -268,7 +268,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       TileCursor cq, cp;
       cq.init(a.segs, s_begin, s_end);
       cp.init(a.segs, s_begin, s_end);
-      const uint32_t ones = base + kOffOnes;
+      // Stage-0 descriptors: latent chunks (K-major for QK^T), RoPE half, the
+      // same latent chunks read MN-major for P·V, and the ones tile.
+      const uint64_t kdesc0 = sdesc_sw128(base + kOffKV, 16, 1024);
+      const uint64_t rdesc0 = sdesc_sw64(base + kOffKV + 4 * kChunkBytes, 16, 512);
+      const uint64_t vdesc0 = sdesc_sw128(base + kOffKV, 8192, 1024);
+      const uint64_t odesc0 = sdesc_sw128(base + kOffOnes, 16, 1024);
       uint32_t tq = 0, tp = 0, spins = 0;
       uint64_t t_stall = 0;
       while (cp.valid()) {
@@ -280,16 +285,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              (!cq.first() || mbar_test_wait(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u));
           if (ready) {
             tc_fence_after();
-            const uint32_t kv = base + kOffKV + st * kStageBytes;
             // S_partial[128 x 64] = Q_r[128 x 288] · K_r^T, K-major, 16 per step:
             // 4 latent chunks (128-byte swizzle) then the RoPE half (64-byte swizzle).
+            // Descriptors are built once per stage and advanced by adding the
+            // byte offset >> 4 to the start-address field (no carry: shared
+            // addresses stay below 2^18).
+            const uint64_t dk = kdesc0 + (uint64_t)((st * kStageBytes) >> 4);
+            const uint64_t dr = rdesc0 + (uint64_t)((st * kStageBytes) >> 4);
+#pragma unroll
             for (int i = 0; i < 4; ++i)
+#pragma unroll
               for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8,
-                       sdesc_sw128(kv + i * kChunkBytes + kk * 32, 16, 1024), kIdescQK, (i | kk) ? 1u : 0u);
+                mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8, dk + (uint64_t)((i * kChunkBytes + kk * 32) >> 4),
+                       kIdescQK, (i | kk) ? 1u : 0u);
+#pragma unroll
             for (int kk = 0; kk < 2; ++kk)
-              mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, sdesc_sw64(kv + 4 * kChunkBytes + kk * 32, 16, 512),
-                     kIdescQK, 1u);
+              mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, dr + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
             tc_commit(BAR(B_S_FULL));
             cq.next();
             ++tq;
@@ -302,16 +313,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                              (!first || mbar_test_wait(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u));
           if (ready) {
             tc_fence_after();
-            const uint32_t v = base + kOffKV + (tp % kStages) * kStageBytes;
             // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
             // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kColO, tmem + kColP + kk * 8, sdesc_sw128(v + kk * 2048, 8192, 1024), kIdescPV,
-                     (first && kk == 0) ? 0u : 1u);
-            // l[128 x 16] += P · 1: every column holds the row sum of P.
-            for (int kk = 0; kk < 4; ++kk)
-              mma_ts(tmem + kColSum, tmem + kColP + kk * 8, sdesc_sw128(ones + kk * 32, 16, 1024), kIdescSum,
-                     (first && kk == 0) ? 0u : 1u);
+            // l[128 x 16] += P · 1 (every column holds the row sum of P), issued
+            // interleaved so consecutive MMAs never share an accumulator.
+            const uint64_t dv = vdesc0 + (uint64_t)(((tp % kStages) * kStageBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+              const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+              mma_ts(tmem + kColO, tmem + kColP + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, acc);
+              mma_ts(tmem + kColSum, tmem + kColP + kk * 8, odesc0 + (uint64_t)((kk * 32) >> 4), kIdescSum, acc);
+            }
             tc_commit(BAR(B_KV_EMPTY + tp % kStages));
             tc_commit(BAR(B_O_DONE));
             cp.next();
@@ -322,7 +334,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (progressed) {
           spins = 0;
         } else {
-          __nanosleep(20);  // poll gently: this SM sub-partition also runs softmax warps
           if (spins == 0) t_stall = globaltimer();
           if ((++spins & 255u) == 0u) {
             if (*abort_flag) break;
@@ -346,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
       for (uint32_t g = 0; g < G; ++g) {
         const uint32_t xb = g & 1u;
-        if (!wait_phase<false, true>(BAR(B_X_READ0 + xb), (g >> 1) & 1u, err, abort_flag)) break;
+        if (!wait_phase(BAR(B_X_READ0 + xb), (g >> 1) & 1u, err, abort_flag)) break;
         mbar_arrive_remote(mapa(BAR(B_X_EMPTY0 + xb), peer));
       }
     }
