@@ -33,10 +33,11 @@
 //  * Online softmax with lazy rescaling: the running reference max only moves
 //    when a tile's max exceeds it by more than 8 (log2 units), so P stays
 //    below 256 and O and l in TMEM are rescaled only on those rare tiles.
-//  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + MMA issue,
+//  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + QK^T issue,
 //    warps 2-9 softmax/epilogue, warp 10 tells the peer when a receive buffer
 //    has been read (a cluster-scope release arrive stalls its thread for
-//    hundreds of cycles, so it is kept off the softmax warps).
+//    hundreds of cycles, so it is kept off the softmax warps), warp 11 P·V
+//    issue.
 //  * Work: the plan cuts all rows' 64-token tiles into equal contiguous ranges,
 //    one per cluster; a row cut by a boundary is written as fp32 partials
 //    (normalised O and log2-sum-exp) and merged by the combine kernel.
@@ -83,7 +84,9 @@ constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 
 constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 480, kTmemCols = 512;
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
+// The two MMA-issuing threads sleep in mbarrier.try_wait rather than poll.
+constexpr bool kIssueSuspend = true;
 constexpr uint32_t kSoftmaxThreads = 256;
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
@@ -106,6 +109,7 @@ enum : int {
   B_X_READ0,   // every softmax warp of this CTA has read receive buffer 0 / 1
   B_X_READ1,
   B_DRAIN,
+  B_DRAIN_PV,
   B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier area too small");
@@ -178,6 +182,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_X_READ0), 8);
     mbar_init(BAR(B_X_READ1), 8);
     mbar_init(BAR(B_DRAIN), 1);
+    mbar_init(BAR(B_DRAIN_PV), 1);
     fence_mbar_init();
   }
   if (threadIdx.x == 64) {
@@ -260,94 +265,81 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issue
-    // Two in-order streams, QK^T(t) and P·V(t); whichever is ready is issued,
-    // QK^T first, so the tensor pipe runs the next scores while the softmax
-    // of the current tile is still in flight.
+    // ---------------------------------------------------------------- QK^T issue
+    // S_partial(t) = Q_r · K_r(t)^T as soon as page t has landed and the
+    // softmax has read S(t-1).  P·V is issued by its own warp (11), so a long
+    // QK^T issue (the tensor pipe throttles it) never delays P·V, nor the
+    // other way round; the two streams share only the tensor pipe.
     if (lane == 0) {
-      TileCursor cq, cp;
+      TileCursor cq;
       cq.init(a.segs, s_begin, s_end);
-      cp.init(a.segs, s_begin, s_end);
-      // Stage-0 descriptors: latent chunks (K-major for QK^T), RoPE half, the
-      // same latent chunks read MN-major for P·V, and the ones tile.
+      // Stage-0 descriptors: latent chunks (K-major) and the RoPE half,
+      // advanced by adding the byte offset >> 4 to the start-address field
+      // (no carry: shared addresses stay below 2^18).
       const uint64_t kdesc0 = sdesc_sw128(base + kOffKV, 16, 1024);
       const uint64_t rdesc0 = sdesc_sw64(base + kOffKV + 4 * kChunkBytes, 16, 512);
-      const uint64_t vdesc0 = sdesc_sw128(base + kOffKV, 8192, 1024);
-      const uint64_t odesc0 = sdesc_sw128(base + kOffOnes, 16, 1024);
-      uint32_t tq = 0, tp = 0, spins = 0;
-      uint64_t t_stall = 0;
-      while (cp.valid()) {
-        bool progressed = false;
-        if (cq.valid()) {
-          const uint32_t st = tq % kStages;
-          const bool ready = mbar_test_wait(BAR(B_KV_FULL + st), (tq / kStages) & 1u) &&
-                             (tq == 0 || mbar_test_wait(BAR(B_S_FREE), (tq - 1) & 1u)) &&
-                             (!cq.first() || mbar_test_wait(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u));
-          if (ready) {
-            tc_fence_after();
-            // S_partial[128 x 64] = Q_r[128 x 288] · K_r^T, K-major, 16 per step:
-            // 4 latent chunks (128-byte swizzle) then the RoPE half (64-byte swizzle).
-            // Descriptors are built once per stage and advanced by adding the
-            // byte offset >> 4 to the start-address field (no carry: shared
-            // addresses stay below 2^18).
-            const uint64_t dk = kdesc0 + (uint64_t)((st * kStageBytes) >> 4);
-            const uint64_t dr = rdesc0 + (uint64_t)((st * kStageBytes) >> 4);
+      for (uint32_t tq = 0; cq.valid(); ++tq) {
+        const uint32_t st = tq % kStages;
+        if (!wait_phase<false, kIssueSuspend>(BAR(B_KV_FULL + st), (tq / kStages) & 1u, err, abort_flag)) break;
+        if (tq > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_S_FREE), (tq - 1) & 1u, err, abort_flag)) break;
+        if (cq.first() &&
+            !wait_phase<false, kIssueSuspend>(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u, err, abort_flag))
+          break;
+        tc_fence_after();
+        // [128 x 64] += Q_r[128 x 288] · K_r^T, K-major, 16 per step: 4 latent
+        // chunks (128-byte swizzle) then the RoPE half (64-byte swizzle).
+        const uint64_t dk = kdesc0 + (uint64_t)((st * kStageBytes) >> 4);
+        const uint64_t dr = rdesc0 + (uint64_t)((st * kStageBytes) >> 4);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
+        for (int i = 0; i < 4; ++i)
 #pragma unroll
-              for (int kk = 0; kk < 4; ++kk)
-                mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8, dk + (uint64_t)((i * kChunkBytes + kk * 32) >> 4),
-                       kIdescQK, (i | kk) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk)
+            mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8, dk + (uint64_t)((i * kChunkBytes + kk * 32) >> 4),
+                   kIdescQK, (i | kk) ? 1u : 0u);
 #pragma unroll
-            for (int kk = 0; kk < 2; ++kk)
-              mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, dr + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
-            tc_commit(BAR(B_S_FULL));
-            cq.next();
-            ++tq;
-            progressed = true;
-          }
-        }
-        if (!progressed && tp < tq) {
-          const bool first = cp.first();
-          const bool ready = mbar_test_wait(BAR(B_P_FULL), tp & 1u) &&
-                             (!first || mbar_test_wait(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u));
-          if (ready) {
-            tc_fence_after();
-            // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
-            // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
-            // l[128 x 16] += P · 1 (every column holds the row sum of P), issued
-            // interleaved so consecutive MMAs never share an accumulator.
-            const uint64_t dv = vdesc0 + (uint64_t)(((tp % kStages) * kStageBytes) >> 4);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-              const uint32_t acc = (first && kk == 0) ? 0u : 1u;
-              mma_ts(tmem + kColO, tmem + kColP + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, acc);
-              mma_ts(tmem + kColSum, tmem + kColP + kk * 8, odesc0 + (uint64_t)((kk * 32) >> 4), kIdescSum, acc);
-            }
-            tc_commit(BAR(B_KV_EMPTY + tp % kStages));
-            tc_commit(BAR(B_O_DONE));
-            cp.next();
-            ++tp;
-            progressed = true;
-          }
-        }
-        if (progressed) {
-          spins = 0;
-        } else {
-          if (spins == 0) t_stall = globaltimer();
-          if ((++spins & 255u) == 0u) {
-            if (*abort_flag) break;
-            if (globaltimer() - t_stall > kWaitLimitNs) {
-              atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
-              *abort_flag = 1;
-              break;
-            }
-          }
-        }
+        for (int kk = 0; kk < 2; ++kk)
+          mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, dr + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
+        tc_commit(BAR(B_S_FULL));
+        cq.next();
       }
-      // Every MMA must be finished before TMEM is released.
+      // Every MMA of this thread must be finished before TMEM is released.
       tc_commit(BAR(B_DRAIN));
       wait_phase_drain(BAR(B_DRAIN), 0);
+    }
+    __syncwarp();
+  } else if (warp == 11) {
+    // ---------------------------------------------------------------- P·V issue
+    if (lane == 0) {
+      TileCursor cp;
+      cp.init(a.segs, s_begin, s_end);
+      // The latent chunks read MN-major for P·V, and the ones tile.
+      const uint64_t vdesc0 = sdesc_sw128(base + kOffKV, 8192, 1024);
+      const uint64_t odesc0 = sdesc_sw128(base + kOffOnes, 16, 1024);
+      for (uint32_t tp = 0; cp.valid(); ++tp) {
+        const bool first = cp.first();
+        if (!wait_phase<false, kIssueSuspend>(BAR(B_P_FULL), tp & 1u, err, abort_flag)) break;
+        if (first && !wait_phase<false, kIssueSuspend>(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u, err, abort_flag))
+          break;
+        tc_fence_after();
+        // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
+        // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
+        // l[128 x 16] += P · 1 (every column holds the row sum of P), issued
+        // interleaved so consecutive MMAs never share an accumulator.
+        const uint64_t dv = vdesc0 + (uint64_t)(((tp % kStages) * kStageBytes) >> 4);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+          mma_ts(tmem + kColO, tmem + kColP + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, acc);
+          mma_ts(tmem + kColSum, tmem + kColP + kk * 8, odesc0 + (uint64_t)((kk * 32) >> 4), kIdescSum, acc);
+        }
+        // QK^T(tp) is complete (its scores were read before P(tp) existed), so
+        // this commit frees the page stage once P·V(tp) has read it.
+        tc_commit(BAR(B_KV_EMPTY + tp % kStages));
+        tc_commit(BAR(B_O_DONE));
+        cp.next();
+      }
+      tc_commit(BAR(B_DRAIN_PV));
+      wait_phase_drain(BAR(B_DRAIN_PV), 0);
     }
     __syncwarp();
   } else if (warp == 10) {
@@ -421,7 +413,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // buffer, load the next segment's Q if tile t ends a segment, and push the
     // fp16 log2-scaled partial to the peer.  `own` keeps the rounded values.
     auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[16]) -> bool {
-      bool w = wait_phase(BAR(B_S_FULL), t & 1u, err, abort_flag);
+      bool w = wait_phase<false, true>(BAR(B_S_FULL), t & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
       uint32_t r[32];
@@ -434,7 +426,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
       const uint32_t xb = t & 1u;
       if (t >= 2) {  // the peer has read what was pushed into this buffer two tiles ago
-        w = wait_phase<true>(BAR(B_X_EMPTY0 + xb), ((t - 2) >> 1) & 1u, err, abort_flag);
+        w = wait_phase<true, true>(BAR(B_X_EMPTY0 + xb), ((t - 2) >> 1) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) return false;
       }
       const uint32_t send = base + kOffSend + xb * kXBytes;
@@ -477,7 +469,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // ---- tile g: add the peer's half (fp16, log2 units)
       const uint32_t xb = g & 1u;
       if (leader) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
-      bool w = wait_phase<true>(BAR(B_X_FULL0 + xb), (g >> 1) & 1u, err, abort_flag);
+      bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g >> 1) & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
@@ -518,9 +510,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t slot = pair + 8u * ((xb * 2 + (wg ^ 1)) * kH + h);
         uint2 v = ld_shared_v2_volatile(slot);
         if (v.y != g) {
-          const uint64_t t0 = globaltimer();
+          const uint64_t t0 = cycles();
           for (uint32_t it = 1; (v = ld_shared_v2_volatile(slot)).y != g; ++it) {
-            if ((it & 255u) == 0u && (*abort_flag || globaltimer() - t0 > kWaitLimitNs)) {
+            if ((it & 255u) == 0u && (*abort_flag || cycles() - t0 > kWaitLimitCycles)) {
               if (!*abort_flag) atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
               *abort_flag = 1;
               break;
@@ -547,7 +539,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // P (single TMEM buffer) and a rescale both need P·V of the previous tile done.
       if (g > 0) {
-        w = wait_phase(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
+        w = wait_phase<false, true>(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;

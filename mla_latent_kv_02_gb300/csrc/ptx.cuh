@@ -13,19 +13,23 @@
 namespace mla {
 namespace dev {
 
-// A legitimate wait inside these kernels lasts microseconds; one second means
-// something is wrong, and the kernel stops instead of hanging the GPU.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
+// A legitimate wait inside these kernels lasts microseconds; 2^31 SM cycles
+// (about one second at the 2.07 GHz maximum clock, a few seconds at the
+// lowest clocks) means something is wrong, and the kernel stops instead of
+// hanging the GPU.  Deadlines count %clock64, a per-SM cycle counter that is
+// read in a few cycles, so a wait that ends early pays nothing for its bound.
+constexpr uint64_t kWaitLimitCycles = 1ull << 31;
+
+__device__ __forceinline__ uint64_t cycles() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%clock64;" : "=l"(t));
+  return t;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer() {
-  uint64_t t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
 
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
@@ -104,12 +108,12 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_
     return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
   };
   if (probe()) return true;
-  const uint64_t t0 = globaltimer();
+  const uint64_t t0 = cycles();
   for (uint32_t i = 1;; ++i) {
     if (probe()) return true;
     if ((i & 255u) == 0u) {
       if (*abort_flag) return false;
-      if (globaltimer() - t0 > kWaitLimitNs) {
+      if (cycles() - t0 > kWaitLimitCycles) {
         atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
         *abort_flag = 1;
         return false;
@@ -121,9 +125,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_
 // Bounded wait that ignores the abort flag: used while draining copies that
 // are still in flight before the CTA exits.
 __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) {
-  const uint64_t t0 = globaltimer();
+  const uint64_t t0 = cycles();
   while (!mbar_test_wait(bar, parity)) {
-    if (globaltimer() - t0 > kWaitLimitNs) return;
+    if (cycles() - t0 > kWaitLimitCycles) return;
   }
 }
 
