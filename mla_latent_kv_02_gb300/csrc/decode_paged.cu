@@ -24,9 +24,15 @@
 //    N = 256, B = the same page tile read as an MN-major operand) and the row
 //    sums l += P·1 (N = 16 against a tile of ones), so l matches exactly the
 //    bf16 P the tensor core accumulated.
+//  * Exchange ring: kXBufs receive buffers per CTA; tile t lands in buffer
+//    t mod kXBufs, and the rows this CTA sends for tile t are staged in its own
+//    buffer (t + kXLead) mod kXBufs.  Pushing tile t needs only the peer's tile
+//    t - kXLead to have arrived: that arrival proves the peer's copy out of
+//    the buffer tile t goes to has finished, and that the peer had consumed
+//    what it held.  No release message crosses the cluster.
 //  * Software pipeline: the scores of tile g+1 are read and pushed to the peer
-//    before tile g's softmax runs; the MMA warp issues each QK^T as soon as
-//    its inputs are ready, independently of the P·V order.
+//    before tile g's softmax runs; QK^T and P·V are issued by two warps, each
+//    as soon as its own inputs are ready.
 //  * Two softmax warpgroups split the 64 tokens of a tile (32 each, thread =
 //    head row = TMEM lane); the two threads of a row swap their maxima through
 //    a tagged shared-memory slot.
@@ -34,10 +40,7 @@
 //    when a tile's max exceeds it by more than 8 (log2 units), so P stays
 //    below 256 and O and l in TMEM are rescaled only on those rare tiles.
 //  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + QK^T issue,
-//    warps 2-9 softmax/epilogue, warp 10 tells the peer when a receive buffer
-//    has been read (a cluster-scope release arrive stalls its thread for
-//    hundreds of cycles, so it is kept off the softmax warps), warp 11 P·V
-//    issue.
+//    warps 2-9 softmax/epilogue, warp 10 P·V issue.
 //  * Work: the plan cuts all rows' 64-token tiles into equal contiguous ranges,
 //    one per cluster; a row cut by a boundary is written as fp32 partials
 //    (normalised O and log2-sum-exp) and merged by the combine kernel.
@@ -65,26 +68,28 @@ constexpr int kStages = 4;
 constexpr int kXBytes = kH * kPage * 2;                   // one CTA's fp16 partial S (16 KB)
 constexpr int kXHalf = kXBytes / 2;                       // one warpgroup's 32 tokens
 constexpr int kXWarp = kXHalf / 4;                        // one warp's 32 rows (2 KB)
+constexpr int kXBufs = 4;                                 // exchange ring depth
+constexpr int kXLead = kXBufs - 2;                        // staging buffer offset
+static_assert(kXLead >= 1 && kXLead <= kXBufs - 2, "the exchange ring needs two tiles between staging and reuse");
 constexpr int kOnesBytes = 16 * kChunk * 2;               // [16 x 64] bf16 ones for the row sums
 
 // Shared memory: a small region (barriers, row-max slots, flags) at the
-// start, then the 1024-byte aligned region (page ring, 2 send + 2 receive
-// exchange buffers, the ones tile).
+// start, then the 1024-byte aligned region (page ring, exchange ring, the
+// ones tile).
 constexpr int kNumBars = 32;
 constexpr int kSmallBar = 0;
 constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [2 parity][2 wg][128]: {max bits, tile}
 constexpr int kSmallMisc = kSmallPair + 2 * 2 * kH * 8;
 constexpr int kSmallBytes = kSmallMisc + 64;
 constexpr int kOffKV = 0;
-constexpr int kOffSend = kStages * kStageBytes;
-constexpr int kOffRecv = kOffSend + 2 * kXBytes;
-constexpr int kOffOnes = kOffRecv + 2 * kXBytes;
+constexpr int kOffX = kStages * kStageBytes;
+constexpr int kOffOnes = kOffX + kXBufs * kXBytes;
 constexpr int kAlignedBytes = kOffOnes + kOnesBytes;
 constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 
 constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 480, kTmemCols = 512;
-constexpr int kThreads = 384;
+constexpr int kThreads = 352;
 // The two MMA-issuing threads sleep in mbarrier.try_wait rather than poll.
 constexpr bool kIssueSuspend = true;
 constexpr uint32_t kSoftmaxThreads = 256;
@@ -102,13 +107,8 @@ enum : int {
   B_O_DONE,
   B_Q_READY,
   B_O_FREE,
-  B_X_FULL0,   // receive buffer 0 / 1 filled by the peer
-  B_X_FULL1,
-  B_X_EMPTY0,  // the peer has read what this CTA pushed into its buffer 0 / 1
-  B_X_EMPTY1,
-  B_X_READ0,   // every softmax warp of this CTA has read receive buffer 0 / 1
-  B_X_READ1,
-  B_DRAIN,
+  B_X_FULL0,                      // exchange buffer i filled by the peer
+  B_DRAIN = B_X_FULL0 + kXBufs,
   B_DRAIN_PV,
   B_COUNT
 };
@@ -175,12 +175,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_O_DONE), 1);
     mbar_init(BAR(B_Q_READY), kSoftmaxThreads);
     mbar_init(BAR(B_O_FREE), kSoftmaxThreads);
-    mbar_init(BAR(B_X_FULL0), 1);
-    mbar_init(BAR(B_X_FULL1), 1);
-    mbar_init(BAR(B_X_EMPTY0), 1);
-    mbar_init(BAR(B_X_EMPTY1), 1);
-    mbar_init(BAR(B_X_READ0), 8);
-    mbar_init(BAR(B_X_READ1), 8);
+    for (int i = 0; i < kXBufs; ++i) mbar_init(BAR(B_X_FULL0 + i), 1);
     mbar_init(BAR(B_DRAIN), 1);
     mbar_init(BAR(B_DRAIN_PV), 1);
     fence_mbar_init();
@@ -267,7 +262,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- QK^T issue
     // S_partial(t) = Q_r · K_r(t)^T as soon as page t has landed and the
-    // softmax has read S(t-1).  P·V is issued by its own warp (11), so a long
+    // softmax has read S(t-1).  P·V is issued by its own warp (10), so a long
     // QK^T issue (the tensor pipe throttles it) never delays P·V, nor the
     // other way round; the two streams share only the tensor pipe.
     if (lane == 0) {
@@ -307,7 +302,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wait_phase_drain(BAR(B_DRAIN), 0);
     }
     __syncwarp();
-  } else if (warp == 11) {
+  } else if (warp == 10) {
     // ---------------------------------------------------------------- P·V issue
     if (lane == 0) {
       TileCursor cp;
@@ -340,18 +335,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       tc_commit(BAR(B_DRAIN_PV));
       wait_phase_drain(BAR(B_DRAIN_PV), 0);
-    }
-    __syncwarp();
-  } else if (warp == 10) {
-    // ---------------------------------------------------------------- signaller
-    if (lane == 0) {
-      uint32_t G = 0;
-      for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
-      for (uint32_t g = 0; g < G; ++g) {
-        const uint32_t xb = g & 1u;
-        if (!wait_phase(BAR(B_X_READ0 + xb), (g >> 1) & 1u, err, abort_flag)) break;
-        mbar_arrive_remote(mapa(BAR(B_X_EMPTY0 + xb), peer));
-      }
     }
     __syncwarp();
   } else {
@@ -424,21 +407,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
-      const uint32_t xb = t & 1u;
-      if (t >= 2) {  // the peer has read what was pushed into this buffer two tiles ago
-        w = wait_phase<true, true>(BAR(B_X_EMPTY0 + xb), ((t - 2) >> 1) & 1u, err, abort_flag);
+      // Stage in own buffer (t + kXLead) mod kXBufs, push into the peer's
+      // buffer t mod kXBufs once the peer's tile t - kXLead has landed here.
+      if (t >= (uint32_t)kXLead) {
+        const uint32_t u = t - kXLead;
+        w = wait_phase<true, true>(BAR(B_X_FULL0 + u % kXBufs), (u / kXBufs) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) return false;
       }
-      const uint32_t send = base + kOffSend + xb * kXBytes;
+      const uint32_t stage = base + kOffX + ((t + kXLead) % kXBufs) * kXBytes;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
-        st_shared_v4(send + row_off + (((uint32_t)k ^ swz) << 4), own[4 * k], own[4 * k + 1], own[4 * k + 2],
+        st_shared_v4(stage + row_off + (((uint32_t)k ^ swz) << 4), own[4 * k], own[4 * k + 1], own[4 * k + 2],
                      own[4 * k + 3]);
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0)
-        bulk_copy_to_peer(mapa(base + kOffRecv + xb * kXBytes + warp_off, peer), send + warp_off, (uint32_t)kXWarp,
-                          mapa(BAR(B_X_FULL0 + xb), peer));
+        bulk_copy_to_peer(mapa(base + kOffX + (t % kXBufs) * kXBytes + warp_off, peer), stage + warp_off,
+                          (uint32_t)kXWarp, mapa(BAR(B_X_FULL0 + t % kXBufs), peer));
       return true;
     };
 
@@ -451,6 +436,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     cf.init(a.segs, s_begin, s_end);
     uint32_t own_cur[16], own_nxt[16];
     bool ok = true;
+    if (leader)  // arm the ring: the first kXBufs tiles each expect one peer push
+      for (uint32_t t = 0; t < G && t < (uint32_t)kXBufs; ++t)
+        mbar_arrive_expect_tx(BAR(B_X_FULL0 + t), (uint32_t)kXBytes);
     if (G > 0) {
       load_q(s_begin);
       ok = fetch_push(0, cf, own_cur);
@@ -467,14 +455,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int pg = cf.pg, vis = sg[4];
 
       // ---- tile g: add the peer's half (fp16, log2 units)
-      const uint32_t xb = g & 1u;
-      if (leader) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
-      bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g >> 1) & 1u, err, abort_flag);
+      const uint32_t xb = g % kXBufs, pb = g & 1u;
+      bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
       }
-      const uint32_t recv = base + kOffRecv + xb * kXBytes + row_off;
+      // Re-arm this buffer's barrier for tile g + kXBufs.  That push cannot
+      // land before every warp here has pushed tile g + kXBufs - kXLead, which
+      // each does only after finishing tile g, so no waiter can miss a phase.
+      if (leader && g + kXBufs < G) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
+      const uint32_t recv = base + kOffX + xb * kXBytes + row_off;
       uint32_t sv[16];
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
@@ -484,8 +475,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         sv[4 * k + 2] = as_u32(__hadd2(as_h2(own_cur[4 * k + 2]), as_h2(__float_as_uint(v.z))));
         sv[4 * k + 3] = as_u32(__hadd2(as_h2(own_cur[4 * k + 3]), as_h2(__float_as_uint(v.w))));
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_X_READ0 + xb));  // this warp has read the buffer
 
       // ---- causal/length mask and this half's row max
       const int valid = vis - pg * kPage - wg * 32;
@@ -504,10 +493,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const float mloc = fmaxf(__low2float(mh), __high2float(mh));
 
       // ---- swap maxima with the other thread of this row (tagged slot)
-      st_shared_v2_volatile(pair + 8u * ((xb * 2 + wg) * kH + h), __float_as_uint(mloc), g);
+      st_shared_v2_volatile(pair + 8u * ((pb * 2 + wg) * kH + h), __float_as_uint(mloc), g);
       float mo;
       {
-        const uint32_t slot = pair + 8u * ((xb * 2 + (wg ^ 1)) * kH + h);
+        const uint32_t slot = pair + 8u * ((pb * 2 + (wg ^ 1)) * kH + h);
         uint2 v = ld_shared_v2_volatile(slot);
         if (v.y != g) {
           const uint64_t t0 = cycles();
