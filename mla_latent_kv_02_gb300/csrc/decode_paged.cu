@@ -407,13 +407,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
-      // Stage in own buffer (t + kXLead) mod kXBufs, push into the peer's
-      // buffer t mod kXBufs once the peer's tile t - kXLead has landed here.
-      if (t >= (uint32_t)kXLead) {
-        const uint32_t u = t - kXLead;
-        w = wait_phase<true, true>(BAR(B_X_FULL0 + u % kXBufs), (u / kXBufs) & 1u, err, abort_flag);
-        if (!__all_sync(0xffffffffu, w)) return false;
-      }
+      // Stage in own buffer (t + kXLead) mod kXBufs and push into the peer's
+      // buffer t mod kXBufs.  Both need the peer's tile t - kXLead to have
+      // landed here; this thread already waited for exactly that (with
+      // cluster acquire) when it finished tile t - kXLead, which precedes this
+      // call (kXLead >= 2), so no wait is needed here.
+      static_assert(kXLead >= 2, "tile t - kXLead must be finished before tile t is pushed");
       const uint32_t stage = base + kOffX + ((t + kXLead) % kXBufs) * kXBytes;
 #pragma unroll
       for (int k = 0; k < 4; ++k)
