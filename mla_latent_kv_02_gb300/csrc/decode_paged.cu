@@ -236,11 +236,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const int32_t* bt = a.block_table + (int64_t)b * a.max_pages;
         for (int pg = pb; pg < pe; ++pg) {
           const uint32_t st = g % kStages, use = g / kStages;
+          int32_t pid = __ldg(bt + pg);  // in flight while the stage drains
+          if (pg == pe - 1 && s + 1 < s_end) {
+            // The next segment's query row is read right after this segment's
+            // last QK^T: warm L2 with it (each CTA one half of q_abs[row],
+            // CTA 0 also q_r[row]) so that load is not a DRAM round trip.
+            const size_t qrow = (size_t)a.segs[8 * (s + 1)];
+            const uint8_t* qa = reinterpret_cast<const uint8_t*>(a.q_abs) + qrow * (kH * kDC * 2);
+            prefetch_l2_bulk(qa + rank * (kH * kDC), kH * kDC);
+            if (rank == 0) prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.q_r) + qrow * (kH * kDR * 2), kH * kDR * 2);
+          }
           if (use > 0 && !wait_phase<false, true>(BAR(B_KV_EMPTY + st), (use - 1) & 1u, err, abort_flag)) {
             ok = false;
             break;
           }
-          int32_t pid = __ldg(bt + pg);
           if (pid < 0 || (int64_t)pid >= a.num_pages) {
             atomicOr(err, (int32_t)MLA_DEVERR_PAGE_OOB);
             pid = 0;
@@ -444,18 +453,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     float m = -INFINITY;
     for (uint32_t g = 0; g < G && ok; ++g) {
+      // Iteration g finishes tile g and fetches/pushes tile g+1, ordered so
+      // that the latencies of one overlap work of the other: the barrier
+      // tests are issued up front and consumed later, and tile g+1's fetch
+      // and push run between publishing this thread's row max and reading
+      // the other warpgroup's.
       TileCursor cn = cf;
       cn.next();
-      if (g + 1 < G && !fetch_push(g + 1, cn, own_nxt)) {
-        ok = false;
-        break;
-      }
+      const bool has_next = g + 1 < G;
+      const uint32_t xb = g % kXBufs, pb = g & 1u;
+      const bool xf_ready = mbar_test_wait_cluster(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u);
       const int32_t* sg = a.segs + 8 * cf.s;
       const int pg = cf.pg, vis = sg[4];
 
       // ---- tile g: add the peer's half (fp16, log2 units)
-      const uint32_t xb = g % kXBufs, pb = g & 1u;
-      bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
+      bool w = xf_ready || wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
@@ -490,9 +502,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         mx[j] = __hmax2(__hmax2(as_h2(sv[4 * j]), as_h2(sv[4 * j + 1])), __hmax2(as_h2(sv[4 * j + 2]), as_h2(sv[4 * j + 3])));
       const __half2 mh = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
       const float mloc = fmaxf(__low2float(mh), __high2float(mh));
-
-      // ---- swap maxima with the other thread of this row (tagged slot)
+      // publish this half's max for the other thread of the row (tagged slot)
       st_shared_v2_volatile(pair + 8u * ((pb * 2 + wg) * kH + h), __float_as_uint(mloc), g);
+
+      // ---- tile g+1: fetch this CTA's partial scores and push them to the peer
+      if (has_next && !fetch_push(g + 1, cn, own_nxt)) {
+        ok = false;
+        break;
+      }
+
+      // ---- tile g: the other half's max, then the reference max m
+      const bool od_ready = (g == 0) || mbar_test_wait(BAR(B_O_DONE), (g - 1) & 1u);
       float mo;
       {
         const uint32_t slot = pair + 8u * ((pb * 2 + (wg ^ 1)) * kH + h);
@@ -525,9 +545,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         m = mt;
         resc = true;
       }
-      // P (single TMEM buffer) and a rescale both need P·V of the previous tile done.
+      // P = 2^(s - m) in fp16 pairs, stored as bf16 for the tensor core.
+      const __half2 m2 = __float2half2_rn(m);  // m is a max of fp16 values: exact
+      uint32_t pk[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hsub2(as_h2(sv[j]), m2)))));
+        pk[j] = pack_bf16x2(p.x, p.y);
+      }
+      // Writing P (single TMEM buffer) and a rescale both need P·V of tile g-1 done.
       if (g > 0) {
-        w = wait_phase<false, true>(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
+        w = od_ready || wait_phase<false, true>(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
@@ -544,14 +572,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           tmem_st32(tl + kColO + wg * 128 + c, o);
         }
         if (wg == 0) tmem_st1(tl + kColSum, __float_as_uint(__uint_as_float(tmem_ld1_sync(tl + kColSum)) * factor));
-      }
-      // P = 2^(s - m) in fp16 pairs, stored as bf16 for the tensor core.
-      const __half2 m2 = __float2half2_rn(m);  // m is a max of fp16 values: exact
-      uint32_t pk[16];
-#pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hsub2(as_h2(sv[j]), m2)))));
-        pk[j] = pack_bf16x2(p.x, p.y);
       }
       tmem_st16(tl + kColP + wg * 16, pk);
       tmem_st_wait();
