@@ -114,10 +114,11 @@ enum : int {
 };
 static_assert(B_COUNT <= kNumBars, "barrier area too small");
 
-// Walks the 64-token tiles of a cluster's segments in order.
+// Walks the 64-token tiles of a cluster's segments in order; a segment's
+// fields are read from the plan once, when the cursor enters it.
 struct TileCursor {
   const int32_t* segs;
-  int s, s_end, pg, pb, pe;
+  int s, s_end, pg, pb, pe, row, vis, slot;
   __device__ __forceinline__ void init(const int32_t* sg, int sb, int se) {
     segs = sg;
     s = sb;
@@ -125,8 +126,14 @@ struct TileCursor {
     if (s < s_end) load();
   }
   __device__ __forceinline__ void load() {
-    pb = segs[8 * s + 2];
-    pe = segs[8 * s + 3];
+    // {row, b, page_begin, page_end} and {visible, out_slot, 0, 0}: 16-byte aligned
+    const int4 lo = __ldg(reinterpret_cast<const int4*>(segs + 8 * s));
+    const int4 hi = __ldg(reinterpret_cast<const int4*>(segs + 8 * s) + 1);
+    row = lo.x;
+    pb = lo.z;
+    pe = lo.w;
+    vis = hi.x;
+    slot = hi.y;
     pg = pb;
   }
   __device__ __forceinline__ bool valid() const { return s < s_end; }
@@ -463,8 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const bool has_next = g + 1 < G;
       const uint32_t xb = g % kXBufs, pb = g & 1u;
       const bool xf_ready = mbar_test_wait_cluster(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u);
-      const int32_t* sg = a.segs + 8 * cf.s;
-      const int pg = cf.pg, vis = sg[4];
+      const int pg = cf.pg, vis = cf.vis;
 
       // ---- tile g: add the peer's half (fp16, log2 units)
       bool w = xf_ready || wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
@@ -580,7 +586,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
       if (cf.last()) {
         // ---- epilogue of this segment: wait for its last P·V, normalise, store
-        const int row = sg[0], slot = sg[5];
+        const int row = cf.row, slot = cf.slot;
         w = wait_phase(BAR(B_O_DONE), g & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
