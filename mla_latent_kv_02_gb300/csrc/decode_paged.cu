@@ -33,14 +33,14 @@
 //  * Software pipeline: the scores of tile g+1 are read and pushed to the peer
 //    before tile g's softmax runs; QK^T and P·V are issued by two warps, each
 //    as soon as its own inputs are ready.
-//  * Two softmax warpgroups split the 64 tokens of a tile (32 each, thread =
-//    head row = TMEM lane); the two threads of a row swap their maxima through
-//    a tagged shared-memory slot.
+//  * kSWG softmax warpgroups split the 64 tokens of a tile (kCols each, thread
+//    = head row = TMEM lane); the threads of a row share their slice maxima
+//    through tagged shared-memory slots.
 //  * Online softmax with lazy rescaling: the running reference max only moves
 //    when a tile's max exceeds it by more than 8 (log2 units), so P stays
 //    below 256 and O and l in TMEM are rescaled only on those rare tiles.
 //  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + QK^T issue,
-//    warps 2-9 softmax/epilogue, warp 10 P·V issue.
+//    warps 2 .. 2+kSWarps-1 softmax/epilogue, the last warp P·V issue.
 //  * Work: the plan cuts all rows' 64-token tiles into equal contiguous ranges,
 //    one per cluster; a row cut by a boundary is written as fp32 partials
 //    (normalised O and log2-sum-exp) and merged by the combine kernel.
@@ -66,8 +66,18 @@ constexpr int kRopeBytes = kPage * kRopeHalf * 2;         // [64 tokens x 32] bf
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes; // 36 KB
 constexpr int kStages = 4;
 constexpr int kXBytes = kH * kPage * 2;                   // one CTA's fp16 partial S (16 KB)
-constexpr int kXHalf = kXBytes / 2;                       // one warpgroup's 32 tokens
-constexpr int kXWarp = kXHalf / 4;                        // one warp's 32 rows (2 KB)
+// Softmax: kSWG warpgroups split the 64 tokens of a tile, kCols per thread.
+constexpr int kSWG = 2;
+constexpr int kSWarps = 4 * kSWG;
+constexpr int kCols = kPage / kSWG;                       // tokens of a tile per softmax thread
+constexpr int kWords = kCols / 2;                         // fp16x2 words per thread
+constexpr int kRowChunks = kCols * 2 / 16;                // 16-byte chunks of a thread's row slice
+constexpr int kSwzShift = kRowChunks == 4 ? 1 : 2;        // chunk swizzle: conflict-free 16-byte accesses
+static_assert(kRowChunks == 4 || kRowChunks == 2, "16 or 32 tokens per softmax thread");
+constexpr int kOCols = 256 / kSWG;                        // O columns per softmax thread (rescale, epilogue)
+constexpr int kQCols = 128 / kSWG;                        // latent Q TMEM columns loaded per warpgroup
+constexpr int kXSlice = kXBytes / kSWG;                   // one warpgroup's tokens, all rows
+constexpr int kXWarp = kXSlice / 4;                       // one warp's 32 rows
 constexpr int kXBufs = 4;                                 // exchange ring depth
 constexpr int kXLead = kXBufs - 2;                        // staging buffer offset
 static_assert(kXLead >= 1 && kXLead <= kXBufs - 2, "the exchange ring needs two tiles between staging and reuse");
@@ -78,8 +88,8 @@ constexpr int kOnesBytes = 16 * kChunk * 2;               // [16 x 64] bf16 ones
 // ones tile).
 constexpr int kNumBars = 32;
 constexpr int kSmallBar = 0;
-constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [2 parity][2 wg][128]: {max bits, tile}
-constexpr int kSmallMisc = kSmallPair + 2 * 2 * kH * 8;
+constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [2 parity][kSWG][128]: {max bits, tile}
+constexpr int kSmallMisc = kSmallPair + 2 * kSWG * kH * 8;
 constexpr int kSmallBytes = kSmallMisc + 64;
 constexpr int kOffKV = 0;
 constexpr int kOffX = kStages * kStageBytes;
@@ -89,10 +99,11 @@ constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 
 constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 480, kTmemCols = 512;
-constexpr int kThreads = 352;
+constexpr int kPvWarp = 2 + kSWarps;                      // warps: producer, QK^T, softmax..., P·V
+constexpr int kThreads = 32 * (kPvWarp + 1);
 // The two MMA-issuing threads sleep in mbarrier.try_wait rather than poll.
 constexpr bool kIssueSuspend = true;
-constexpr uint32_t kSoftmaxThreads = 256;
+constexpr uint32_t kSoftmaxThreads = 128 * kSWG;
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
@@ -146,6 +157,17 @@ struct TileCursor {
     }
   }
 };
+
+__device__ __forceinline__ __half2 hmax_tree(const __half2 (&m)[4]) {
+  return __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
+}
+__device__ __forceinline__ __half2 hmax_tree(const __half2 (&m)[2]) { return __hmax2(m[0], m[1]); }
+
+// TMEM access sized by the array: a thread's score slice and its P words.
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32_sync(taddr, r); }
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16_sync(taddr, r); }
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[8]) { tmem_st8(taddr, r); }
 
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
@@ -208,7 +230,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   // Row-max slots start with an impossible tile tag; the ones tile feeds the
   // row-sum MMA (written by the generic proxy, read by the tensor core).
-  for (int i = threadIdx.x; i < 2 * 2 * kH; i += kThreads) st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
+  for (int i = threadIdx.x; i < 2 * kSWG * kH; i += kThreads) st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
   if (layout_fits) {
     uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + kOffOnes);
     for (int i = threadIdx.x; i < kOnesBytes / 4; i += kThreads) ones[i] = 0x3F803F80u;  // bf16 1.0 pairs
@@ -278,7 +300,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ---------------------------------------------------------------- QK^T issue
     // S_partial(t) = Q_r · K_r(t)^T as soon as page t has landed and the
-    // softmax has read S(t-1).  P·V is issued by its own warp (10), so a long
+    // softmax has read S(t-1).  P·V is issued by its own warp, so a long
     // QK^T issue (the tensor pipe throttles it) never delays P·V, nor the
     // other way round; the two streams share only the tensor pipe.
     if (lane == 0) {
@@ -318,7 +340,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wait_phase_drain(BAR(B_DRAIN), 0);
     }
     __syncwarp();
-  } else if (warp == 10) {
+  } else if (warp == kPvWarp) {
     // ---------------------------------------------------------------- P·V issue
     if (lane == 0) {
       TileCursor cp;
@@ -355,33 +377,36 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
-    const int sw = warp - 2;                 // 0..7
-    const int wg = sw >> 2;                  // warpgroup: tokens [32 wg, 32 wg + 32) of each tile
+    const int sw = warp - 2;                 // 0 .. kSWarps-1
+    const int wg = sw >> 2;                  // warpgroup: tokens [kCols wg, kCols wg + kCols) of each tile
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
     const int h = q4 * 32 + lane;            // head row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
-    const uint32_t swz = (uint32_t)((h >> 1) & 3);
-    const uint32_t row_off = (uint32_t)(wg * kXHalf + h * 64);
-    const uint32_t warp_off = (uint32_t)(wg * kXHalf + q4 * kXWarp);
+    const uint32_t swz = (uint32_t)((h >> kSwzShift) & (kRowChunks - 1));
+    const uint32_t row_off = (uint32_t)(wg * kXSlice + h * (kCols * 2));
+    const uint32_t warp_off = (uint32_t)(wg * kXSlice + q4 * kXWarp);
     const bool leader = (sw == 0 && lane == 0);
     const float c2 = a.scale_log2;
     __syncwarp();
 
-    // Q_r of a row into TMEM: warpgroup 0 loads latent chunks 0-1, warpgroup 1
-    // latent chunks 2-3 and the RoPE half; all loads issued before any store.
+    // Q_r of a row into TMEM: warpgroup w loads latent columns [kQCols w,
+    // kQCols (w+1)) of this CTA's half, the last warpgroup also the RoPE half;
+    // all loads are issued before any store.
     auto load_q = [&](int s) {
+      constexpr int kLat = kQCols / 4;  // 16-byte pieces of the latent slice
       const int row = a.segs[8 * s];
-      const uint4* lat = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256) + wg * 16;
-      uint4 v[20];
+      const uint4* lat =
+          reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256) + wg * kLat;
+      uint4 v[kLat + 4];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) v[j] = __ldg(lat + j);
-      if (wg == 1) {
+      for (int j = 0; j < kLat; ++j) v[j] = __ldg(lat + j);
+      if (wg == kSWG - 1) {
         const uint4* rp = reinterpret_cast<const uint4*>(a.q_r + ((size_t)row * kH + h) * kDR + rank * kRopeHalf);
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[16 + j] = __ldg(rp + j);
+        for (int j = 0; j < 4; ++j) v[kLat + j] = __ldg(rp + j);
       }
 #pragma unroll
-      for (int ci = 0; ci < 2; ++ci) {
+      for (int ci = 0; ci < kQCols / 32; ++ci) {
         uint32_t r[32];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -390,16 +415,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           r[4 * j + 2] = v[ci * 8 + j].z;
           r[4 * j + 3] = v[ci * 8 + j].w;
         }
-        tmem_st32(tl + kColQ + (wg * 2 + ci) * 32, r);
+        tmem_st32(tl + kColQ + wg * kQCols + ci * 32, r);
       }
-      if (wg == 1) {
+      if (wg == kSWG - 1) {
         uint32_t r[16];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          r[4 * j] = v[16 + j].x;
-          r[4 * j + 1] = v[16 + j].y;
-          r[4 * j + 2] = v[16 + j].z;
-          r[4 * j + 3] = v[16 + j].w;
+          r[4 * j] = v[kLat + j].x;
+          r[4 * j + 1] = v[kLat + j].y;
+          r[4 * j + 2] = v[kLat + j].z;
+          r[4 * j + 3] = v[kLat + j].w;
         }
         tmem_st16(tl + kColQ + 128, r);
       }
@@ -408,20 +433,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_arrive(BAR(B_Q_READY));
     };
 
-    // Read this warpgroup's 32 columns of tile t's partial scores, free the S
+    // Read this warpgroup's kCols columns of tile t's partial scores, free the S
     // buffer, load the next segment's Q if tile t ends a segment, and push the
     // fp16 log2-scaled partial to the peer.  `own` keeps the rounded values.
-    auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[16]) -> bool {
+    auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[kWords]) -> bool {
       bool w = wait_phase<false, true>(BAR(B_S_FULL), t & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
-      uint32_t r[32];
-      tmem_ld32_sync(tl + kColS + wg * 32, r);
+      uint32_t r[kCols];
+      tmem_ld_cols(tl + kColS + wg * kCols, r);
       tc_fence_before();
       mbar_arrive(BAR(B_S_FREE));
       if (c.last() && c.s + 1 < c.s_end) load_q(c.s + 1);  // every QK^T of this segment is done
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
+      for (int j = 0; j < kWords; ++j)
         own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
       // Stage in own buffer (t + kXLead) mod kXBufs and push into the peer's
       // buffer t mod kXBufs.  Both need the peer's tile t - kXLead to have
@@ -431,7 +456,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       static_assert(kXLead >= 2, "tile t - kXLead must be finished before tile t is pushed");
       const uint32_t stage = base + kOffX + ((t + kXLead) % kXBufs) * kXBytes;
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
+      for (int k = 0; k < kRowChunks; ++k)
         st_shared_v4(stage + row_off + (((uint32_t)k ^ swz) << 4), own[4 * k], own[4 * k + 1], own[4 * k + 2],
                      own[4 * k + 3]);
       fence_proxy_async_smem();
@@ -449,7 +474,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_arrive(BAR(B_O_FREE));  // O is free for the first segment
     TileCursor cf;               // the tile being finished
     cf.init(a.segs, s_begin, s_end);
-    uint32_t own_cur[16], own_nxt[16];
+    uint32_t own_cur[kWords], own_nxt[kWords];
     bool ok = true;
     if (leader)  // arm the ring: the first kXBufs tiles each expect one peer push
       for (uint32_t t = 0; t < G && t < (uint32_t)kXBufs; ++t)
@@ -483,9 +508,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // each does only after finishing tile g, so no waiter can miss a phase.
       if (leader && g + kXBufs < G) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
       const uint32_t recv = base + kOffX + xb * kXBytes + row_off;
-      uint32_t sv[16];
+      uint32_t sv[kWords];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
+      for (int k = 0; k < kRowChunks; ++k) {
         const float4 v = ld_shared_v4(recv + (((uint32_t)k ^ swz) << 4));
         sv[4 * k] = as_u32(__hadd2(as_h2(own_cur[4 * k]), as_h2(__float_as_uint(v.x))));
         sv[4 * k + 1] = as_u32(__hadd2(as_h2(own_cur[4 * k + 1]), as_h2(__float_as_uint(v.y))));
@@ -494,22 +519,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
 
       // ---- causal/length mask and this half's row max
-      const int valid = vis - pg * kPage - wg * 32;
-      if (valid < 32) {
+      const int valid = vis - pg * kPage - wg * kCols;
+      if (valid < kCols) {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
+        for (int j = 0; j < kWords; ++j) {
           if (2 * j >= valid) sv[j] = (sv[j] & 0xFFFF0000u) | 0xFC00u;          // low half -> -inf
           if (2 * j + 1 >= valid) sv[j] = (sv[j] & 0x0000FFFFu) | 0xFC000000u;  // high half -> -inf
         }
       }
-      __half2 mx[4];
+      __half2 mx[kWords / 4];
 #pragma unroll
-      for (int j = 0; j < 4; ++j)
+      for (int j = 0; j < kWords / 4; ++j)
         mx[j] = __hmax2(__hmax2(as_h2(sv[4 * j]), as_h2(sv[4 * j + 1])), __hmax2(as_h2(sv[4 * j + 2]), as_h2(sv[4 * j + 3])));
-      const __half2 mh = __hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3]));
+      const __half2 mh = hmax_tree(mx);
       const float mloc = fmaxf(__low2float(mh), __high2float(mh));
-      // publish this half's max for the other thread of the row (tagged slot)
-      st_shared_v2_volatile(pair + 8u * ((pb * 2 + wg) * kH + h), __float_as_uint(mloc), g);
+      // publish this slice's max for the other threads of the row (tagged slot)
+      st_shared_v2_volatile(pair + 8u * ((pb * kSWG + wg) * kH + h), __float_as_uint(mloc), g);
 
       // ---- tile g+1: fetch this CTA's partial scores and push them to the peer
       if (has_next && !fetch_push(g + 1, cn, own_nxt)) {
@@ -517,11 +542,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         break;
       }
 
-      // ---- tile g: the other half's max, then the reference max m
+      // ---- tile g: the other warpgroups' maxima, then the reference max m
       const bool od_ready = (g == 0) || mbar_test_wait(BAR(B_O_DONE), (g - 1) & 1u);
-      float mo;
-      {
-        const uint32_t slot = pair + 8u * ((pb * 2 + (wg ^ 1)) * kH + h);
+      float mo = -INFINITY;
+      w = true;
+#pragma unroll
+      for (int o = 1; o < kSWG; ++o) {
+        const uint32_t slot = pair + 8u * ((pb * kSWG + ((wg + o) % kSWG)) * kH + h);
         uint2 v = ld_shared_v2_volatile(slot);
         if (v.y != g) {
           const uint64_t t0 = cycles();
@@ -533,8 +560,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
-        mo = __uint_as_float(v.x);
-        w = (v.y == g);
+        mo = fmaxf(mo, __uint_as_float(v.x));
+        w = w && (v.y == g);
       }
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
@@ -553,9 +580,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       // P = 2^(s - m) in fp16 pairs, stored as bf16 for the tensor core.
       const __half2 m2 = __float2half2_rn(m);  // m is a max of fp16 values: exact
-      uint32_t pk[16];
+      uint32_t pk[kWords];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
+      for (int j = 0; j < kWords; ++j) {
         const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hsub2(as_h2(sv[j]), m2)))));
         pk[j] = pack_bf16x2(p.x, p.y);
       }
@@ -570,16 +597,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
+        for (int c = 0; c < kOCols; c += 32) {
           uint32_t o[32];
-          tmem_ld32_sync(tl + kColO + wg * 128 + c, o);
+          tmem_ld32_sync(tl + kColO + wg * kOCols + c, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-          tmem_st32(tl + kColO + wg * 128 + c, o);
+          tmem_st32(tl + kColO + wg * kOCols + c, o);
         }
         if (wg == 0) tmem_st1(tl + kColSum, __float_as_uint(__uint_as_float(tmem_ld1_sync(tl + kColSum)) * factor));
       }
-      tmem_st16(tl + kColP + wg * 16, pk);
+      tmem_st_cols(tl + kColP + wg * kWords, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(BAR(B_P_FULL));
@@ -596,11 +623,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float lt = __uint_as_float(tmem_ld1_sync(tl + kColSum));
         const float inv = 1.f / lt;
         if (slot < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256 + wg * 128);
+          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256 + wg * kOCols);
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 32) {
+          for (int c = 0; c < kOCols; c += 32) {
             uint32_t o[32];
-            tmem_ld32_sync(tl + kColO + wg * 128 + c, o);
+            tmem_ld32_sync(tl + kColO + wg * kOCols + c, o);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               dst[c / 8 + v] = make_uint4(
@@ -610,11 +637,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * kH + h) * kDC + rank * 256 + wg * 128);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * kH + h) * kDC + rank * 256 + wg * kOCols);
 #pragma unroll 1
-          for (int c = 0; c < 128; c += 32) {
+          for (int c = 0; c < kOCols; c += 32) {
             uint32_t o[32];
-            tmem_ld32_sync(tl + kColO + wg * 128 + c, o);
+            tmem_ld32_sync(tl + kColO + wg * kOCols + c, o);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[c / 4 + v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
@@ -633,7 +660,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
       }
 #pragma unroll
-      for (int j = 0; j < 16; ++j) own_cur[j] = own_nxt[j];
+      for (int j = 0; j < kWords; ++j) own_cur[j] = own_nxt[j];
       cf = cn;
     }
   }

@@ -353,6 +353,20 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
                :
                : "memory");
 }
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+               MLA_W8(r, 0)
+               : "memory");
+}
+// Load 16 columns and wait for completion (registers tied to the wait).
+__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : MLA_R8(r, 0), MLA_R8(r, 8)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" : MLA_RW8(r, 0), MLA_RW8(r, 8) : : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // fp16x2 of two values, saturating to the finite fp16 range (no infinities).
