@@ -30,17 +30,17 @@
 //    t - kXLead to have arrived: that arrival proves the peer's copy out of
 //    the buffer tile t goes to has finished, and that the peer had consumed
 //    what it held.  No release message crosses the cluster.
-//  * Software pipeline: the scores of tile g+1 are read and pushed to the peer
-//    before tile g's softmax runs; QK^T and P·V are issued by two warps, each
-//    as soon as its own inputs are ready.
-//  * kSWG softmax warpgroups split the 64 tokens of a tile (kCols each, thread
-//    = head row = TMEM lane); the threads of a row share their slice maxima
-//    through tagged shared-memory slots.
+//  * Two softmax warpgroups take alternate tiles, each tile whole (thread =
+//    head row = TMEM lane, all 64 tokens): while one waits for the peer's half
+//    of its tile, the other computes.  The only hand-off between them is the
+//    row's reference max, passed from tile g-1 to tile g through a tagged
+//    shared-memory slot.  QK^T and P·V are issued by two warps, each as soon
+//    as its own inputs are ready.
 //  * Online softmax with lazy rescaling: the running reference max only moves
 //    when a tile's max exceeds it by more than 8 (log2 units), so P stays
 //    below 256 and O and l in TMEM are rescaled only on those rare tiles.
 //  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + QK^T issue,
-//    warps 2 .. 2+kSWarps-1 softmax/epilogue, the last warp P·V issue.
+//    warps 2-9 softmax/epilogue (two warpgroups), warp 10 P·V issue.
 //  * Work: the plan cuts all rows' 64-token tiles into equal contiguous ranges,
 //    one per cluster; a row cut by a boundary is written as fp32 partials
 //    (normalised O and log2-sum-exp) and merged by the combine kernel.
@@ -66,18 +66,11 @@ constexpr int kRopeBytes = kPage * kRopeHalf * 2;         // [64 tokens x 32] bf
 constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes; // 36 KB
 constexpr int kStages = 4;
 constexpr int kXBytes = kH * kPage * 2;                   // one CTA's fp16 partial S (16 KB)
-// Softmax: kSWG warpgroups split the 64 tokens of a tile, kCols per thread.
-constexpr int kSWG = 2;
-constexpr int kSWarps = 4 * kSWG;
-constexpr int kCols = kPage / kSWG;                       // tokens of a tile per softmax thread
-constexpr int kWords = kCols / 2;                         // fp16x2 words per thread
-constexpr int kRowChunks = kCols * 2 / 16;                // 16-byte chunks of a thread's row slice
-constexpr int kSwzShift = kRowChunks == 4 ? 1 : 2;        // chunk swizzle: conflict-free 16-byte accesses
-static_assert(kRowChunks == 4 || kRowChunks == 2, "16 or 32 tokens per softmax thread");
-constexpr int kOCols = 256 / kSWG;                        // O columns per softmax thread (rescale, epilogue)
-constexpr int kQCols = 128 / kSWG;                        // latent Q TMEM columns loaded per warpgroup
-constexpr int kXSlice = kXBytes / kSWG;                   // one warpgroup's tokens, all rows
-constexpr int kXWarp = kXSlice / 4;                       // one warp's 32 rows
+// Softmax: two warpgroups take alternate tiles whole (thread = head row).
+constexpr int kSWarps = 8;
+constexpr int kWords = kPage / 2;                         // fp16x2 words of a row's 64 scores
+constexpr int kXRow = kPage * 2;                          // one row of a partial S tile (128 bytes)
+constexpr int kXWarp = 32 * kXRow;                        // one warp's 32 rows (4 KB)
 constexpr int kXBufs = 4;                                 // exchange ring depth
 constexpr int kXLead = kXBufs - 2;                        // staging buffer offset
 static_assert(kXLead >= 1 && kXLead <= kXBufs - 2, "the exchange ring needs two tiles between staging and reuse");
@@ -88,8 +81,8 @@ constexpr int kOnesBytes = 16 * kChunk * 2;               // [16 x 64] bf16 ones
 // ones tile).
 constexpr int kNumBars = 32;
 constexpr int kSmallBar = 0;
-constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [2 parity][kSWG][128]: {max bits, tile}
-constexpr int kSmallMisc = kSmallPair + 2 * kSWG * kH * 8;
+constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [4][128]: {reference max bits, tile}
+constexpr int kSmallMisc = kSmallPair + 4 * kH * 8;
 constexpr int kSmallBytes = kSmallMisc + 64;
 constexpr int kOffKV = 0;
 constexpr int kOffX = kStages * kStageBytes;
@@ -103,7 +96,7 @@ constexpr int kPvWarp = 2 + kSWarps;                      // warps: producer, QK
 constexpr int kThreads = 32 * (kPvWarp + 1);
 // The two MMA-issuing threads sleep in mbarrier.try_wait rather than poll.
 constexpr bool kIssueSuspend = true;
-constexpr uint32_t kSoftmaxThreads = 128 * kSWG;
+constexpr uint32_t kTileThreads = 128;                    // the warpgroup that handles one tile
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
@@ -112,10 +105,15 @@ constexpr uint32_t kIdescSum = idesc_bf16_f32(128, 16, false, false);
 enum : int {
   B_KV_FULL = 0,
   B_KV_EMPTY = kStages,
-  B_S_FULL = 2 * kStages,
+  // S_FULL and O_DONE come in pairs by tile parity: each softmax warpgroup
+  // waits only on its own tiles' phases, in order (a parity test cannot tell
+  // a phase from the one two before it, and the warpgroups run apart).
+  B_S_FULL0 = 2 * kStages,
+  B_S_FULL1,
   B_S_FREE,
   B_P_FULL,
-  B_O_DONE,
+  B_O_DONE0,
+  B_O_DONE1,
   B_Q_READY,
   B_O_FREE,
   B_X_FULL0,                      // exchange buffer i filled by the peer
@@ -158,17 +156,6 @@ struct TileCursor {
   }
 };
 
-__device__ __forceinline__ __half2 hmax_tree(const __half2 (&m)[4]) {
-  return __hmax2(__hmax2(m[0], m[1]), __hmax2(m[2], m[3]));
-}
-__device__ __forceinline__ __half2 hmax_tree(const __half2 (&m)[2]) { return __hmax2(m[0], m[1]); }
-
-// TMEM access sized by the array: a thread's score slice and its P words.
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32_sync(taddr, r); }
-__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16_sync(taddr, r); }
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
-__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const uint32_t (&r)[8]) { tmem_st8(taddr, r); }
-
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 
@@ -198,12 +185,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(BAR(B_KV_FULL + i), 1);
       mbar_init(BAR(B_KV_EMPTY + i), 1);
     }
-    mbar_init(BAR(B_S_FULL), 1);
-    mbar_init(BAR(B_S_FREE), kSoftmaxThreads);
-    mbar_init(BAR(B_P_FULL), kSoftmaxThreads);
-    mbar_init(BAR(B_O_DONE), 1);
-    mbar_init(BAR(B_Q_READY), kSoftmaxThreads);
-    mbar_init(BAR(B_O_FREE), kSoftmaxThreads);
+    mbar_init(BAR(B_S_FULL0), 1);
+    mbar_init(BAR(B_S_FULL1), 1);
+    mbar_init(BAR(B_S_FREE), kTileThreads);
+    mbar_init(BAR(B_P_FULL), kTileThreads);
+    mbar_init(BAR(B_O_DONE0), 1);
+    mbar_init(BAR(B_O_DONE1), 1);
+    mbar_init(BAR(B_Q_READY), kTileThreads);
+    mbar_init(BAR(B_O_FREE), kTileThreads);
     for (int i = 0; i < kXBufs; ++i) mbar_init(BAR(B_X_FULL0 + i), 1);
     mbar_init(BAR(B_DRAIN), 1);
     mbar_init(BAR(B_DRAIN_PV), 1);
@@ -230,7 +219,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   }
   // Row-max slots start with an impossible tile tag; the ones tile feeds the
   // row-sum MMA (written by the generic proxy, read by the tensor core).
-  for (int i = threadIdx.x; i < 2 * kSWG * kH; i += kThreads) st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
+  for (int i = threadIdx.x; i < 4 * kH; i += kThreads) st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
   if (layout_fits) {
     uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + kOffOnes);
     for (int i = threadIdx.x; i < kOnesBytes / 4; i += kThreads) ones[i] = 0x3F803F80u;  // bf16 1.0 pairs
@@ -332,7 +321,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)
           mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, dr + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
-        tc_commit(BAR(B_S_FULL));
+        tc_commit(BAR(B_S_FULL0 + (tq & 1u)));
         cq.next();
       }
       // Every MMA of this thread must be finished before TMEM is released.
@@ -368,7 +357,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         // QK^T(tp) is complete (its scores were read before P(tp) existed), so
         // this commit frees the page stage once P·V(tp) has read it.
         tc_commit(BAR(B_KV_EMPTY + tp % kStages));
-        tc_commit(BAR(B_O_DONE));
+        tc_commit(BAR(B_O_DONE0 + (tp & 1u)));
         cp.next();
       }
       tc_commit(BAR(B_DRAIN_PV));
@@ -377,86 +366,91 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax + epilogue
+    // Warpgroup wg (warps 2-5, 6-9) takes the tiles g with g % 2 == wg, whole:
+    // thread = head row = TMEM lane, all 64 tokens.  The only hand-off between
+    // the warpgroups is the row's reference max, passed from tile g-1 to g.
     const int sw = warp - 2;                 // 0 .. kSWarps-1
-    const int wg = sw >> 2;                  // warpgroup: tokens [kCols wg, kCols wg + kCols) of each tile
+    const int wg = sw >> 2;
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
     const int h = q4 * 32 + lane;            // head row = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(q4 * 32) << 16);
-    const uint32_t swz = (uint32_t)((h >> kSwzShift) & (kRowChunks - 1));
-    const uint32_t row_off = (uint32_t)(wg * kXSlice + h * (kCols * 2));
-    const uint32_t warp_off = (uint32_t)(wg * kXSlice + q4 * kXWarp);
-    const bool leader = (sw == 0 && lane == 0);
+    const uint32_t swz = (uint32_t)(h & 7);  // 128-byte rows: 16-byte chunk k sits at k ^ (h & 7)
+    const uint32_t row_off = (uint32_t)(h * kXRow);
+    const uint32_t warp_off = (uint32_t)(q4 * kXWarp);
+    const bool wg_leader = ((sw & 3) == 0 && lane == 0);
     const float c2 = a.scale_log2;
     __syncwarp();
 
-    // Q_r of a row into TMEM: warpgroup w loads latent columns [kQCols w,
-    // kQCols (w+1)) of this CTA's half, the last warpgroup also the RoPE half;
-    // all loads are issued before any store.
+    // Q_r of a segment's row into TMEM, this thread's row (144 columns), in
+    // two rounds of loads so that at most 20 16-byte values are live.
     auto load_q = [&](int s) {
-      constexpr int kLat = kQCols / 4;  // 16-byte pieces of the latent slice
       const int row = a.segs[8 * s];
-      const uint4* lat =
-          reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256) + wg * kLat;
-      uint4 v[kLat + 4];
+      const uint4* lat = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256);
+      const uint4* rp = reinterpret_cast<const uint4*>(a.q_r + ((size_t)row * kH + h) * kDR + rank * kRopeHalf);
 #pragma unroll
-      for (int j = 0; j < kLat; ++j) v[j] = __ldg(lat + j);
-      if (wg == kSWG - 1) {
-        const uint4* rp = reinterpret_cast<const uint4*>(a.q_r + ((size_t)row * kH + h) * kDR + rank * kRopeHalf);
+      for (int half = 0; half < 2; ++half) {
+        uint4 v[20];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) v[kLat + j] = __ldg(rp + j);
-      }
+        for (int j = 0; j < 16; ++j) v[j] = __ldg(lat + half * 16 + j);
+        if (half == 0) {
 #pragma unroll
-      for (int ci = 0; ci < kQCols / 32; ++ci) {
-        uint32_t r[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          r[4 * j] = v[ci * 8 + j].x;
-          r[4 * j + 1] = v[ci * 8 + j].y;
-          r[4 * j + 2] = v[ci * 8 + j].z;
-          r[4 * j + 3] = v[ci * 8 + j].w;
+          for (int j = 0; j < 4; ++j) v[16 + j] = __ldg(rp + j);
         }
-        tmem_st32(tl + kColQ + wg * kQCols + ci * 32, r);
-      }
-      if (wg == kSWG - 1) {
-        uint32_t r[16];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          r[4 * j] = v[kLat + j].x;
-          r[4 * j + 1] = v[kLat + j].y;
-          r[4 * j + 2] = v[kLat + j].z;
-          r[4 * j + 3] = v[kLat + j].w;
+        for (int ci = 0; ci < 2; ++ci) {
+          uint32_t r[32];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            r[4 * j] = v[ci * 8 + j].x;
+            r[4 * j + 1] = v[ci * 8 + j].y;
+            r[4 * j + 2] = v[ci * 8 + j].z;
+            r[4 * j + 3] = v[ci * 8 + j].w;
+          }
+          tmem_st32(tl + kColQ + half * 64 + ci * 32, r);
         }
-        tmem_st16(tl + kColQ + 128, r);
+        if (half == 0) {
+          uint32_t r[16];
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            r[4 * j] = v[16 + j].x;
+            r[4 * j + 1] = v[16 + j].y;
+            r[4 * j + 2] = v[16 + j].z;
+            r[4 * j + 3] = v[16 + j].w;
+          }
+          tmem_st16(tl + kColQ + 128, r);
+        }
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(BAR(B_Q_READY));
     };
 
-    // Read this warpgroup's kCols columns of tile t's partial scores, free the S
-    // buffer, load the next segment's Q if tile t ends a segment, and push the
-    // fp16 log2-scaled partial to the peer.  `own` keeps the rounded values.
+    // Read this row's 64 partial scores of tile t, free S, push the fp16
+    // log2-scaled partial to the peer, and load the next segment's Q if tile
+    // t ends a segment (its QK^T was the segment's last).  `own` keeps the
+    // rounded values.
     auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[kWords]) -> bool {
-      bool w = wait_phase<false, true>(BAR(B_S_FULL), t & 1u, err, abort_flag);
+      bool w = wait_phase<false, true>(BAR(B_S_FULL0 + (t & 1u)), (t >> 1) & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
-      uint32_t r[kCols];
-      tmem_ld_cols(tl + kColS + wg * kCols, r);
-      tc_fence_before();
-      mbar_arrive(BAR(B_S_FREE));
-      if (c.last() && c.s + 1 < c.s_end) load_q(c.s + 1);  // every QK^T of this segment is done
+      {
+        uint32_t r[64];
+        tmem_ld64_sync(tl + kColS, r);
+        tc_fence_before();
+        mbar_arrive(BAR(B_S_FREE));
 #pragma unroll
-      for (int j = 0; j < kWords; ++j)
-        own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
+        for (int j = 0; j < kWords; ++j)
+          own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
+      }
       // Stage in own buffer (t + kXLead) mod kXBufs and push into the peer's
       // buffer t mod kXBufs.  Both need the peer's tile t - kXLead to have
-      // landed here; this thread already waited for exactly that (with
-      // cluster acquire) when it finished tile t - kXLead, which precedes this
-      // call (kXLead >= 2), so no wait is needed here.
-      static_assert(kXLead >= 2, "tile t - kXLead must be finished before tile t is pushed");
+      // landed here; this warpgroup already waited for exactly that (with
+      // cluster acquire) when it finished tile t - kXLead, its previous tile
+      // but one, so no wait is needed here.
+      static_assert(kXLead == 2, "tile t - kXLead must be this warpgroup's, already finished");
       const uint32_t stage = base + kOffX + ((t + kXLead) % kXBufs) * kXBytes;
 #pragma unroll
-      for (int k = 0; k < kRowChunks; ++k)
+      for (int k = 0; k < 8; ++k)
         st_shared_v4(stage + row_off + (((uint32_t)k ^ swz) << 4), own[4 * k], own[4 * k + 1], own[4 * k + 2],
                      own[4 * k + 3]);
       fence_proxy_async_smem();
@@ -464,6 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (lane == 0)
         bulk_copy_to_peer(mapa(base + kOffX + (t % kXBufs) * kXBytes + warp_off, peer), stage + warp_off,
                           (uint32_t)kXWarp, mapa(BAR(B_X_FULL0 + t % kXBufs), peer));
+      if (c.last() && c.s + 1 < c.s_end) load_q(c.s + 1);
       return true;
     };
 
@@ -471,88 +466,70 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     uint32_t G = 0;
     for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
 
-    mbar_arrive(BAR(B_O_FREE));  // O is free for the first segment
-    TileCursor cf;               // the tile being finished
-    cf.init(a.segs, s_begin, s_end);
-    uint32_t own_cur[kWords], own_nxt[kWords];
-    bool ok = true;
-    if (leader)  // arm the ring: the first kXBufs tiles each expect one peer push
+    if (wg == 0) mbar_arrive(BAR(B_O_FREE));  // O is free for the first segment
+    if (sw == 0 && lane == 0)                  // arm the ring: the first kXBufs tiles each expect one peer push
       for (uint32_t t = 0; t < G && t < (uint32_t)kXBufs; ++t)
         mbar_arrive_expect_tx(BAR(B_X_FULL0 + t), (uint32_t)kXBytes);
-    if (G > 0) {
-      load_q(s_begin);
-      ok = fetch_push(0, cf, own_cur);
-    }
-    float m = -INFINITY;
-    for (uint32_t g = 0; g < G && ok; ++g) {
-      // Iteration g finishes tile g and fetches/pushes tile g+1, ordered so
-      // that the latencies of one overlap work of the other: the barrier
-      // tests are issued up front and consumed later, and tile g+1's fetch
-      // and push run between publishing this thread's row max and reading
-      // the other warpgroup's.
-      TileCursor cn = cf;
-      cn.next();
-      const bool has_next = g + 1 < G;
-      const uint32_t xb = g % kXBufs, pb = g & 1u;
-      const bool xf_ready = mbar_test_wait_cluster(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u);
-      const int pg = cf.pg, vis = cf.vis;
-
-      // ---- tile g: add the peer's half (fp16, log2 units)
-      bool w = xf_ready || wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
+    TileCursor cf;  // this warpgroup's tile
+    cf.init(a.segs, s_begin, s_end);
+    if (wg == 1 && cf.valid()) cf.next();
+    if (wg == 0 && G > 0) load_q(s_begin);
+    uint32_t own[kWords];
+    bool ok = true;
+    for (uint32_t g = (uint32_t)wg; g < G && ok; g += 2) {
+      if (!fetch_push(g, cf, own)) {
+        ok = false;
+        break;
+      }
+      // ---- add the peer's half (fp16, log2 units)
+      const uint32_t xb = g % kXBufs;
+      bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
       }
-      // Re-arm this buffer's barrier for tile g + kXBufs.  That push cannot
-      // land before every warp here has pushed tile g + kXBufs - kXLead, which
-      // each does only after finishing tile g, so no waiter can miss a phase.
-      if (leader && g + kXBufs < G) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
+      // Re-arm this buffer's barrier for tile g + kXBufs (this warpgroup's
+      // again).  That push cannot land before this warpgroup has pushed tile
+      // g + kXBufs - kXLead, which it does only after finishing tile g.
+      if (wg_leader && g + kXBufs < G) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
       const uint32_t recv = base + kOffX + xb * kXBytes + row_off;
-      uint32_t sv[kWords];
 #pragma unroll
-      for (int k = 0; k < kRowChunks; ++k) {
+      for (int k = 0; k < 8; ++k) {
         const float4 v = ld_shared_v4(recv + (((uint32_t)k ^ swz) << 4));
-        sv[4 * k] = as_u32(__hadd2(as_h2(own_cur[4 * k]), as_h2(__float_as_uint(v.x))));
-        sv[4 * k + 1] = as_u32(__hadd2(as_h2(own_cur[4 * k + 1]), as_h2(__float_as_uint(v.y))));
-        sv[4 * k + 2] = as_u32(__hadd2(as_h2(own_cur[4 * k + 2]), as_h2(__float_as_uint(v.z))));
-        sv[4 * k + 3] = as_u32(__hadd2(as_h2(own_cur[4 * k + 3]), as_h2(__float_as_uint(v.w))));
+        own[4 * k] = as_u32(__hadd2(as_h2(own[4 * k]), as_h2(__float_as_uint(v.x))));
+        own[4 * k + 1] = as_u32(__hadd2(as_h2(own[4 * k + 1]), as_h2(__float_as_uint(v.y))));
+        own[4 * k + 2] = as_u32(__hadd2(as_h2(own[4 * k + 2]), as_h2(__float_as_uint(v.z))));
+        own[4 * k + 3] = as_u32(__hadd2(as_h2(own[4 * k + 3]), as_h2(__float_as_uint(v.w))));
       }
 
-      // ---- causal/length mask and this half's row max
-      const int valid = vis - pg * kPage - wg * kCols;
-      if (valid < kCols) {
+      // ---- causal/length mask and the row max of this tile
+      const int valid = cf.vis - cf.pg * kPage;
+      if (valid < kPage) {
 #pragma unroll
         for (int j = 0; j < kWords; ++j) {
-          if (2 * j >= valid) sv[j] = (sv[j] & 0xFFFF0000u) | 0xFC00u;          // low half -> -inf
-          if (2 * j + 1 >= valid) sv[j] = (sv[j] & 0x0000FFFFu) | 0xFC000000u;  // high half -> -inf
+          if (2 * j >= valid) own[j] = (own[j] & 0xFFFF0000u) | 0xFC00u;          // low half -> -inf
+          if (2 * j + 1 >= valid) own[j] = (own[j] & 0x0000FFFFu) | 0xFC000000u;  // high half -> -inf
         }
       }
-      __half2 mx[kWords / 4];
+      __half2 mx[8];
 #pragma unroll
-      for (int j = 0; j < kWords / 4; ++j)
-        mx[j] = __hmax2(__hmax2(as_h2(sv[4 * j]), as_h2(sv[4 * j + 1])), __hmax2(as_h2(sv[4 * j + 2]), as_h2(sv[4 * j + 3])));
-      const __half2 mh = hmax_tree(mx);
-      const float mloc = fmaxf(__low2float(mh), __high2float(mh));
-      // publish this slice's max for the other threads of the row (tagged slot)
-      st_shared_v2_volatile(pair + 8u * ((pb * kSWG + wg) * kH + h), __float_as_uint(mloc), g);
+      for (int j = 0; j < 8; ++j)
+        mx[j] = __hmax2(__hmax2(as_h2(own[4 * j]), as_h2(own[4 * j + 1])), __hmax2(as_h2(own[4 * j + 2]), as_h2(own[4 * j + 3])));
+      const __half2 mh = __hmax2(__hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3])),
+                                 __hmax2(__hmax2(mx[4], mx[5]), __hmax2(mx[6], mx[7])));
+      const float mt = fmaxf(__low2float(mh), __high2float(mh));
 
-      // ---- tile g+1: fetch this CTA's partial scores and push them to the peer
-      if (has_next && !fetch_push(g + 1, cn, own_nxt)) {
-        ok = false;
-        break;
-      }
-
-      // ---- tile g: the other warpgroups' maxima, then the reference max m
-      const bool od_ready = (g == 0) || mbar_test_wait(BAR(B_O_DONE), (g - 1) & 1u);
-      float mo = -INFINITY;
-      w = true;
-#pragma unroll
-      for (int o = 1; o < kSWG; ++o) {
-        const uint32_t slot = pair + 8u * ((pb * kSWG + ((wg + o) % kSWG)) * kH + h);
+      // ---- reference max: tile g-1's (the other warpgroup's) unless this tile starts a segment
+      const uint32_t gp = g - 1;  // the previous tile (the other warpgroup's)
+      const bool od_ready = (g == 0) || mbar_test_wait(BAR(B_O_DONE0 + (gp & 1u)), (gp >> 1) & 1u);
+      float m = mt, factor = 1.f;
+      bool resc = false;
+      if (!cf.first()) {
+        const uint32_t slot = pair + 8u * (((g - 1) & 3u) * kH + h);
         uint2 v = ld_shared_v2_volatile(slot);
-        if (v.y != g) {
+        if (v.y != g - 1) {
           const uint64_t t0 = cycles();
-          for (uint32_t it = 1; (v = ld_shared_v2_volatile(slot)).y != g; ++it) {
+          for (uint32_t it = 1; (v = ld_shared_v2_volatile(slot)).y != g - 1; ++it) {
             if ((it & 255u) == 0u && (*abort_flag || cycles() - t0 > kWaitLimitCycles)) {
               if (!*abort_flag) atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
               *abort_flag = 1;
@@ -560,35 +537,35 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             }
           }
         }
-        mo = fmaxf(mo, __uint_as_float(v.x));
-        w = w && (v.y == g);
+        if (!__all_sync(0xffffffffu, v.y == g - 1)) {
+          ok = false;
+          break;
+        }
+        const float mp = __uint_as_float(v.x);
+        if (mt > mp + 8.f) {  // lazy rescale: move the reference only on a large jump
+          factor = exp2f(mp - mt);
+          resc = true;
+        } else {
+          m = mp;
+        }
       }
-      if (!__all_sync(0xffffffffu, w)) {
-        ok = false;
-        break;
-      }
-      const float mt = fmaxf(mloc, mo);
+      // Hand m to tile g+1.  Four slots: the next writer of this one is tile
+      // g+4, and the next writer of tile g-1's is tile g+3, which needs S
+      // freed by tile g+2, fetched by this warpgroup only after this read;
+      // two slots would not do, since a tile that starts a segment reads none
+      // and may run ahead.
+      st_shared_v2_volatile(pair + 8u * ((g & 3u) * kH + h), __float_as_uint(m), g);
 
-      float factor = 1.f;
-      bool resc = false;
-      if (cf.first()) {
-        m = mt;
-      } else if (mt > m + 8.f) {
-        factor = exp2f(m - mt);
-        m = mt;
-        resc = true;
-      }
-      // P = 2^(s - m) in fp16 pairs, stored as bf16 for the tensor core.
+      // ---- P = 2^(s - m) in fp16 pairs, stored as bf16 for the tensor core
       const __half2 m2 = __float2half2_rn(m);  // m is a max of fp16 values: exact
-      uint32_t pk[kWords];
 #pragma unroll
       for (int j = 0; j < kWords; ++j) {
-        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hsub2(as_h2(sv[j]), m2)))));
-        pk[j] = pack_bf16x2(p.x, p.y);
+        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hsub2(as_h2(own[j]), m2)))));
+        own[j] = pack_bf16x2(p.x, p.y);
       }
       // Writing P (single TMEM buffer) and a rescale both need P·V of tile g-1 done.
       if (g > 0) {
-        w = od_ready || wait_phase<false, true>(BAR(B_O_DONE), (g - 1) & 1u, err, abort_flag);
+        w = od_ready || wait_phase<false, true>(BAR(B_O_DONE0 + (gp & 1u)), (gp >> 1) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
@@ -597,16 +574,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       }
       if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
-        for (int c = 0; c < kOCols; c += 32) {
+        for (int c = 0; c < 256; c += 32) {
           uint32_t o[32];
-          tmem_ld32_sync(tl + kColO + wg * kOCols + c, o);
+          tmem_ld32_sync(tl + kColO + c, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
-          tmem_st32(tl + kColO + wg * kOCols + c, o);
+          tmem_st32(tl + kColO + c, o);
         }
-        if (wg == 0) tmem_st1(tl + kColSum, __float_as_uint(__uint_as_float(tmem_ld1_sync(tl + kColSum)) * factor));
+        tmem_st1(tl + kColSum, __float_as_uint(__uint_as_float(tmem_ld1_sync(tl + kColSum)) * factor));
       }
-      tmem_st_cols(tl + kColP + wg * kWords, pk);
+      tmem_st32(tl + kColP, own);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(BAR(B_P_FULL));
@@ -614,7 +591,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       if (cf.last()) {
         // ---- epilogue of this segment: wait for its last P·V, normalise, store
         const int row = cf.row, slot = cf.slot;
-        w = wait_phase(BAR(B_O_DONE), g & 1u, err, abort_flag);
+        w = wait_phase(BAR(B_O_DONE0 + (g & 1u)), (g >> 1) & 1u, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
@@ -623,11 +600,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         const float lt = __uint_as_float(tmem_ld1_sync(tl + kColSum));
         const float inv = 1.f / lt;
         if (slot < 0) {
-          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256 + wg * kOCols);
+          uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256);
 #pragma unroll 1
-          for (int c = 0; c < kOCols; c += 32) {
+          for (int c = 0; c < 256; c += 32) {
             uint32_t o[32];
-            tmem_ld32_sync(tl + kColO + wg * kOCols + c, o);
+            tmem_ld32_sync(tl + kColO + c, o);
 #pragma unroll
             for (int v = 0; v < 4; ++v)
               dst[c / 8 + v] = make_uint4(
@@ -637,11 +614,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                   pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
           }
         } else {
-          float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * kH + h) * kDC + rank * 256 + wg * kOCols);
+          float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * kH + h) * kDC + rank * 256);
 #pragma unroll 1
-          for (int c = 0; c < kOCols; c += 32) {
+          for (int c = 0; c < 256; c += 32) {
             uint32_t o[32];
-            tmem_ld32_sync(tl + kColO + wg * kOCols + c, o);
+            tmem_ld32_sync(tl + kColO + c, o);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[c / 4 + v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
@@ -650,7 +627,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(BAR(B_O_FREE));
-        if (rank == 0 && wg == 0) {
+        if (rank == 0) {
           const float lse2 = m + log2f(lt);
           if (slot < 0) {
             if (a.lse) a.lse[(size_t)row * kH + h] = lse2 * 0.6931471805599453f;
@@ -659,9 +636,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
         }
       }
-#pragma unroll
-      for (int j = 0; j < kWords; ++j) own_cur[j] = own_nxt[j];
-      cf = cn;
+      cf.next();
+      cf.next();
     }
   }
 

@@ -367,6 +367,20 @@ __device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]
       : "r"(taddr));
   asm volatile("tcgen05.wait::ld.sync.aligned;" : MLA_RW8(r, 0), MLA_RW8(r, 8) : : "memory");
 }
+// Load 64 columns (one row's whole tile slice) and wait; registers tied to the wait.
+__device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x64.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32, %33, %34, %35, %36, %37, %38, %39, %40, %41, %42, %43, %44, %45, %46, %47, %48, %49, %50, %51, %52, %53, %54, %55, %56, %57, %58, %59, %60, %61, %62, %63}, [%64];"
+      : MLA_R8(r, 0), MLA_R8(r, 8), MLA_R8(r, 16), MLA_R8(r, 24), MLA_R8(r, 32), MLA_R8(r, 40), MLA_R8(r, 48),
+        MLA_R8(r, 56)
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : MLA_RW8(r, 0), MLA_RW8(r, 8), MLA_RW8(r, 16), MLA_RW8(r, 24), MLA_RW8(r, 32), MLA_RW8(r, 40),
+                 MLA_RW8(r, 48), MLA_RW8(r, 56)
+               :
+               : "memory");
+}
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // fp16x2 of two values, saturating to the finite fp16 range (no infinities).
