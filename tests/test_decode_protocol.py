@@ -1,0 +1,262 @@
+"""Model check of the decode kernel's synchronisation protocol (CPU only).
+
+The decode kernel (csrc/decode_paged.cu) coordinates seven roles per CTA and
+two CTAs per cluster through mbarriers, a score-exchange ring in distributed
+shared memory and tagged shared-memory slots.  Hardware mbarrier waits test
+a phase *parity*, so a waiter that runs two phases ahead of the barrier
+passes early; a buffer reused too soon is overwritten before it is read.
+Neither shows up as a fault on the GPU: the first reads stale data, the
+second corrupts it, and a wrong ordering hangs until the kernel's bounded
+waits expire.
+
+This file restates the protocol as a small Python model and runs it under
+random interleavings of every role and every asynchronous completion (TMA
+loads, MMA completions, copies landing in the peer CTA), over random segment
+layouts.  It checks:
+  * no deadlock (some role or completion can always make progress);
+  * every parity wait passes only when its own phase has completed;
+  * no exchange buffer region is overwritten while it holds unconsumed
+    scores or while a copy out of it is still reading it;
+  * no reference-max slot is overwritten before its reader has read it.
+Negative controls re-introduce, one at a time, a single shared score barrier,
+two hand-off slots instead of four, and a staging offset of one or three
+buffers; each must be caught.  The model is test infrastructure for the
+kernel's control flow only: it computes none of the attention arithmetic.
+"""
+import random
+
+import pytest
+
+STAGES = 4      # page ring
+XBUFS = 4       # exchange ring depth
+WARPS = 2       # row blocks per warpgroup modelled (the kernel has 4)
+
+
+class ProtocolError(RuntimeError):
+    pass
+
+
+class Barrier:
+    """mbarrier with an arrival count and a transaction count; waits test parity."""
+
+    def __init__(self, count):
+        self.count, self.pending, self.phase, self.tx = count, count, 0, 0
+
+    def arrive(self, n=1, expect_tx=0):
+        self.tx += expect_tx
+        self.pending -= n
+        if self.pending < 0:
+            raise ProtocolError("more arrivals than the barrier's count")
+        self._complete()
+
+    def complete_tx(self, n):
+        self.tx -= n
+        self._complete()
+
+    def _complete(self):
+        if self.pending == 0 and self.tx == 0:
+            self.phase += 1
+            self.pending = self.count
+
+    def test(self, k):
+        """Hardware semantics: true iff the last completed phase has k's parity."""
+        passed = self.phase >= 1 and ((self.phase - 1) & 1) == (k & 1)
+        if passed and self.phase != k + 1:
+            raise ProtocolError(f"parity wait for phase {k} passed at phase {self.phase}")
+        return passed
+
+
+def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2):
+    rnd = random.Random(seed)
+    tiles = []
+    for si, n in enumerate(segs):
+        for i in range(n):
+            tiles.append((si, i == 0, i == n - 1))
+    G = len(tiles)
+    WG_THREADS = 128
+    per_warp = WG_THREADS // WARPS
+    ctas = []
+    for _ in range(2):
+        ctas.append(dict(
+            kv_full=[Barrier(1) for _ in range(STAGES)], kv_empty=[Barrier(1) for _ in range(STAGES)],
+            s_full=[Barrier(1), Barrier(1)], s_free=Barrier(WG_THREADS), p_full=Barrier(WG_THREADS),
+            o_done=[Barrier(1), Barrier(1)], q_ready=Barrier(WG_THREADS), o_free=Barrier(WG_THREADS),
+            x_full=[Barrier(1) for _ in range(XBUFS)],
+            xbuf=[[None] * WARPS for _ in range(XBUFS)],   # region state per (buffer, row block)
+            reading=[[False] * WARPS for _ in range(XBUFS)],  # a copy out of this region is in flight
+            slot=[[None] * WARPS for _ in range(slots)], slot_unread=[[False] * WARPS for _ in range(slots)],
+        ))
+    events = []
+
+    def s_full_bar(c, t):
+        return (c["s_full"][0], t) if shared_s_full else (c["s_full"][t & 1], t >> 1)
+
+    def o_done_bar(c, t):
+        return (c["o_done"][0], t) if shared_s_full else (c["o_done"][t & 1], t >> 1)
+
+    def producer(ci):
+        c = ctas[ci]
+        for t in range(G):
+            if t >= STAGES:
+                while not c["kv_empty"][t % STAGES].test(t // STAGES - 1):
+                    yield
+            events.append(("kv", ci, t))
+
+    def qk(ci):
+        c = ctas[ci]
+        for t in range(G):
+            while not c["kv_full"][t % STAGES].test(t // STAGES):
+                yield
+            if t > 0:
+                while not c["s_free"].test(t - 1):
+                    yield
+            seg, first, _ = tiles[t]
+            if first:
+                while not c["q_ready"].test(seg):
+                    yield
+            events.append(("s", ci, t))
+
+    def pv(ci):
+        c = ctas[ci]
+        for t in range(G):
+            while not c["p_full"].test(t):
+                yield
+            seg, first, _ = tiles[t]
+            if first:
+                while not c["o_free"].test(seg):
+                    yield
+            events.append(("o", ci, t))
+
+    def softmax_warp(ci, wg, w):
+        c = ctas[ci]
+        if wg == 0:
+            c["o_free"].arrive(per_warp)
+            c["q_ready"].arrive(per_warp)
+            if w == 0:
+                for t in range(min(G, XBUFS)):
+                    c["x_full"][t].arrive(1, expect_tx=WARPS)
+        for t in range(wg, G, 2):
+            seg, first, last = tiles[t]
+            bar, k = s_full_bar(c, t)
+            while not bar.test(k):
+                yield
+            c["s_free"].arrive(per_warp)
+            # stage this row block's scores and push them to the peer
+            sb = (t + xlead) % XBUFS
+            state = c["xbuf"][sb][w]
+            if state is not None and state[0] == "data":
+                raise ProtocolError(f"staging tile {t} over unconsumed scores of tile {state[1]}")
+            if c["reading"][sb][w]:
+                raise ProtocolError(f"staging tile {t} over a copy still in flight")
+            c["xbuf"][sb][w] = ("stage", t)
+            c["reading"][sb][w] = True
+            events.append(("x", ci, (t, w, sb)))
+            if last and seg + 1 < len(segs):
+                c["q_ready"].arrive(per_warp)
+            yield
+            # the peer's half of tile t
+            b = t % XBUFS
+            while not c["x_full"][b].test(t // XBUFS):
+                yield
+            if c["xbuf"][b][w] != ("data", t):
+                raise ProtocolError(f"tile {t} reads {c['xbuf'][b][w]}")
+            c["xbuf"][b][w] = None
+            if w == 0 and t + XBUFS < G:
+                c["x_full"][b].arrive(1, expect_tx=WARPS)
+            # reference max from tile t-1
+            if not first:
+                sl = (t - 1) % slots
+                while c["slot"][sl][w] != t - 1:
+                    yield
+                c["slot_unread"][sl][w] = False
+            sl = t % slots
+            if c["slot_unread"][sl][w]:
+                raise ProtocolError(f"tile {t} overwrites tile {c['slot'][sl][w]}'s max before it was read")
+            c["slot"][sl][w] = t
+            c["slot_unread"][sl][w] = t + 1 < G and not tiles[t + 1][1]
+            yield
+            if t > 0:
+                bar, k = o_done_bar(c, t - 1)
+                while not bar.test(k):
+                    yield
+            c["p_full"].arrive(per_warp)
+            if last:
+                bar, k = o_done_bar(c, t)
+                while not bar.test(k):
+                    yield
+                c["o_free"].arrive(per_warp)
+
+    roles = {}
+    for ci in range(2):
+        roles[("prod", ci)] = producer(ci)
+        roles[("qk", ci)] = qk(ci)
+        roles[("pv", ci)] = pv(ci)
+        for wg in range(2):
+            for w in range(WARPS):
+                roles[("sm", ci, wg, w)] = softmax_warp(ci, wg, w)
+    idle = 0
+    while roles or events:
+        pick = rnd.randrange(len(roles) + len(events))
+        if pick >= len(roles):
+            kind, ci, t = events.pop(pick - len(roles))
+            c = ctas[ci]
+            if kind == "kv":
+                c["kv_full"][t % STAGES].arrive()
+            elif kind == "s":
+                bar, _ = s_full_bar(c, t)
+                bar.arrive()
+            elif kind == "o":
+                c["kv_empty"][t % STAGES].arrive()
+                bar, _ = o_done_bar(c, t)
+                bar.arrive()
+            else:  # a row block's copy lands in the peer's buffer t mod XBUFS
+                tile, w, sb = t
+                p = ctas[1 - ci]
+                b = tile % XBUFS
+                state = p["xbuf"][b][w]
+                if state is not None and state[0] == "data":
+                    raise ProtocolError(f"tile {tile} lands over unconsumed tile {state[1]}")
+                if p["reading"][b][w]:
+                    raise ProtocolError(f"tile {tile} lands over staging still being copied")
+                p["xbuf"][b][w] = ("data", tile)
+                c["reading"][sb][w] = False
+                p["x_full"][b].complete_tx(1)
+            idle = 0
+            continue
+        key = list(roles)[pick]
+        try:
+            next(roles[key])
+            idle += 1
+        except StopIteration:
+            del roles[key]
+            idle = 0
+        if idle > 50000:
+            raise ProtocolError(f"deadlock; roles still running: {sorted(map(str, roles))}")
+
+
+def _layouts(n, seed):
+    rng = random.Random(seed)
+    for _ in range(n):
+        yield [rng.choice([1, 1, 2, 3, 5, 9]) for _ in range(rng.randint(1, 7))]
+
+
+def test_protocol_holds_on_random_interleavings():
+    for i, segs in enumerate(_layouts(150, 11)):
+        run_model(segs, seed=i)
+
+
+def test_protocol_holds_on_single_tile_segments():
+    # the layout whose hazards were found on the GPU: many one-tile segments
+    for seed in range(100):
+        run_model([1, 1, 1, 1, 2, 2, 3, 3, 11], seed)
+
+
+@pytest.mark.parametrize("mistake", [dict(shared_s_full=True), dict(slots=2), dict(xlead=1), dict(xlead=3)])
+def test_planted_protocol_mistakes_are_caught(mistake):
+    caught = 0
+    for i, segs in enumerate(_layouts(60, 12)):
+        try:
+            run_model(segs + [1, 1, 3], seed=i, **mistake)
+        except ProtocolError:
+            caught += 1
+    assert caught > 0, f"the model did not catch {mistake}"
