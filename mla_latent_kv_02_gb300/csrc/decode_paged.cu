@@ -94,8 +94,9 @@ static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 480, kTmemCols = 512;
 constexpr int kPvWarp = 2 + kSWarps;                      // warps: producer, QK^T, softmax..., P·V
 constexpr int kThreads = 32 * (kPvWarp + 1);
-// The two MMA-issuing threads sleep in mbarrier.try_wait rather than poll.
-constexpr bool kIssueSuspend = true;
+// The producer and the two MMA-issuing threads poll (mbarrier.test_wait)
+// rather than sleep: their wake-up sits on the score chain.
+constexpr bool kIssueSuspend = false;
 constexpr uint32_t kTileThreads = 128;                    // the warpgroup that handles one tile
 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
@@ -264,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             prefetch_l2_bulk(qa + rank * (kH * kDC), kH * kDC);
             if (rank == 0) prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.q_r) + qrow * (kH * kDR * 2), kH * kDR * 2);
           }
-          if (use > 0 && !wait_phase<false, true>(BAR(B_KV_EMPTY + st), (use - 1) & 1u, err, abort_flag)) {
+          if (use > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_KV_EMPTY + st), (use - 1) & 1u, err, abort_flag)) {
             ok = false;
             break;
           }
