@@ -118,35 +118,63 @@ mla_status build_plan(const int32_t* seq_lens, const int32_t* q_lens, int32_t B,
       return fail(MLA_ERR_INVALID_ARG, "too many query rows");
   }
   const int64_t T = (int64_t)rows.size();
-  int64_t used = 0, tiles_per = 0;
-  if (total > 0) {
-    tiles_per = std::max<int64_t>((total + num_clusters - 1) / num_clusters, kMinTilesPerCluster);
-    used = (total + tiles_per - 1) / tiles_per;
+  // Lanes: when every sequence has the same number Q >= 2 of query rows
+  // (multi-token decode), the clusters are split into Q lanes and lane j takes
+  // row j of every sequence, cut into equal contiguous tile ranges the same
+  // way in every lane.  Cluster c of each lane then reads the same pages at
+  // nearly the same time, so the rows of a sequence share one DRAM read of
+  // each page through L2.  Otherwise there is one lane over all rows.
+  int32_t lanes = 1;
+  {
+    int32_t q0 = -1;
+    bool uniform = true;
+    for (int32_t b = 0; b < B; ++b) {
+      if (q_lens[b] == 0) continue;
+      if (q0 < 0) q0 = q_lens[b];
+      uniform = uniform && q_lens[b] == q0;
+    }
+    if (uniform && q0 >= 2 && num_clusters / q0 >= 1) lanes = q0;
   }
+  std::vector<std::vector<int32_t>> lane_rows(lanes);
+  {
+    int32_t r = 0;
+    for (int32_t b = 0; b < B; ++b)
+      for (int32_t i = 0; i < q_lens[b]; ++i, ++r) lane_rows[lanes == 1 ? 0 : i].push_back(r);
+  }
+  const int32_t clusters_per_lane = num_clusters / lanes;
   // segments
-  std::vector<int32_t> seg_off(used + 1, 0);
   struct Seg {
     int32_t row, b, pb, pe, vis, slot;
   };
   std::vector<Seg> segs;
+  std::vector<int32_t> seg_off;
   std::vector<int32_t> row_pieces(T, 0);
-  {
+  for (int32_t lane = 0; lane < lanes; ++lane) {
+    const std::vector<int32_t>& lr = lane_rows[lane];
+    int64_t lane_total = 0;
+    for (int32_t r : lr) lane_total += rows[r].npages;
+    if (lane_total == 0) continue;
+    const int64_t tiles_per =
+        std::max<int64_t>((lane_total + clusters_per_lane - 1) / clusters_per_lane, kMinTilesPerCluster);
+    const int64_t used = (lane_total + tiles_per - 1) / tiles_per;
     int64_t row_start = 0;
-    size_t r = 0;
+    size_t k = 0;  // index into lr
     for (int64_t c = 0; c < used; ++c) {
-      const int64_t lo = c * tiles_per, hi = std::min(total, lo + tiles_per);
-      seg_off[c] = (int32_t)segs.size();
-      while (r < rows.size() && row_start + rows[r].npages <= lo) row_start += rows[r++].npages;
+      const int64_t lo = c * tiles_per, hi = std::min(lane_total, lo + tiles_per);
+      seg_off.push_back((int32_t)segs.size());
+      while (k < lr.size() && row_start + rows[lr[k]].npages <= lo) row_start += rows[lr[k++]].npages;
       int64_t rs = row_start;
-      for (size_t rr = r; rr < rows.size() && rs < hi; rs += rows[rr++].npages) {
+      for (size_t kk = k; kk < lr.size() && rs < hi; rs += rows[lr[kk++]].npages) {
+        const int32_t rr = lr[kk];
         const int64_t pb = std::max<int64_t>(lo - rs, 0), pe = std::min<int64_t>(hi - rs, rows[rr].npages);
         if (pe <= pb) continue;
-        segs.push_back({(int32_t)rr, rows[rr].b, (int32_t)pb, (int32_t)pe, rows[rr].visible, -1});
+        segs.push_back({rr, rows[rr].b, (int32_t)pb, (int32_t)pe, rows[rr].visible, -1});
         ++row_pieces[rr];
       }
     }
-    seg_off[used] = (int32_t)segs.size();
   }
+  const int64_t used = (int64_t)seg_off.size();
+  seg_off.push_back((int32_t)segs.size());
   // partial slots for rows cut into several pieces, contiguous per row
   std::vector<int32_t> split;  // {row, slot_begin, n, 0}
   int32_t nslots = 0;

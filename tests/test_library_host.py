@@ -128,7 +128,21 @@ def test_planner_covers_every_tile_once(api, seq_lens, q_lens, nc):
     # contiguous, balanced ranges
     assert seg_off[0] == 0 and seg_off[-1] == info.num_segments and np.all(np.diff(seg_off) >= 1)
     per = [sum(int(s[3] - s[2]) for s in segs[seg_off[c]:seg_off[c + 1]]) for c in range(info.num_clusters)]
-    assert max(per) - min(per[:-1] or per) <= 0 and info.num_clusters <= nc
+    assert info.num_clusters <= nc
+    # Lanes (uniform multi-token decode): each cluster serves one in-sequence
+    # row index; within a lane every cluster but the last holds the same count.
+    lane_of = [{rows[int(s[0])][2] for s in segs[seg_off[c]:seg_off[c + 1]]} for c in range(info.num_clusters)]
+    q = set(x for x in q_lens if x > 0)
+    laned = len(q) == 1 and min(q) >= 2 and nc // min(q) >= 1
+    if laned:
+        assert all(len(l) == 1 for l in lane_of)
+        lanes = [next(iter(l)) for l in lane_of]
+        assert lanes == sorted(lanes)
+        groups = [[per[c] for c in range(len(per)) if lanes[c] == j] for j in sorted(set(lanes))]
+    else:
+        groups = [per]
+    for g in groups:
+        assert max(g) - min(g[:-1] or g) <= 0
     # split rows: exactly the rows with several pieces, slots contiguous
     pieces = {}
     for s in segs:
@@ -139,6 +153,24 @@ def test_planner_covers_every_tile_once(api, seq_lens, q_lens, nc):
         assert multi[row] == list(range(s0, s0 + n))
     assert all(p == [-1] for r, p in pieces.items() if r not in multi)
     assert info.num_partials == sum(len(p) for p in multi.values())
+
+
+def test_planner_lanes_align_the_rows_of_a_sequence(api):
+    # Multi-token decode: cluster c of lane j reads the same pages of the same
+    # sequences as cluster c of lane 0 (up to the one-tile difference between
+    # the rows' visible lengths), so the rows of a sequence share page reads.
+    seq_lens, q_lens, nc = [8194] * 64, [2] * 64, 76
+    buf, info = api.mla_decode_plan_host(seq_lens, q_lens, nc)
+    seg_off, segs, _ = _plan_segments(buf, info)
+    rows = oracle.row_index(seq_lens, q_lens)
+    lanes = {}
+    for c in range(info.num_clusters):
+        work = [(int(s[1]), p) for s in segs[seg_off[c]:seg_off[c + 1]] for p in range(int(s[2]), int(s[3]))]
+        lane = rows[int(segs[seg_off[c]][0])][2]
+        lanes.setdefault(lane, []).append(work)
+    assert sorted(lanes) == [0, 1] and len(lanes[0]) == len(lanes[1]) == nc // 2
+    for w0, w1 in zip(lanes[0], lanes[1]):
+        assert w0 == w1
 
 
 def test_planner_rejects_bad_lengths(api):
