@@ -275,9 +275,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           const uint32_t dst = base + kOffKV + st * kStageBytes;
           mbar_arrive_expect_tx(BAR(B_KV_FULL + st), (uint32_t)kStageBytes);
-          for (int i = 0; i < 4; ++i)
-            tma_load_2d(dst + i * kChunkBytes, &kv_map, (int)(4 * rank + i) * kChunk, pid * kPage,
-                        BAR(B_KV_FULL + st));
+          // latent chunks 4r..4r+3 in one 3D box, then the RoPE half
+          tma_load_3d(dst, &kv_map, 0, pid * kPage, (int)(4 * rank), BAR(B_KV_FULL + st));
           tma_load_2d(dst + 4 * kChunkBytes, &rope_map, kDC + (int)rank * kRopeHalf, pid * kPage, BAR(B_KV_FULL + st));
           ++g;
         }

@@ -562,12 +562,17 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
   }
 
   CUtensorMap kv_map, rope_map;
+  // Latent part as a 3D view {64 elements, token, 64-element chunk}: one box
+  // of 4 chunks x 64 tokens lands as 4 consecutive 128-byte-swizzled 8 KB
+  // tiles, one TMA instruction per page for a CTA's latent half.
+  const uint64_t ldims[3] = {64, (uint64_t)num_pages * MLA_PAGE_SIZE, MLA_LATENT_DIM / 64};
+  const uint64_t lstr[2] = {(uint64_t)kRowBytes, 128};
+  const uint32_t lbox[3] = {64, 64, 4};
+  mla_status s = make_map(&kv_map, kv_cache, 3, ldims, lstr, lbox, "kv_cache latent chunks");
+  if (s != MLA_OK) return s;
   const uint64_t dims[2] = {MLA_TOKEN_ELEMS, (uint64_t)num_pages * MLA_PAGE_SIZE};
   const uint64_t str[1] = {(uint64_t)kRowBytes};
-  const uint32_t box[2] = {64, 64};
   const uint32_t rope_box[2] = {32, 64};
-  mla_status s = make_map(&kv_map, kv_cache, 2, dims, str, box, "kv_cache");
-  if (s != MLA_OK) return s;
   s = make_map(&rope_map, kv_cache, 2, dims, str, rope_box, "kv_cache RoPE halves", CU_TENSOR_MAP_SWIZZLE_64B);
   if (s != MLA_OK) return s;
 
