@@ -188,8 +188,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     }
     mbar_init(BAR(B_S_FULL0), 1);
     mbar_init(BAR(B_S_FULL1), 1);
-    mbar_init(BAR(B_S_FREE), kTileThreads);
-    mbar_init(BAR(B_P_FULL), kTileThreads);
+    mbar_init(BAR(B_S_FREE), kTileThreads / 32);  // one arrival per warp
+    mbar_init(BAR(B_P_FULL), kTileThreads / 32);
     mbar_init(BAR(B_O_DONE0), 1);
     mbar_init(BAR(B_O_DONE1), 1);
     mbar_init(BAR(B_Q_READY), kTileThreads);
@@ -437,7 +437,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t r[64];
         tmem_ld64_sync(tl + kColS, r);
         tc_fence_before();
-        mbar_arrive(BAR(B_S_FREE));
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_S_FREE));
 #pragma unroll
         for (int j = 0; j < kWords; ++j)
           own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
@@ -586,7 +587,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tmem_st32(tl + kColP, own);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(BAR(B_P_FULL));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_P_FULL));
 
       if (cf.last()) {
         // ---- epilogue of this segment: wait for its last P·V, normalise, store
