@@ -14,7 +14,8 @@
 //    4r..4r+3 (64 columns each, 128-byte swizzle) and RoPE dims [32r, 32r+32)
 //    (64-byte swizzle).  Each CTA computes a partial S = Q_r·K_r^T (tcgen05,
 //    M = 128 heads, N = 64 tokens, A = Q from TMEM, B = the page tile in shared
-//    memory).  The partials, scaled to log2 units, are exchanged as fp16: each
+//    memory).  The partials are exchanged unscaled as fp16 (the scale times
+//    log2 e enters once, in the exponent of P): each
 //    warp stages its rows and one bulk copy per warp pushes them into the peer
 //    CTA, completing on the peer's mbarrier.  Both CTAs add the same two
 //    rounded halves, so they hold bit-identical S and take identical softmax
@@ -378,7 +379,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t row_off = (uint32_t)(h * kXRow);
     const uint32_t warp_off = (uint32_t)(q4 * kXWarp);
     const bool wg_leader = ((sw & 3) == 0 && lane == 0);
+    // Scores cross the pair and are compared unscaled; the scale (times
+    // log2 e) enters once, in the exponent.
     const float c2 = a.scale_log2;
+    const float rescale_thr = 8.f / c2;  // lazy-rescale threshold: 8 in log2 units
+    const __half2 c2h = __float2half2_rn(c2);
     __syncwarp();
 
     // Q_r of a segment's row into TMEM, this thread's row (144 columns), in
@@ -426,7 +431,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     };
 
     // Read this row's 64 partial scores of tile t, free S, push the fp16
-    // log2-scaled partial to the peer, and load the next segment's Q if tile
+    // partial to the peer, and load the next segment's Q if tile
     // t ends a segment (its QK^T was the segment's last).  `own` keeps the
     // rounded values.
     auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[kWords]) -> bool {
@@ -441,7 +446,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (lane == 0) mbar_arrive(BAR(B_S_FREE));
 #pragma unroll
         for (int j = 0; j < kWords; ++j)
-          own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]) * c2, __uint_as_float(r[2 * j + 1]) * c2);
+          own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
       }
       // Stage in own buffer (t + kXLead) mod kXBufs and push into the peer's
       // buffer t mod kXBufs.  Both need the peer's tile t - kXLead to have
@@ -482,7 +487,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         ok = false;
         break;
       }
-      // ---- add the peer's half (fp16, log2 units)
+      // ---- add the peer's half (fp16, unscaled)
       const uint32_t xb = g % kXBufs;
       bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) {
@@ -543,8 +548,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           break;
         }
         const float mp = __uint_as_float(v.x);
-        if (mt > mp + 8.f) {  // lazy rescale: move the reference only on a large jump
-          factor = exp2f(mp - mt);
+        if (mt > mp + rescale_thr) {  // lazy rescale: move the reference only on a large jump
+          factor = exp2f((mp - mt) * c2);
           resc = true;
         } else {
           m = mp;
@@ -557,11 +562,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       // and may run ahead.
       st_shared_v2_volatile(pair + 8u * ((g & 3u) * kH + h), __float_as_uint(m), g);
 
-      // ---- P = 2^(s - m) in fp16 pairs, stored as bf16 for the tensor core
-      const __half2 m2 = __float2half2_rn(m);  // m is a max of fp16 values: exact
+      // ---- P = 2^(c2 (s - m)) in fp16 pairs (one fused multiply-add for the
+      //      exponent), stored as bf16 for the tensor core
+      const __half2 mc2 = __float2half2_rn(-m * c2);
 #pragma unroll
       for (int j = 0; j < kWords; ++j) {
-        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hsub2(as_h2(own[j]), m2)))));
+        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hfma2(as_h2(own[j]), c2h, mc2)))));
         own[j] = pack_bf16x2(p.x, p.y);
       }
       // Writing P (single TMEM buffer) and a rescale both need P·V of tile g-1 done.
@@ -630,7 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(BAR(B_O_FREE));
         if (rank == 0) {
-          const float lse2 = m + log2f(lt);
+          const float lse2 = m * c2 + log2f(lt);
           if (slot < 0) {
             if (a.lse) a.lse[(size_t)row * kH + h] = lse2 * 0.6931471805599453f;
           } else {
