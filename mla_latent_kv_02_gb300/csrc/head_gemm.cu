@@ -5,11 +5,13 @@
 //   A5  out[t, h, :]   = o_lat[t, h, :] · W_UV[h]   (K = 512 -> N = 128)
 //       ([P2] "DeepSeek的推理为什么比别人便宜一个数量级？…", MLA section: V = c·W_UV)
 //
-// One CTA computes a 128-row tile of tokens for one head: D[128 x N] fp32 in
-// TMEM, A (activation rows, K-major) and W (row-major [K x N], read as an
-// MN-major operand) staged by TMA with 128-byte swizzle through a K-chunk
-// ring.  Rows past T are zero-filled by TMA and never stored.  For small T
-// the kernel streams the 16 MiB of weights once (HBM bound).
+// One CTA computes a 128-row tile of tokens for one head and one of NSPLIT
+// column blocks: D[128 x N/NSPLIT] fp32 in TMEM, A (activation rows,
+// K-major) and W (row-major [K x N], read as an MN-major operand) staged by
+// TMA with 128-byte swizzle through a K-chunk ring.  When split, two CTAs
+// fit on an SM, so one CTA's stores overlap another's loads.  Rows past T are zero-filled
+// by TMA and never stored.  For small T the kernel streams the 16 MiB of
+// weights once (HBM bound).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -23,25 +25,27 @@ namespace gemm {
 
 using namespace mla::dev;
 
-template <int N, int K, int STAGES>
+template <int N, int K, int STAGES, int NSPLIT>
 struct Cfg {
+  static constexpr int kNC = N / NSPLIT;  // columns of this CTA
   static constexpr int kKCh = K / 64;
   static constexpr int kABytes = 128 * 64 * 2;
-  static constexpr int kBBytes = 64 * N * 2;
+  static constexpr int kBBytes = 64 * kNC * 2;
   static constexpr int kStage = kABytes + kBBytes;
   static constexpr int kOffBar = STAGES * kStage;
   static constexpr int kOffMisc = kOffBar + 8 * (2 * STAGES + 1);
   static constexpr int kSmem = kOffMisc + 16 + 1024;
-  static constexpr int kMmaN = N < 256 ? N : 256;
+  static constexpr int kMmaN = kNC < 256 ? kNC : 256;
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN, false, true);
-  static_assert(kSmem <= 232448, "head GEMM exceeds shared memory");
+  static_assert((NSPLIT == 1 ? 1 : 2) * kSmem <= 232448, "a split head GEMM needs two CTAs per SM");
+  static_assert(kNC % 64 == 0 && kNC >= 64, "column block is a multiple of 64");
 };
 
-template <int N, int K, int STAGES>
-__global__ void __launch_bounds__(128, 1)
+template <int N, int K, int STAGES, int NSPLIT>
+__global__ void __launch_bounds__(128, 2)
     head_gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
                      uint16_t* __restrict__ c, int32_t T, int32_t* err) {
-  using C = Cfg<N, K, STAGES>;
+  using C = Cfg<N, K, STAGES, NSPLIT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -54,6 +58,7 @@ __global__ void __launch_bounds__(128, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.y;
   const int m0 = blockIdx.x * 128;
+  const int n0 = blockIdx.z * C::kNC;  // first output column of this CTA
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
@@ -66,7 +71,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(smem_u32(tmem_slot), N);
+    tmem_alloc(smem_u32(tmem_slot), C::kNC);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -86,8 +91,8 @@ __global__ void __launch_bounds__(128, 1)
         mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::kStage);
         tma_load_3d(dst, &a_map, kc * 64, h, m0, full0 + 8 * st);
 #pragma unroll
-        for (int nb = 0; nb < N / 64; ++nb)
-          tma_load_3d(dst + C::kABytes + nb * 8192, &w_map, nb * 64, kc * 64, h, full0 + 8 * st);
+        for (int nb = 0; nb < C::kNC / 64; ++nb)
+          tma_load_3d(dst + C::kABytes + nb * 8192, &w_map, n0 + nb * 64, kc * 64, h, full0 + 8 * st);
         ++issued;
       }
       for (int k = (issued > STAGES ? issued - STAGES : 0); k < issued; ++k)
@@ -109,7 +114,7 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-          for (int nh = 0; nh < N / C::kMmaN; ++nh)
+          for (int nh = 0; nh < C::kNC / C::kMmaN; ++nh)
             mma_ss(tmem + nh * C::kMmaN, sdesc_sw128(sa + kk * 32, 16, 1024),
                    sdesc_sw128(sb + nh * (C::kMmaN / 64) * 8192 + kk * 2048, 8192, 1024), C::kIdesc,
                    (kc | kk) ? 1u : 0u);
@@ -128,9 +133,9 @@ __global__ void __launch_bounds__(128, 1)
   if (w) {
     const int t = m0 + warp * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-    uint4* dst = reinterpret_cast<uint4*>(c + ((size_t)t * 128 + h) * N);
+    uint4* dst = reinterpret_cast<uint4*>(c + ((size_t)t * 128 + h) * N + n0);
 #pragma unroll 1
-    for (int col = 0; col < N; col += 32) {
+    for (int col = 0; col < C::kNC; col += 32) {
       uint32_t r[32];
       __syncwarp();
       tmem_ld32_sync(tl + col, r);
@@ -149,18 +154,18 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, N);
+    tmem_dealloc(tmem, C::kNC);
   }
 }
 
-template <int N, int K, int STAGES>
+template <int N, int K, int STAGES, int NSPLIT>
 cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c, int32_t T, int32_t* err,
                 cudaStream_t stream) {
-  using C = Cfg<N, K, STAGES>;
-  auto* kern = head_gemm_kernel<N, K, STAGES>;
+  using C = Cfg<N, K, STAGES, NSPLIT>;
+  auto* kern = head_gemm_kernel<N, K, STAGES, NSPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((T + 127) / 128, 128);
+  dim3 grid((T + 127) / 128, 128, NSPLIT);
   kern<<<grid, 128, C::kSmem, stream>>>(a_map, w_map, c, T, err);
   return cudaGetLastError();
 }
@@ -169,8 +174,8 @@ cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
 
 cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
                              int32_t T, int32_t* err, cudaStream_t stream) {
-  if (kind == HeadGemm::kAbsorbQ) return gemm::run<512, 128, 2>(a_map, w_map, c, T, err, stream);
-  return gemm::run<128, 512, 4>(a_map, w_map, c, T, err, stream);
+  if (kind == HeadGemm::kAbsorbQ) return gemm::run<512, 128, 2, 2>(a_map, w_map, c, T, err, stream);
+  return gemm::run<128, 512, 4, 1>(a_map, w_map, c, T, err, stream);
 }
 
 }  // namespace mla
