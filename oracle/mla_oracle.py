@@ -287,3 +287,44 @@ def absorbed_scores(q_c_row, q_r_row, c_kv, k_r, w_uk, scale):
     """[P1] §4 path B scores [H, n]."""
     qa = absorb_q(np.asarray(q_c_row)[None], w_uk)[0]
     return scores(qa, q_r_row, c_kv, k_r, scale)
+
+
+# --------------------------------------------------------------------------
+# Decoupled RoPE in fp32 ([P1] §1, §3, §4)
+# --------------------------------------------------------------------------
+# [P1] §1: the 64-d shared RoPE vector carries the position, apart from the
+# 512-d latent.  [P1] §3's plugin settings fix the RoPE compute dtype to fp32,
+# and [P1] §4 traces a failed equivalence check to RoPE computed in fp16
+# (phase error), fixed by generating the precomputed RoPE table in fp32 and
+# multiply-adding in fp32.  The pages print no rotation formula; the reading
+# used here (listed in the design notes) is the standard rotary embedding:
+# consecutive pairs (x[2i], x[2i+1]), i < d/2, rotated by the angle
+# p * base^(-2i/d) with base 10000.
+ROPE_BASE = 10000.0
+
+
+def rope_angles(positions, dim: int = 64, base: float = ROPE_BASE) -> np.ndarray:
+    """Angle of pair i at position p: p * base^(-2i/dim), float64 [..., dim/2]."""
+    p = np.asarray(positions, dtype=np.float64)[..., None]
+    inv = base ** (-2.0 * np.arange(dim // 2, dtype=np.float64) / dim)
+    return p * inv
+
+
+def rope_table(max_pos: int, dim: int = 64, base: float = ROPE_BASE) -> np.ndarray:
+    """cos/sin of every position's angles, float64 [max_pos, dim/2, 2]."""
+    a = rope_angles(np.arange(max_pos), dim, base)
+    return np.stack([np.cos(a), np.sin(a)], axis=-1)
+
+
+def rope_apply(x: np.ndarray, positions, dim: int = 64, base: float = ROPE_BASE) -> np.ndarray:
+    """Rotate each pair (x[2i], x[2i+1]) of the last axis by its angle at the
+    broadcast position; float64.  x: [..., dim]; positions broadcast against
+    x's leading axes."""
+    x = np.asarray(x, dtype=np.float64)
+    a = rope_angles(positions, dim, base)
+    c, s = np.cos(a), np.sin(a)
+    x0, x1 = x[..., 0::2], x[..., 1::2]
+    out = np.empty_like(x)
+    out[..., 0::2] = x0 * c - x1 * s
+    out[..., 1::2] = x0 * s + x1 * c
+    return out
