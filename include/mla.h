@@ -71,6 +71,7 @@ typedef enum mla_status {
 #define MLA_DEVERR_SLOT_OOB 2u /* append/gather slot outside the pool: that token skipped */
 #define MLA_DEVERR_TIMEOUT 4u  /* an mbarrier wait exceeded its limit; the kernel stopped early */
 #define MLA_DEVERR_PLAN 8u     /* the plan buffer is not a valid decode plan */
+#define MLA_DEVERR_POS_OOB 16u /* RoPE position outside [0, max_pos): that token / row skipped */
 
 /* Thread-local message of the last failing call (never NULL). */
 const char* mla_last_error(void);
@@ -292,6 +293,50 @@ mla_status mla_decode_paged_noalloc(const void* q_abs, const void* q_r, const vo
                                     int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                                     const int32_t* seq_lens_host, const int32_t* q_lens_host, int32_t B,
                                     float scale, void* o_lat, float* lse, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Decoupled RoPE in fp32 ([P1] §1: the 64-d RoPE key carries the position
+ * apart from the latent; §3: the plugin's RoPE compute dtype is fp32; §4:
+ * the RoPE table is generated in fp32 and applied with fp32 multiply-adds).
+ * Rotation: consecutive pairs (x[2i], x[2i+1]), i < 32, turned by the angle
+ * p * base^(-2i/64) (the pages print no formula; the standard rotary
+ * embedding, base 10000 by convention).
+ * Shared rules: table is 16-byte aligned, positions and dev_err 4-byte
+ * aligned (else MLA_ERR_MISALIGNED); NULL pointers, negative counts and
+ * max_pos < 1 are MLA_ERR_INVALID_ARG and enqueue nothing.
+ * ------------------------------------------------------------------------- */
+
+/*
+ * Fill table fp32 [max_pos, 32, 2] (device, caller-owned, 256 B per
+ * position) with (cos, sin) of every position's angles, each computed in
+ * double precision and rounded once to fp32.  base must be finite and > 1;
+ * max_pos in [1, 2^24].  max_pos == 0 is a no-op.
+ */
+mla_status mla_rope_table(int32_t max_pos, float base, float* table, void* stream);
+
+/*
+ * Step A1 with the RoPE key rotated on the way in.  For i < n:
+ *   kv_cache[slots[i]] = [c_kv_new[i, 0:512] | rope(k_pe_new[i, 0:64], positions[i])]
+ * c_kv_new bf16 [n, 512] (copied bit for bit), k_pe_new bf16 [n, 64] (the
+ * unrotated key), positions int32 [n] (each token's position in its sequence),
+ * table from mla_rope_table with max_pos rows, slots int64 [n]; all device.
+ * The rotation is fp32 (fused multiply-add) rounded to bf16.  A slot outside
+ * the pool sets MLA_DEVERR_SLOT_OOB, a position outside [0, max_pos) sets
+ * MLA_DEVERR_POS_OOB; either way that token is skipped.  n == 0 is a no-op.
+ */
+mla_status mla_kv_append_rope(const void* c_kv_new, const void* k_pe_new, const int32_t* positions,
+                              const float* table, int32_t max_pos, const int64_t* slots, int32_t n,
+                              void* kv_cache, int64_t num_pages, int32_t* dev_err, void* stream);
+
+/*
+ * Rotate the queries' RoPE part: q_r[t, h, :] = rope(q_pe[t, h, :], positions[t]),
+ * q_pe and q_r bf16 [T, 128, 64] (may not overlap), positions int32 [T], table
+ * as above; fp32 rotation rounded to bf16.  A position outside [0, max_pos)
+ * sets MLA_DEVERR_POS_OOB and leaves that token's rows unwritten.  T == 0
+ * is a no-op; overlapping q_pe and q_r is MLA_ERR_INVALID_ARG.
+ */
+mla_status mla_rope_q(const void* q_pe, const int32_t* positions, const float* table, int32_t max_pos,
+                      void* q_r, int32_t T, int32_t* dev_err, void* stream);
 
 /*
  * Synchronise `stream`, read the device error word into *word_out (may be

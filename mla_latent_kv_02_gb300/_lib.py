@@ -48,6 +48,9 @@ SIGNATURES = {
     "mla_cache_init": (C.c_int, [P, I64, P]),
     "mla_kv_append": (C.c_int, [P, P, P, I32, P, I64, P, P]),
     "mla_gather_paged": (C.c_int, [P, I64, P, I32, I32, I32, P, P, P]),
+    "mla_rope_table": (C.c_int, [I32, C.c_float, P, P]),
+    "mla_kv_append_rope": (C.c_int, [P, P, P, P, I32, P, I32, P, I64, P, P]),
+    "mla_rope_q": (C.c_int, [P, P, P, I32, P, I32, P, P]),
     "mla_absorb_q": (C.c_int, [P, P, P, I32, P, P]),
     "mla_up_v": (C.c_int, [P, P, P, I32, P, P]),
     "mla_decode_max_clusters": (C.c_int, [PI32]),

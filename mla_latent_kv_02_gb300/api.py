@@ -21,7 +21,7 @@ D_QK = D_C + D_R
 
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_MISALIGNED", 3: "MLA_ERR_UNSUPPORTED",
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE", 6: "MLA_ERR_TIMEOUT", 7: "MLA_ERR_NO_SPACE"}
-DEVERR_PAGE_OOB, DEVERR_SLOT_OOB, DEVERR_TIMEOUT, DEVERR_PLAN = 1, 2, 4, 8
+DEVERR_PAGE_OOB, DEVERR_SLOT_OOB, DEVERR_TIMEOUT, DEVERR_PLAN, DEVERR_POS_OOB = 1, 2, 4, 8, 16
 
 
 class MlaError(RuntimeError):
@@ -134,6 +134,40 @@ def mla_kv_append(c_kv_new, k_r_new, slots, kv_cache, dev_err, stream=None) -> N
     _need(dev_err, "dev_err", torch.int32, (1,))
     _check(lib().mla_kv_append(_ptr(c_kv_new), _ptr(k_r_new), _ptr(slots), int(n), _ptr(kv_cache),
                                kv_cache.shape[0], _ptr(dev_err), _stream(stream)))
+
+
+def mla_rope_table(max_pos: int, table, base: float = 10000.0, stream=None) -> None:
+    _need(table, "table", torch.float32, (max_pos, D_R // 2, 2))
+    _check(lib().mla_rope_table(int(max_pos), float(base), _ptr(table), _stream(stream)))
+
+
+def mla_kv_append_rope(c_kv_new, k_pe_new, positions, table, slots, kv_cache, dev_err, stream=None) -> None:
+    n = c_kv_new.shape[0]
+    _need(c_kv_new, "c_kv_new", torch.bfloat16, (n, D_C))
+    _need(k_pe_new, "k_pe_new", torch.bfloat16, (n, D_R))
+    _need(positions, "positions", torch.int32, (n,))
+    _need(table, "table", torch.float32)
+    _need(slots, "slots", torch.int64, (n,))
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    if table.dim() != 3 or tuple(table.shape[1:]) != (D_R // 2, 2):
+        raise ValueError(f"table has shape {tuple(table.shape)}, expected (max_pos, {D_R // 2}, 2)")
+    _check(lib().mla_kv_append_rope(_ptr(c_kv_new), _ptr(k_pe_new), _ptr(positions), _ptr(table), table.shape[0],
+                                    _ptr(slots), int(n), _ptr(kv_cache), kv_cache.shape[0], _ptr(dev_err),
+                                    _stream(stream)))
+
+
+def mla_rope_q(q_pe, positions, table, q_r, dev_err, stream=None) -> None:
+    T = q_pe.shape[0]
+    _need(q_pe, "q_pe", torch.bfloat16, (T, H, D_R))
+    _need(positions, "positions", torch.int32, (T,))
+    _need(table, "table", torch.float32)
+    _need(q_r, "q_r", torch.bfloat16, (T, H, D_R))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    if table.dim() != 3 or tuple(table.shape[1:]) != (D_R // 2, 2):
+        raise ValueError(f"table has shape {tuple(table.shape)}, expected (max_pos, {D_R // 2}, 2)")
+    _check(lib().mla_rope_q(_ptr(q_pe), _ptr(positions), _ptr(table), table.shape[0], _ptr(q_r), int(T),
+                            _ptr(dev_err), _stream(stream)))
 
 
 def mla_gather_paged(kv_cache, block_table, b: int, n_tokens: int, out, dev_err, stream=None) -> None:

@@ -86,6 +86,12 @@ cudaError_t launch_combine(const CombineArgs& args, int num_split_rows, cudaStre
 
 cudaError_t launch_kv_append(const uint16_t* c_kv_new, const uint16_t* k_r_new, const int64_t* slots, int32_t n,
                              uint16_t* kv_cache, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_rope_table(float* table, int32_t max_pos, double base, cudaStream_t stream);
+cudaError_t launch_kv_append_rope(const uint16_t* c_kv_new, const uint16_t* k_pe_new, const int32_t* positions,
+                                  const float* table, int32_t max_pos, const int64_t* slots, int32_t n,
+                                  uint16_t* kv_cache, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_rope_q(const uint16_t* q_pe, const int32_t* positions, const float* table, int32_t max_pos,
+                          uint16_t* q_r, int32_t T, int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                           int32_t b, int32_t n_tokens, uint16_t* out, int32_t* dev_err, cudaStream_t stream);
 

@@ -416,6 +416,68 @@ mla_status mla_kv_append(const void* c_kv_new, const void* k_r_new, const int64_
   return MLA_OK;
 }
 
+mla_status mla_rope_table(int32_t max_pos, float base, float* table, void* stream) {
+  if (max_pos < 0 || max_pos > (1 << 24)) return fail(MLA_ERR_INVALID_ARG, "max_pos = %d outside [0, 2^24]", max_pos);
+  if (!(base > 1.f) || !std::isfinite(base)) return fail(MLA_ERR_INVALID_ARG, "base must be finite and > 1");
+  if (max_pos == 0) return MLA_OK;
+  CHECK_PTR(table);
+  CHECK_ALIGN16(table);
+  cudaError_t e = mla::launch_rope_table(table, max_pos, (double)base, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope_table launch");
+  return MLA_OK;
+}
+
+mla_status mla_kv_append_rope(const void* c_kv_new, const void* k_pe_new, const int32_t* positions, const float* table,
+                              int32_t max_pos, const int64_t* slots, int32_t n, void* kv_cache, int64_t num_pages,
+                              int32_t* dev_err, void* stream) {
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (n == 0) return MLA_OK;
+  CHECK_PTR(c_kv_new);
+  CHECK_PTR(k_pe_new);
+  CHECK_PTR(positions);
+  CHECK_PTR(table);
+  CHECK_PTR(slots);
+  CHECK_PTR(kv_cache);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(c_kv_new);
+  CHECK_ALIGN16(k_pe_new);
+  CHECK_ALIGN16(kv_cache);
+  CHECK_ALIGN16(table);
+  if (!aligned(slots, 8)) return fail(MLA_ERR_MISALIGNED, "slots is not 8-byte aligned");
+  if (!aligned(positions, 4) || !aligned(dev_err, 4))
+    return fail(MLA_ERR_MISALIGNED, "positions and dev_err must be 4-byte aligned");
+  if (max_pos < 1) return fail(MLA_ERR_INVALID_ARG, "max_pos = %d < 1", max_pos);
+  if (num_pages < 1) return fail(MLA_ERR_INVALID_ARG, "num_pages = %lld < 1", (long long)num_pages);
+  cudaError_t e = mla::launch_kv_append_rope((const uint16_t*)c_kv_new, (const uint16_t*)k_pe_new, positions, table,
+                                             max_pos, slots, n, (uint16_t*)kv_cache, num_pages * MLA_PAGE_SIZE,
+                                             dev_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append_rope launch");
+  return MLA_OK;
+}
+
+mla_status mla_rope_q(const void* q_pe, const int32_t* positions, const float* table, int32_t max_pos, void* q_r,
+                      int32_t T, int32_t* dev_err, void* stream) {
+  if (T < 0) return fail(MLA_ERR_INVALID_ARG, "T = %d < 0", T);
+  if (T == 0) return MLA_OK;
+  CHECK_PTR(q_pe);
+  CHECK_PTR(positions);
+  CHECK_PTR(table);
+  CHECK_PTR(q_r);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(q_pe);
+  CHECK_ALIGN16(q_r);
+  if (!aligned(positions, 4) || !aligned(dev_err, 4))
+    return fail(MLA_ERR_MISALIGNED, "positions and dev_err must be 4-byte aligned");
+  CHECK_ALIGN16(table);
+  if (max_pos < 1) return fail(MLA_ERR_INVALID_ARG, "max_pos = %d < 1", max_pos);
+  const uintptr_t a0 = (uintptr_t)q_pe, b0 = (uintptr_t)q_r, len = (uintptr_t)T * MLA_NUM_HEADS * MLA_ROPE_DIM * 2;
+  if (a0 < b0 + len && b0 < a0 + len) return fail(MLA_ERR_INVALID_ARG, "q_pe and q_r overlap");
+  cudaError_t e = mla::launch_rope_q((const uint16_t*)q_pe, positions, table, max_pos, (uint16_t*)q_r, T, dev_err,
+                                     (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "rope_q launch");
+  return MLA_OK;
+}
+
 mla_status mla_gather_paged(const void* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                             int32_t b, int32_t n_tokens, void* out, int32_t* dev_err, void* stream) {
   if (n_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "n_tokens = %d < 0", n_tokens);

@@ -109,6 +109,11 @@ class Case:
             out.extend(range(int(off[b]) + n - q, int(off[b]) + n))
         return np.asarray(out, dtype=np.int64)
 
+    def query_positions(self) -> np.ndarray:
+        """Position of each query row's token in its sequence (int32 [T])."""
+        out = [np.arange(int(n) - int(q), int(n), dtype=np.int32) for n, q in zip(self.seq_lens, self.q_lens)]
+        return np.concatenate(out) if out else np.zeros(0, np.int32)
+
     def positions(self) -> tuple:
         """(seq_ids, positions) of every cached token, in c_kv row order."""
         seq = np.repeat(np.arange(self.B, dtype=np.int32), self.seq_lens)

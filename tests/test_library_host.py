@@ -225,3 +225,40 @@ def test_device_calls_validate_before_any_launch(api):
     assert lib.mla_decode_paged(ok, ok, ok, 200, ok, 110, ok, C.byref(pinfo), C.c_float(0.07), ok, 16,
                                 ok, None, err, None) == 1
     assert "workspace" in lib.mla_last_error().decode()
+
+
+def test_rope_calls_validate_before_any_launch(api):
+    """RoPE entry points reject bad arguments on the host (nothing is enqueued)."""
+    lib = _lib.lib()
+    P = C.c_void_p
+    ok = P(0x10000)
+    odd8 = P(0x10004)    # 4-byte but not 8-byte aligned
+    odd16 = P(0x10008)   # 8-byte but not 16-byte aligned
+    err = P(0x20000)
+    f = C.c_float
+    # table: base must be finite and > 1; max_pos within [0, 2^24]; 0 rows is a no-op
+    assert lib.mla_rope_table(16, f(1.0), ok, None) == 1
+    assert lib.mla_rope_table(16, f(float("inf")), ok, None) == 1
+    assert lib.mla_rope_table(16, f(float("nan")), ok, None) == 1
+    assert lib.mla_rope_table((1 << 24) + 1, f(10000.0), ok, None) == 1
+    assert lib.mla_rope_table(-1, f(10000.0), ok, None) == 1
+    assert lib.mla_rope_table(16, f(10000.0), None, None) == 1
+    assert lib.mla_rope_table(16, f(10000.0), odd8, None) == 2
+    assert lib.mla_rope_table(16, f(10000.0), odd16, None) == 2
+    assert lib.mla_rope_table(0, f(10000.0), None, None) == 0
+    # append with rotation
+    assert lib.mla_kv_append_rope(ok, ok, ok, ok, 64, ok, -1, ok, 4, err, None) == 1
+    assert lib.mla_kv_append_rope(None, None, None, None, 0, None, 0, None, 0, None, None) == 0
+    assert lib.mla_kv_append_rope(ok, ok, None, ok, 64, ok, 1, ok, 4, err, None) == 1
+    assert lib.mla_kv_append_rope(ok, odd16, ok, ok, 64, ok, 1, ok, 4, err, None) == 2
+    assert lib.mla_kv_append_rope(ok, ok, ok, odd8, 64, ok, 1, ok, 4, err, None) == 2
+    assert lib.mla_rope_q(ok, ok, odd16, 64, P(0x90000), 1, err, None) == 2
+    assert lib.mla_kv_append_rope(ok, ok, ok, ok, 0, ok, 1, ok, 4, err, None) == 1
+    assert lib.mla_kv_append_rope(ok, ok, ok, ok, 64, ok, 1, ok, 0, err, None) == 1
+    # query rotation: alignment, max_pos, overlap of input and output
+    assert lib.mla_rope_q(None, None, None, 0, None, 0, None, None) == 0
+    assert lib.mla_rope_q(ok, ok, ok, 64, ok, -1, err, None) == 1
+    assert lib.mla_rope_q(odd16, ok, ok, 64, P(0x90000), 1, err, None) == 2
+    assert lib.mla_rope_q(ok, ok, ok, 0, P(0x90000), 1, err, None) == 1
+    assert lib.mla_rope_q(ok, ok, ok, 64, P(0x10000 + 16384 - 16), 1, err, None) == 1   # overlaps by 16 B
+    assert "overlap" in lib.mla_last_error().decode()
