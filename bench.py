@@ -203,13 +203,15 @@ def _time_launches(torch, stream, fn, reps=5, warmup=3):
     return a.elapsed_time(b) / reps * 1e3
 
 
-def measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos_old, q_r, kv, dev_err, hbm_gbs):
+def measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos_old, q_r, kv, dev_err, hbm_gbs,
+                 plan=None, q_abs=None, st=None, peaks=None):
     """HBM-bound kernels outside the timed step, each timed alone (outside the
     step's timed region; inputs larger than L2): the bulk cache fill (A1 over
     the whole context), the same fill with the RoPE key rotated on the way in,
-    and the query RoPE rotation for this step's rows and for a prefill-sized
-    block of rows.  Algorithmic bytes: every operand read once, every output
-    written once; a RoPE table row is counted once per distinct position."""
+    the query RoPE rotation for this step's rows and for a prefill-sized block
+    of rows, the quantising FP8 fill and the decode step over the FP8 cache.
+    Algorithmic bytes: every operand read once, every output written once; a
+    RoPE table row is counted once per distinct position."""
     n = int(c_old.shape[0])
     max_pos = int(case.seq_lens.max())
     table = torch.empty((max_pos, 32, 2), dtype=torch.float32, device=dev)
@@ -246,8 +248,39 @@ def measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos_old
     qo = torch.empty_like(qp)
     us = _time_launches(torch, stream, lambda i: api.mla_rope_q(qp, pp, table, qo, dev_err))
     entry("rope_q_prefill8192", us, Tp * (128 * 128 * 2 + 4) + min(Tp, max_pos) * 256, rows=Tp * 128)
+    del qp, qo
+    if plan is not None:
+        # FP8 (E4M3) cache: quantising fill of the whole context, then the
+        # decode step over it (the same plan), against the same roofline as
+        # the bf16 decode: flops unchanged, KV bytes 644 per token.
+        rows = torch.empty((case.num_pages, 64, 640), dtype=torch.uint8, device=dev)
+        scales = torch.ones((case.num_pages, 64), dtype=torch.float32, device=dev)
+        rows.zero_()
+        us = _time_launches(torch, stream, lambda i: api.mla_kv_append_fp8(c_old, k_old, slots_old, rows, scales,
+                                                                             dev_err))
+        entry("kv_append_fp8_bulk", us, n * (1152 + 8 + 644), tokens=n)
+        new_idx = case.new_token_index()
+        seq, pos = case.positions()
+        slots_new = torch.from_numpy(api.mla_slot_mapping(case.block_table, seq, pos)[new_idx]).to(dev)
+        c_new = torch.from_numpy(np.ascontiguousarray(case.c_kv[new_idx])).to(device=dev, dtype=torch.bfloat16)
+        k_new = torch.from_numpy(np.ascontiguousarray(case.k_r[new_idx])).to(device=dev, dtype=torch.bfloat16)
+        api.mla_kv_append_fp8(c_new, k_new, slots_new, rows, scales, dev_err)
+        bt = torch.from_numpy(case.block_table).to(dev)
+        o8 = torch.empty((q_abs.shape[0], 128, 512), dtype=torch.bfloat16, device=dev)
+        l8 = torch.empty((q_abs.shape[0], 128), dtype=torch.float32, device=dev)
+        us = _time_launches(torch, stream, lambda i: api.mla_decode_paged_fp8(q_abs, q_r, rows, scales, bt, plan, o8,
+                                                                               dev_err, lse=l8, scale=SCALE))
+        fbytes = st["kv_tokens"] * 644 + st["T"] * 128 * (576 + 512) * 2
+        t_f = st["flops"] / (peaks["bf16_tflops"] * 1e12)
+        t_b = fbytes / (peaks["hbm_gbs"] * 1e9)
+        tf = st["flops"] / (us * 1e-6) / 1e12
+        out["decode_paged_fp8"] = dict(us=round(us, 2), bytes=int(fbytes), gbs=round(fbytes / (us * 1e-6) / 1e9, 1),
+                                       tflops=round(tf, 1), bound="tensor" if t_f >= t_b else "hbm",
+                                       frac=round(max(t_f, t_b) / (us * 1e-6), 4),
+                                       peak_source=peaks["source"] + " (burst)")
+        del rows, scales
     if api.mla_check(dev_err) != 0:
-        raise RuntimeError("device error word set while timing the cache-fill and RoPE kernels")
+        raise RuntimeError("device error word set while timing the cache-fill, RoPE and FP8 kernels")
     # put the unrotated keys back (the cache holds them for the step above)
     api.mla_kv_append(c_old, k_old, slots_old, kv, dev_err)
     return out
@@ -374,7 +407,7 @@ def run_mla(args):
 
     peaks = load_peaks()
     rows = measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos[old_idx], q_r, kv, dev_err,
-                        peaks["hbm_gbs"]) if old_idx.size else {}
+                        peaks["hbm_gbs"], plan=plan, q_abs=q_abs, st=st, peaks=peaks) if old_idx.size else {}
     step_s = ms_total / 1e3 / K
     tokens = T * ws
     value = tokens / step_s

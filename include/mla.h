@@ -338,6 +338,55 @@ mla_status mla_kv_append_rope(const void* c_kv_new, const void* k_pe_new, const 
 mla_status mla_rope_q(const void* q_pe, const int32_t* positions, const float* table, int32_t max_pos,
                       void* q_r, int32_t T, int32_t* dev_err, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * FP8 (E4M3) latent cache ([P3] bjbfmj.com/news/60700: quantisation scale
+ * factors are stored beside the cached elements; [P1] opening section and
+ * §5: a quantised gather with 16-byte vector loads).  E4M3 is the OCP 8-bit
+ * floating point format (bias 7, 3 mantissa bits, subnormals, max 448).
+ * Each token's 512 latent values share a power-of-two scale 2^k, k the
+ * smallest integer with max|c| <= 448 * 2^k (k = 0 for an all-zero row);
+ * codes are c * 2^-k rounded to the nearest E4M3 value, ties to even.  The
+ * 64 RoPE values stay bf16.
+ *
+ * Layout (caller-owned device memory):
+ *   rows   uint8 [num_pages][64][MLA_FP8_ROW_BYTES]: codes 0..511, then the
+ *          64 bf16 RoPE values (bytes 512..639); 16-byte aligned;
+ *   scales fp32 [num_pages][64]: 2^k per token; 16-byte aligned.
+ * 644 bytes per token against 1152 for the bf16 cache.
+ * ------------------------------------------------------------------------- */
+#define MLA_FP8_ROW_BYTES 640
+
+/*
+ * Quantise and store: for i < n, rows[slots[i]] = [codes(c_kv_new[i]) | k_r_new[i]]
+ * and scales[slots[i]] = 2^k.  c_kv_new bf16 [n, 512], k_r_new bf16 [n, 64],
+ * slots int64 [n] (8-byte aligned).  A slot outside the pool sets
+ * MLA_DEVERR_SLOT_OOB and that token is skipped.  n == 0 is a no-op.
+ */
+mla_status mla_kv_append_fp8(const void* c_kv_new, const void* k_r_new, const int64_t* slots, int32_t n,
+                             void* rows, float* scales, int64_t num_pages, int32_t* dev_err, void* stream);
+
+/*
+ * Dequantising gather: out bf16 [n_tokens, 576] = the first n_tokens cached
+ * tokens of sequence b, latent as code * 2^k (exact in bf16), then the RoPE
+ * values bit for bit.  Errors as for mla_gather_paged.
+ */
+mla_status mla_gather_paged_fp8(const void* rows, const float* scales, int64_t num_pages,
+                                const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
+                                void* out, int32_t* dev_err, void* stream);
+
+/*
+ * Steps A3 and A4 over the FP8 cache: as mla_decode_paged with kv_cache
+ * replaced by (rows, scales) above.  The latent is dequantised exactly to
+ * bf16 on chip (code * 2^k), so the attention sees the same values the
+ * dequantising gather returns; the same plan and workspace serve both
+ * formats.  Every slot read must hold finite codes (E4M3 NaN codes are never
+ * written by mla_kv_append_fp8) and a power-of-two scale.
+ */
+mla_status mla_decode_paged_fp8(const void* q_abs, const void* q_r, const void* rows, const float* scales,
+                                int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                const void* plan_dev, const mla_plan_info* info, float scale, void* workspace,
+                                size_t ws_bytes, void* o_lat, float* lse, int32_t* dev_err, void* stream);
+
 /*
  * Synchronise `stream`, read the device error word into *word_out (may be
  * NULL) and map it: 0 -> MLA_OK, MLA_DEVERR_TIMEOUT set -> MLA_ERR_TIMEOUT,

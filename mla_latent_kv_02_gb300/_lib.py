@@ -48,6 +48,8 @@ SIGNATURES = {
     "mla_cache_init": (C.c_int, [P, I64, P]),
     "mla_kv_append": (C.c_int, [P, P, P, I32, P, I64, P, P]),
     "mla_gather_paged": (C.c_int, [P, I64, P, I32, I32, I32, P, P, P]),
+    "mla_kv_append_fp8": (C.c_int, [P, P, P, I32, P, P, I64, P, P]),
+    "mla_gather_paged_fp8": (C.c_int, [P, P, I64, P, I32, I32, I32, P, P, P]),
     "mla_rope_table": (C.c_int, [I32, C.c_float, P, P]),
     "mla_kv_append_rope": (C.c_int, [P, P, P, P, I32, P, I32, P, I64, P, P]),
     "mla_rope_q": (C.c_int, [P, P, P, I32, P, I32, P, P]),
@@ -59,6 +61,8 @@ SIGNATURES = {
     "mla_decode_plan_host": (C.c_int, [PI32, PI32, I32, I32, P, SZ, C.POINTER(mla_plan_info)]),
     "mla_decode_plan": (C.c_int, [PI32, PI32, I32, I32, P, SZ, C.POINTER(mla_plan_info), P]),
     "mla_decode_paged": (C.c_int, [P, P, P, I64, P, I32, P, C.POINTER(mla_plan_info), C.c_float, P, SZ, P, P, P, P]),
+    "mla_decode_paged_fp8": (C.c_int, [P, P, P, P, I64, P, I32, P, C.POINTER(mla_plan_info), C.c_float, P, SZ, P, P,
+                                       P, P]),
     "mla_check": (C.c_int, [P, P, PI32]),
     "mla_decode_paged_noalloc": (C.c_int, [P, P, P, I64, P, I32, PI32, PI32, I32, C.c_float, P, P, P, P]),
 }

@@ -136,6 +136,33 @@ def mla_kv_append(c_kv_new, k_r_new, slots, kv_cache, dev_err, stream=None) -> N
                                kv_cache.shape[0], _ptr(dev_err), _stream(stream)))
 
 
+FP8_ROW_BYTES = 640
+
+
+def mla_kv_append_fp8(c_kv_new, k_r_new, slots, rows, scales, dev_err, stream=None) -> None:
+    """Quantise new tokens into the FP8 cache: rows uint8 [pages, 64, 640], scales fp32 [pages, 64]."""
+    n = c_kv_new.shape[0]
+    _need(c_kv_new, "c_kv_new", torch.bfloat16, (n, D_C))
+    _need(k_r_new, "k_r_new", torch.bfloat16, (n, D_R))
+    _need(slots, "slots", torch.int64, (n,))
+    _need(rows, "rows", torch.uint8, (rows.shape[0], PAGE, FP8_ROW_BYTES))
+    _need(scales, "scales", torch.float32, (rows.shape[0], PAGE))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_kv_append_fp8(_ptr(c_kv_new), _ptr(k_r_new), _ptr(slots), int(n), _ptr(rows), _ptr(scales),
+                                   rows.shape[0], _ptr(dev_err), _stream(stream)))
+
+
+def mla_gather_paged_fp8(rows, scales, block_table, b: int, n_tokens: int, out, dev_err, stream=None) -> None:
+    _need(rows, "rows", torch.uint8, (rows.shape[0], PAGE, FP8_ROW_BYTES))
+    _need(scales, "scales", torch.float32, (rows.shape[0], PAGE))
+    _need(block_table, "block_table", torch.int32)
+    _need(out, "out", torch.bfloat16, (n_tokens, D_QK))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_gather_paged_fp8(_ptr(rows), _ptr(scales), rows.shape[0], _ptr(block_table),
+                                      block_table.shape[1], int(b), int(n_tokens), _ptr(out), _ptr(dev_err),
+                                      _stream(stream)))
+
+
 def mla_rope_table(max_pos: int, table, base: float = 10000.0, stream=None) -> None:
     _need(table, "table", torch.float32, (max_pos, D_R // 2, 2))
     _check(lib().mla_rope_table(int(max_pos), float(base), _ptr(table), _stream(stream)))
@@ -279,6 +306,27 @@ def mla_decode_paged(q_abs, q_r, kv_cache, block_table, plan: DecodePlan, o_lat,
                                   block_table.shape[1], _ptr(plan.plan), C.byref(plan.info), float(scale),
                                   _ptr(plan.workspace), plan.workspace.numel(), _ptr(o_lat), _ptr(lse),
                                   _ptr(dev_err), _stream(stream)))
+
+
+def mla_decode_paged_fp8(q_abs, q_r, rows, scales, block_table, plan: DecodePlan, o_lat, dev_err, lse=None,
+                         scale: float = 1.0 / (192 ** 0.5), stream=None) -> None:
+    """Steps A3 + A4 over the FP8 cache (rows uint8 [pages, 64, 640], scales fp32 [pages, 64])."""
+    T = q_abs.shape[0]
+    _need(q_abs, "q_abs", torch.bfloat16, (T, H, D_C))
+    _need(q_r, "q_r", torch.bfloat16, (T, H, D_R))
+    _need(rows, "rows", torch.uint8, (rows.shape[0], PAGE, FP8_ROW_BYTES))
+    _need(scales, "scales", torch.float32, (rows.shape[0], PAGE))
+    _need(block_table, "block_table", torch.int32)
+    _need(o_lat, "o_lat", torch.bfloat16, (T, H, D_C))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    if lse is not None:
+        _need(lse, "lse", torch.float32, (T, H))
+    if int(plan.info.T) != T:
+        raise ValueError(f"plan has {plan.info.T} rows, q_abs has {T}")
+    _check(lib().mla_decode_paged_fp8(_ptr(q_abs), _ptr(q_r), _ptr(rows), _ptr(scales), rows.shape[0],
+                                      _ptr(block_table), block_table.shape[1], _ptr(plan.plan), C.byref(plan.info),
+                                      float(scale), _ptr(plan.workspace), plan.workspace.numel(), _ptr(o_lat),
+                                      _ptr(lse), _ptr(dev_err), _stream(stream)))
 
 
 def mla_check(dev_err, stream=None) -> int:

@@ -51,6 +51,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "fp8.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -64,8 +65,6 @@ constexpr int kChunk = 64;                                // elements in one 128
 constexpr int kChunkBytes = kPage * kChunk * 2;           // [64 tokens x 64] bf16 = 8 KB
 constexpr int kRopeHalf = 32;                             // RoPE dims per CTA
 constexpr int kRopeBytes = kPage * kRopeHalf * 2;         // [64 tokens x 32] bf16 = 4 KB, 64-byte rows
-constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes; // 36 KB
-constexpr int kStages = 4;
 constexpr int kXBytes = kH * kPage * 2;                   // one CTA's fp16 partial S (16 KB)
 // Softmax: two warpgroups take alternate tiles whole (thread = head row).
 constexpr int kSWarps = 8;
@@ -77,24 +76,86 @@ constexpr int kXLead = kXBufs - 2;                        // staging buffer offs
 static_assert(kXLead >= 1 && kXLead <= kXBufs - 2, "the exchange ring needs two tiles between staging and reuse");
 constexpr int kOnesBytes = 16 * kChunk * 2;               // [16 x 64] bf16 ones for the row sums
 
+// FP8 stage (one page, this CTA's half): the 32 KB latent area, whose first
+// 16 KB first receive the 64 token rows of 256 E4M3 codes and are then
+// overwritten by their bf16 values; the RoPE half (64-byte swizzle); the 64
+// token scales.
+constexpr int kF8Codes = kPage * 256;                     // 16 KB
+constexpr int kF8RopeOff = 4 * kChunkBytes;               // 32 KB
+constexpr int kF8ScaleOff = kF8RopeOff + kRopeBytes;
+constexpr int kF8Payload = kF8Codes + kRopeBytes + kPage * 4;  // bytes the TMA delivers per stage
+constexpr int kF8StageBytes = 37 * 1024;                  // keeps every stage 1024-byte aligned
+constexpr int kConvWarps = 4;
+constexpr uint32_t kConvBarrier = 1;                      // named barrier of the converter warps
+static_assert(kF8ScaleOff + kPage * 4 <= kF8StageBytes, "FP8 stage too small");
+
 // Shared memory: a small region (barriers, row-max slots, flags) at the
-// start, then the 1024-byte aligned region (page ring, exchange ring, the
-// ones tile).
+// start, then the 1024-byte aligned region (page ring, FP8 staging ring,
+// exchange ring, the ones tile).
 constexpr int kNumBars = 32;
 constexpr int kSmallBar = 0;
 constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [4][128]: {reference max bits, tile}
 constexpr int kSmallMisc = kSmallPair + 4 * kH * 8;
 constexpr int kSmallBytes = kSmallMisc + 64;
-constexpr int kOffKV = 0;
-constexpr int kOffX = kStages * kStageBytes;
-constexpr int kOffOnes = kOffX + kXBufs * kXBytes;
-constexpr int kAlignedBytes = kOffOnes + kOnesBytes;
-constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
-static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
+
+// The two cache formats.  bf16: the producer's TMA fills a 4-deep ring of
+// [latent half | RoPE half] stages.  FP8: the TMA fills the same 4-deep ring
+// with [codes | RoPE half | scales], and a converter warpgroup dequantises
+// the codes in place (all codes read into registers, a barrier, then the
+// bf16 rows written over them).  Warp roles:
+//   bf16: 0 producer, 1 QK^T, 2-9 softmax, 10 P·V                (352 threads)
+//   FP8:  0 producer, 1 QK^T, 2 P·V, 3 idle, 4-11 softmax,
+//         12-15 converters; warpgroups 0 and 3 give registers to 1 and 2 (512)
+template <bool kF8>
+struct Cfg;
+template <>
+struct Cfg<false> {
+  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = 4 * kChunkBytes + kRopeBytes;  // 36 KB
+  static constexpr int kSoftWarp0 = 2, kPvWarp = 2 + kSWarps, kConvWarp0 = 1 << 20;
+  static constexpr int kThreads = 32 * (kPvWarp + 1);
+};
+template <>
+struct Cfg<true> {
+  static constexpr int kStages = 4;
+  static constexpr int kStageBytes = kF8StageBytes;                 // 37 KB
+  static constexpr int kSoftWarp0 = 4, kPvWarp = 2, kConvWarp0 = 12;
+  static constexpr int kThreads = 512;
+};
+
+template <bool kF8>
+struct Layout : Cfg<kF8> {
+  using C = Cfg<kF8>;
+  static constexpr int kOffKV = 0;
+  static constexpr int kOffX = C::kStages * C::kStageBytes;
+  static constexpr int kOffOnes = kOffX + kXBufs * kXBytes;
+  static constexpr int kAlignedBytes = kOffOnes + kOnesBytes;
+  static constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
+  static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
+  enum : int {
+    B_KV_FULL = 0,
+    B_KV_EMPTY = C::kStages,
+    // S_FULL and O_DONE come in pairs by tile parity: each softmax warpgroup
+    // waits only on its own tiles' phases, in order (a parity test cannot tell
+    // a phase from the one two before it, and the warpgroups run apart).
+    B_S_FULL0 = 2 * C::kStages,
+    B_S_FULL1,
+    B_S_FREE,
+    B_P_FULL,
+    B_O_DONE0,
+    B_O_DONE1,
+    B_Q_READY,
+    B_O_FREE,
+    B_X_FULL0,                      // exchange buffer i filled by the peer
+    B_DRAIN = B_X_FULL0 + kXBufs,
+    B_DRAIN_PV,
+    B_F8_FULL,                      // FP8: stage i's codes, RoPE half and scales landed
+    B_COUNT = B_F8_FULL + (kF8 ? C::kStages : 0)
+  };
+  static_assert(B_COUNT <= kNumBars, "barrier area too small");
+};
 
 constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 480, kTmemCols = 512;
-constexpr int kPvWarp = 2 + kSWarps;                      // warps: producer, QK^T, softmax..., P·V
-constexpr int kThreads = 32 * (kPvWarp + 1);
 // The producer and the two MMA-issuing threads poll (mbarrier.test_wait)
 // rather than sleep: their wake-up sits on the score chain.
 constexpr bool kIssueSuspend = false;
@@ -103,27 +164,6 @@ constexpr uint32_t kTileThreads = 128;                    // the warpgroup that 
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
 constexpr uint32_t kIdescSum = idesc_bf16_f32(128, 16, false, false);
-
-enum : int {
-  B_KV_FULL = 0,
-  B_KV_EMPTY = kStages,
-  // S_FULL and O_DONE come in pairs by tile parity: each softmax warpgroup
-  // waits only on its own tiles' phases, in order (a parity test cannot tell
-  // a phase from the one two before it, and the warpgroups run apart).
-  B_S_FULL0 = 2 * kStages,
-  B_S_FULL1,
-  B_S_FREE,
-  B_P_FULL,
-  B_O_DONE0,
-  B_O_DONE1,
-  B_Q_READY,
-  B_O_FREE,
-  B_X_FULL0,                      // exchange buffer i filled by the peer
-  B_DRAIN = B_X_FULL0 + kXBufs,
-  B_DRAIN_PV,
-  B_COUNT
-};
-static_assert(B_COUNT <= kNumBars, "barrier area too small");
 
 // Walks the 64-token tiles of a cluster's segments in order; a segment's
 // fields are read from the plan once, when the cursor enters it.
@@ -161,9 +201,23 @@ struct TileCursor {
 __device__ __forceinline__ __half2 as_h2(uint32_t u) { return *reinterpret_cast<const __half2*>(&u); }
 __device__ __forceinline__ uint32_t as_u32(__half2 h) { return *reinterpret_cast<const uint32_t*>(&h); }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+// kv_map / rope_map: bf16 cache — latent chunks (3D, 128-byte swizzle) and
+// RoPE halves; FP8 cache — code rows (uint8, 256-byte boxes, no swizzle) and
+// RoPE halves of the 640-byte rows.
+template <bool kF8>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap rope_map,
                   const DecodeArgs a) {
+  using L = Layout<kF8>;
+  constexpr int kStages = L::kStages, kStageBytes = L::kStageBytes, kThreads = L::kThreads;
+  constexpr int kPvWarp = L::kPvWarp, kSoftWarp0 = L::kSoftWarp0, kConvWarp0 = L::kConvWarp0;
+  constexpr int kOffKV = L::kOffKV, kOffX = L::kOffX, kOffOnes = L::kOffOnes;
+  constexpr int kAlignedBytes = L::kAlignedBytes, kSmemBytes = L::kSmemBytes;
+  constexpr int B_KV_FULL = L::B_KV_FULL, B_KV_EMPTY = L::B_KV_EMPTY, B_S_FULL0 = L::B_S_FULL0,
+                B_S_FULL1 = L::B_S_FULL1, B_S_FREE = L::B_S_FREE, B_P_FULL = L::B_P_FULL,
+                B_O_DONE0 = L::B_O_DONE0, B_O_DONE1 = L::B_O_DONE1, B_Q_READY = L::B_Q_READY,
+                B_O_FREE = L::B_O_FREE, B_X_FULL0 = L::B_X_FULL0, B_DRAIN = L::B_DRAIN, B_DRAIN_PV = L::B_DRAIN_PV,
+                B_F8_FULL = L::B_F8_FULL;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t bars = raw + kSmallBar;
@@ -184,8 +238,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     *abort_flag = 0;
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(BAR(B_KV_FULL + i), 1);
+      mbar_init(BAR(B_KV_FULL + i), kF8 ? kConvWarps : 1);  // FP8: one arrival per converter warp
       mbar_init(BAR(B_KV_EMPTY + i), 1);
+      if (kF8) mbar_init(BAR(B_F8_FULL + i), 1);
     }
     mbar_init(BAR(B_S_FULL0), 1);
     mbar_init(BAR(B_S_FULL1), 1);
@@ -245,7 +300,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   const int s_begin = seg_range[0];
   const int s_end = seg_range[1];
 
-  if (warp == 0) {
+  // Each role is a lambda so that the FP8 layout can give each warpgroup its
+  // register budget at the top of a branch that reaches only its own roles.
+  auto role_producer = [&]() {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       uint32_t g = 0;
@@ -275,19 +332,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             pid = 0;
           }
           const uint32_t dst = base + kOffKV + st * kStageBytes;
-          mbar_arrive_expect_tx(BAR(B_KV_FULL + st), (uint32_t)kStageBytes);
-          // latent chunks 4r..4r+3 in one 3D box, then the RoPE half
-          tma_load_3d(dst, &kv_map, 0, pid * kPage, (int)(4 * rank), BAR(B_KV_FULL + st));
-          tma_load_2d(dst + 4 * kChunkBytes, &rope_map, kDC + (int)rank * kRopeHalf, pid * kPage, BAR(B_KV_FULL + st));
+          if constexpr (kF8) {
+            // this CTA's 256 codes of each of the page's 64 rows, its RoPE
+            // half, and the page's 64 token scales
+            mbar_arrive_expect_tx(BAR(B_F8_FULL + st), (uint32_t)kF8Payload);
+            tma_load_2d(dst, &kv_map, (int)(256 * rank), pid * kPage, BAR(B_F8_FULL + st));
+            tma_load_2d(dst + kF8RopeOff, &rope_map, 256 + (int)rank * kRopeHalf, pid * kPage, BAR(B_F8_FULL + st));
+            bulk_load_g2s(dst + kF8ScaleOff, a.kv_scales + (size_t)pid * kPage, kPage * 4, BAR(B_F8_FULL + st));
+          } else {
+            mbar_arrive_expect_tx(BAR(B_KV_FULL + st), (uint32_t)kStageBytes);
+            // latent chunks 4r..4r+3 in one 3D box, then the RoPE half
+            tma_load_3d(dst, &kv_map, 0, pid * kPage, (int)(4 * rank), BAR(B_KV_FULL + st));
+            tma_load_2d(dst + 4 * kChunkBytes, &rope_map, kDC + (int)rank * kRopeHalf, pid * kPage,
+                        BAR(B_KV_FULL + st));
+          }
           ++g;
         }
       }
       // Loads still in flight must land before this CTA may exit.
       for (uint32_t k = (g > (uint32_t)kStages ? g - kStages : 0u); k < g; ++k)
-        wait_phase_drain(BAR(B_KV_FULL + k % kStages), (k / kStages) & 1u);
+        wait_phase_drain(BAR((kF8 ? B_F8_FULL : B_KV_FULL) + k % kStages), (k / kStages) & 1u);
     }
     __syncwarp();
-  } else if (warp == 1) {
+  };
+  auto role_qk = [&]() {
     // ---------------------------------------------------------------- QK^T issue
     // S_partial(t) = Q_r · K_r(t)^T as soon as page t has landed and the
     // softmax has read S(t-1).  P·V is issued by its own warp, so a long
@@ -304,6 +372,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       for (uint32_t tq = 0; cq.valid(); ++tq) {
         const uint32_t st = tq % kStages;
         if (!wait_phase<false, kIssueSuspend>(BAR(B_KV_FULL + st), (tq / kStages) & 1u, err, abort_flag)) break;
+        // FP8: the RoPE half came with the codes (already complete; waited for its TMA visibility)
+        if (kF8 && !wait_phase<false, kIssueSuspend>(BAR(B_F8_FULL + st), (tq / kStages) & 1u, err, abort_flag))
+          break;
         if (tq > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_S_FREE), (tq - 1) & 1u, err, abort_flag)) break;
         if (cq.first() &&
             !wait_phase<false, kIssueSuspend>(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u, err, abort_flag))
@@ -330,7 +401,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wait_phase_drain(BAR(B_DRAIN), 0);
     }
     __syncwarp();
-  } else if (warp == kPvWarp) {
+  };
+  auto role_pv = [&]() {
     // ---------------------------------------------------------------- P·V issue
     if (lane == 0) {
       TileCursor cp;
@@ -365,12 +437,90 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       wait_phase_drain(BAR(B_DRAIN_PV), 0);
     }
     __syncwarp();
-  } else {
+  };
+  auto role_convert = [&]() {
+    // ---------------------------------------------------------------- FP8 converters
+    // Tile t, stage t mod kStages.  Warp cw takes token rows cw, cw+4, ...;
+    // lane l the row's output chunk l (latent dims 8l..8l+7 of this CTA's
+    // half): 8 codes in, one 16-byte bf16 chunk out, written in the 128-byte
+    // swizzled layout the tensor core reads.  The bf16 rows overwrite the
+    // codes, so every converter thread reads all of its codes first and the
+    // four warps meet at a named barrier before the first store.
+    const int cw = warp - kConvWarp0;
+    uint32_t G = 0;
+    for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
+    const uint32_t ct = (uint32_t)lane >> 3, cc = (uint32_t)lane & 7u;
+    constexpr int kRows = kPage / kConvWarps;
+    constexpr int kBatch = 8;
+    for (uint32_t t = 0; t < G; ++t) {
+      const uint32_t st = t % kStages;
+      const bool w = wait_phase<false, true>(BAR(B_F8_FULL + st), (t / kStages) & 1u, err, abort_flag);
+      // every converter warp takes this decision alike: all of them pass the
+      // barrier below or none does
+      if (!__all_sync(0xffffffffu, w)) break;
+      const uint32_t stage = base + kOffKV + st * kStageBytes;
+      // All loads first (codes and row scales into registers), so that the
+      // store loop holds no shared-memory load behind a store and its rows'
+      // arithmetic overlaps.
+      uint2 code[kRows];
+      float scale[kRows];
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) {
+        const uint32_t r = (uint32_t)(kConvWarps * j + cw);
+        code[j] = ld_shared_v2(stage + r * 256u + (uint32_t)lane * 8u);
+        scale[j] = ld_shared_f32(stage + kF8ScaleOff + 4u * r);
+      }
+      // Rows whose scale leaves [2^-126, 2^15] take the general two-multiply
+      // path; the common case is one conversion and one multiply per pair,
+      // issued kBatch rows at a time so that one warp keeps many in flight.
+      bool fast = true;
+#pragma unroll
+      for (int j = 0; j < kRows; ++j) fast = fast && fp8_fast_scale(scale[j]);
+      named_bar_sync(kConvBarrier, kConvWarps * 32);
+      if (fast) {
+#pragma unroll
+        for (int j0 = 0; j0 < kRows; j0 += kBatch) {
+          uint32_t h[kBatch][4];
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            h[j][0] = e4m3x2_to_f16x2(code[j0 + j].x & 0xFFFFu);
+            h[j][1] = e4m3x2_to_f16x2(code[j0 + j].x >> 16);
+            h[j][2] = e4m3x2_to_f16x2(code[j0 + j].y & 0xFFFFu);
+            h[j][3] = e4m3x2_to_f16x2(code[j0 + j].y >> 16);
+          }
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            const uint32_t f = fp8_fast_factor(scale[j0 + j]);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) h[j][q] = mul_bf16x2(f16x2_to_bf16_pattern(h[j][q]), f);
+          }
+#pragma unroll
+          for (int j = 0; j < kBatch; ++j) {
+            const uint32_t r = (uint32_t)(kConvWarps * (j0 + j) + cw);
+            st_shared_v4(stage + ct * kChunkBytes + r * 128u + ((cc ^ (r & 7u)) << 4), h[j][0], h[j][1], h[j][2],
+                         h[j][3]);
+          }
+        }
+      } else {
+#pragma unroll 4
+        for (int j = 0; j < kRows; ++j) {
+          const uint32_t r = (uint32_t)(kConvWarps * j + cw);
+          const uint4 o = dequant8(code[j], fp8_row_scale(scale[j]));
+          st_shared_v4(stage + ct * kChunkBytes + r * 128u + ((cc ^ (r & 7u)) << 4), o.x, o.y, o.z, o.w);
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_KV_FULL + st));
+    }
+    __syncwarp();
+  };
+  auto role_softmax = [&]() {
     // ---------------------------------------------------------------- softmax + epilogue
-    // Warpgroup wg (warps 2-5, 6-9) takes the tiles g with g % 2 == wg, whole:
+    // Warpgroup wg (warps 2-5 and 6-9; FP8: 4-7 and 8-11) takes the tiles g with g % 2 == wg, whole:
     // thread = head row = TMEM lane, all 64 tokens.  The only hand-off between
     // the warpgroups is the row's reference max, passed from tile g-1 to g.
-    const int sw = warp - 2;                 // 0 .. kSWarps-1
+    const int sw = warp - kSoftWarp0;        // 0 .. kSWarps-1
     const int wg = sw >> 2;
     const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
     const int h = q4 * 32 + lane;            // head row = TMEM lane
@@ -647,6 +797,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       cf.next();
       cf.next();
     }
+  };
+  if constexpr (kF8) {
+    // 512 threads x 128 registers at launch: warpgroup 0 (producer, MMA
+    // issue, an idle warp) drops to 64, warpgroup 3 (converters, which hold
+    // a tile's codes in registers) to 96, the softmax warpgroups 1-2 rise
+    // to 176; 128*64 + 128*96 + 256*176 = 65536, the launch's total.
+    if (warp < 4) {
+      regs_dec<64>();
+      if (warp == 0) role_producer();
+      else if (warp == 1) role_qk();
+      else if (warp == kPvWarp) role_pv();
+    } else if (warp >= kConvWarp0) {
+      regs_dec<96>();
+      role_convert();
+    } else {
+      regs_inc<176>();
+      role_softmax();
+    }
+  } else {
+    if (warp == 0) role_producer();
+    else if (warp == 1) role_qk();
+    else if (warp == kPvWarp) role_pv();
+    else role_softmax();
   }
 
   tc_fence_before();
@@ -691,21 +864,22 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
 
 }  // namespace decode
 
-int decode_smem_bytes() { return decode::kSmemBytes; }
-int decode_threads() { return decode::kThreads; }
+int decode_smem_bytes() { return decode::Layout<false>::kSmemBytes; }
+int decode_threads() { return decode::Layout<false>::kThreads; }
 
-cudaError_t decode_prepare() {
-  return cudaFuncSetAttribute(decode::decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              decode::kSmemBytes);
+template <bool kF8>
+static cudaError_t decode_prepare() {
+  return cudaFuncSetAttribute(decode::decode_kernel<kF8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              decode::Layout<kF8>::kSmemBytes);
 }
 
 cudaError_t decode_max_clusters(int* out) {
-  cudaError_t e = decode_prepare();
+  cudaError_t e = decode_prepare<false>();
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * 1024, 1, 1);
-  cfg.blockDim = dim3(decode::kThreads, 1, 1);
-  cfg.dynamicSmemBytes = decode::kSmemBytes;
+  cfg.blockDim = dim3(decode::Layout<false>::kThreads, 1, 1);
+  cfg.dynamicSmemBytes = decode::Layout<false>::kSmemBytes;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -713,14 +887,19 @@ cudaError_t decode_max_clusters(int* out) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(out, (const void*)decode::decode_kernel, &cfg);
+  return cudaOccupancyMaxActiveClusters(out, (const void*)decode::decode_kernel<false>, &cfg);
 }
 
 cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& rope_map, const DecodeArgs& args,
-                          int num_clusters, cudaStream_t stream) {
-  cudaError_t e = decode_prepare();
+                          int num_clusters, bool fp8, cudaStream_t stream) {
+  cudaError_t e = fp8 ? decode_prepare<true>() : decode_prepare<false>();
   if (e != cudaSuccess) return e;
-  decode::decode_kernel<<<2 * num_clusters, decode::kThreads, decode::kSmemBytes, stream>>>(kv_map, rope_map, args);
+  if (fp8)
+    decode::decode_kernel<true><<<2 * num_clusters, decode::Layout<true>::kThreads, decode::Layout<true>::kSmemBytes,
+                                  stream>>>(kv_map, rope_map, args);
+  else
+    decode::decode_kernel<false><<<2 * num_clusters, decode::Layout<false>::kThreads,
+                                   decode::Layout<false>::kSmemBytes, stream>>>(kv_map, rope_map, args);
   return cudaGetLastError();
 }
 

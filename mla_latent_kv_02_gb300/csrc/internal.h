@@ -62,6 +62,7 @@ struct DecodeArgs {
   int32_t B;
   int32_t num_segments;
   int32_t num_partials;
+  const float* kv_scales;  // FP8 cache: fp32 [num_pages * 64] token scales (null for bf16)
 };
 
 struct CombineArgs {
@@ -78,10 +79,12 @@ struct CombineArgs {
 int decode_smem_bytes();
 int decode_threads();
 cudaError_t decode_max_clusters(int* out);
-// kv_map: 128-byte swizzled boxes of 64 columns x 64 tokens (latent chunks);
-// rope_map: 64-byte swizzled boxes of 32 columns x 64 tokens (RoPE halves).
+// bf16 cache: kv_map 128-byte swizzled boxes of 64 columns x 64 tokens x 4
+// chunks (latent), rope_map 64-byte swizzled boxes of 32 columns x 64 tokens.
+// FP8 cache (fp8 = true): kv_map uint8 boxes of 256 codes x 64 tokens (no
+// swizzle), rope_map as above over the 640-byte rows; args.kv_scales set.
 cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& rope_map, const DecodeArgs& args,
-                          int num_clusters, cudaStream_t stream);
+                          int num_clusters, bool fp8, cudaStream_t stream);
 cudaError_t launch_combine(const CombineArgs& args, int num_split_rows, cudaStream_t stream);
 
 cudaError_t launch_kv_append(const uint16_t* c_kv_new, const uint16_t* k_r_new, const int64_t* slots, int32_t n,
@@ -92,6 +95,12 @@ cudaError_t launch_kv_append_rope(const uint16_t* c_kv_new, const uint16_t* k_pe
                                   uint16_t* kv_cache, int64_t num_slots, int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_rope_q(const uint16_t* q_pe, const int32_t* positions, const float* table, int32_t max_pos,
                           uint16_t* q_r, int32_t T, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_kv_append_fp8(const uint16_t* c_kv_new, const uint16_t* k_r_new, const int64_t* slots, int32_t n,
+                                 uint8_t* rows, float* scales, int64_t num_slots, int32_t* dev_err,
+                                 cudaStream_t stream);
+cudaError_t launch_gather_fp8(const uint8_t* rows, const float* scales, int64_t num_pages,
+                              const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
+                              uint16_t* out, int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                           int32_t b, int32_t n_tokens, uint16_t* out, int32_t* dev_err, cudaStream_t stream);
 

@@ -69,11 +69,12 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 // first, strides in bytes for dims 1..rank-1.
 mla_status make_map(CUtensorMap* m, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
                     const uint32_t* box, const char* what,
-                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B) {
+                    CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B,
+                    CUtensorMapDataType dtype = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return fail(MLA_ERR_CUDA, "cuTensorMapEncodeTiled entry point unavailable");
   cuuint32_t estr[5] = {1, 1, 1, 1, 1};
-  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base),
+  CUresult r = fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(base),
                   reinterpret_cast<const cuuint64_t*>(dims), reinterpret_cast<const cuuint64_t*>(strides),
                   reinterpret_cast<const cuuint32_t*>(box), estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -497,6 +498,54 @@ mla_status mla_gather_paged(const void* kv_cache, int64_t num_pages, const int32
   return MLA_OK;
 }
 
+mla_status mla_kv_append_fp8(const void* c_kv_new, const void* k_r_new, const int64_t* slots, int32_t n,
+                             void* rows, float* scales, int64_t num_pages, int32_t* dev_err, void* stream) {
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (n == 0) return MLA_OK;
+  CHECK_PTR(c_kv_new);
+  CHECK_PTR(k_r_new);
+  CHECK_PTR(slots);
+  CHECK_PTR(rows);
+  CHECK_PTR(scales);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(c_kv_new);
+  CHECK_ALIGN16(k_r_new);
+  CHECK_ALIGN16(rows);
+  CHECK_ALIGN16(scales);
+  if (!aligned(slots, 8)) return fail(MLA_ERR_MISALIGNED, "slots is not 8-byte aligned");
+  if (!aligned(dev_err, 4)) return fail(MLA_ERR_MISALIGNED, "dev_err is not 4-byte aligned");
+  if (num_pages < 1) return fail(MLA_ERR_INVALID_ARG, "num_pages = %lld < 1", (long long)num_pages);
+  cudaError_t e = mla::launch_kv_append_fp8((const uint16_t*)c_kv_new, (const uint16_t*)k_r_new, slots, n,
+                                            (uint8_t*)rows, scales, num_pages * MLA_PAGE_SIZE, dev_err,
+                                            (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append_fp8 launch");
+  return MLA_OK;
+}
+
+mla_status mla_gather_paged_fp8(const void* rows, const float* scales, int64_t num_pages,
+                                const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
+                                void* out, int32_t* dev_err, void* stream) {
+  if (n_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "n_tokens = %d < 0", n_tokens);
+  if (n_tokens == 0) return MLA_OK;
+  CHECK_PTR(rows);
+  CHECK_PTR(scales);
+  CHECK_PTR(block_table);
+  CHECK_PTR(out);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(rows);
+  CHECK_ALIGN16(scales);
+  CHECK_ALIGN16(out);
+  if (!aligned(block_table, 4) || !aligned(dev_err, 4))
+    return fail(MLA_ERR_MISALIGNED, "block_table and dev_err must be 4-byte aligned");
+  if (num_pages < 1 || max_pages < 1 || b < 0) return fail(MLA_ERR_INVALID_ARG, "bad pool/table sizes");
+  if ((n_tokens + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE > max_pages)
+    return fail(MLA_ERR_INVALID_ARG, "n_tokens = %d needs more than max_pages = %d pages", n_tokens, max_pages);
+  cudaError_t e = mla::launch_gather_fp8((const uint8_t*)rows, scales, num_pages, block_table, max_pages, b,
+                                         n_tokens, (uint16_t*)out, dev_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gather_fp8 launch");
+  return MLA_OK;
+}
+
 static mla_status head_gemm(mla::HeadGemm kind, const void* a, const void* w, void* c, int32_t T, int32_t* dev_err,
                             void* stream) {
   if (T < 0) return fail(MLA_ERR_INVALID_ARG, "T = %d < 0", T);
@@ -588,10 +637,11 @@ mla_status mla_decode_plan(const int32_t* seq_lens_host, const int32_t* q_lens_h
   return MLA_OK;
 }
 
-mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_cache, int64_t num_pages,
-                            const int32_t* block_table, int32_t max_pages, const void* plan_dev,
-                            const mla_plan_info* info, float scale, void* workspace, size_t ws_bytes, void* o_lat,
-                            float* lse, int32_t* dev_err, void* stream) {
+static mla_status decode_common(const void* q_abs, const void* q_r, const void* kv_cache, const float* kv_scales,
+                                int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                const void* plan_dev, const mla_plan_info* info, float scale, void* workspace,
+                                size_t ws_bytes, void* o_lat, float* lse, int32_t* dev_err, void* stream,
+                                bool fp8) {
   CHECK_PTR(info);
   if (info->magic != MLA_PLAN_MAGIC) return fail(MLA_ERR_INVALID_ARG, "info is not a decode plan summary");
   if (info->T == 0 || info->num_clusters == 0) return MLA_OK;
@@ -607,6 +657,10 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
   CHECK_ALIGN16(kv_cache);
   CHECK_ALIGN16(plan_dev);
   CHECK_ALIGN16(o_lat);
+  if (fp8) {
+    CHECK_PTR(kv_scales);
+    CHECK_ALIGN16(kv_scales);
+  }
   if (!aligned(block_table, 4) || !aligned(dev_err, 4) || (lse && !aligned(lse, 4)))
     return fail(MLA_ERR_MISALIGNED, "block_table, dev_err and lse must be 4-byte aligned");
   if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and positive");
@@ -624,19 +678,35 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
   }
 
   CUtensorMap kv_map, rope_map;
-  // Latent part as a 3D view {64 elements, token, 64-element chunk}: one box
-  // of 4 chunks x 64 tokens lands as 4 consecutive 128-byte-swizzled 8 KB
-  // tiles, one TMA instruction per page for a CTA's latent half.
-  const uint64_t ldims[3] = {64, (uint64_t)num_pages * MLA_PAGE_SIZE, MLA_LATENT_DIM / 64};
-  const uint64_t lstr[2] = {(uint64_t)kRowBytes, 128};
-  const uint32_t lbox[3] = {64, 64, 4};
-  mla_status s = make_map(&kv_map, kv_cache, 3, ldims, lstr, lbox, "kv_cache latent chunks");
-  if (s != MLA_OK) return s;
-  const uint64_t dims[2] = {MLA_TOKEN_ELEMS, (uint64_t)num_pages * MLA_PAGE_SIZE};
-  const uint64_t str[1] = {(uint64_t)kRowBytes};
-  const uint32_t rope_box[2] = {32, 64};
-  s = make_map(&rope_map, kv_cache, 2, dims, str, rope_box, "kv_cache RoPE halves", CU_TENSOR_MAP_SWIZZLE_64B);
-  if (s != MLA_OK) return s;
+  mla_status s;
+  if (fp8) {
+    // Codes: a CTA's 256 of each token row, 64 rows per box (no swizzle: the
+    // converters read them); RoPE halves as bf16 columns 256.. of the rows.
+    const uint64_t cdims[2] = {MLA_FP8_ROW_BYTES, (uint64_t)num_pages * MLA_PAGE_SIZE};
+    const uint64_t cstr[1] = {MLA_FP8_ROW_BYTES};
+    const uint32_t cbox[2] = {256, 64};
+    s = make_map(&kv_map, kv_cache, 2, cdims, cstr, cbox, "fp8 codes", CU_TENSOR_MAP_SWIZZLE_NONE,
+                 CU_TENSOR_MAP_DATA_TYPE_UINT8);
+    if (s != MLA_OK) return s;
+    const uint64_t rdims[2] = {MLA_FP8_ROW_BYTES / 2, (uint64_t)num_pages * MLA_PAGE_SIZE};
+    const uint32_t rope_box[2] = {32, 64};
+    s = make_map(&rope_map, kv_cache, 2, rdims, cstr, rope_box, "fp8 RoPE halves", CU_TENSOR_MAP_SWIZZLE_64B);
+    if (s != MLA_OK) return s;
+  } else {
+    // Latent part as a 3D view {64 elements, token, 64-element chunk}: one box
+    // of 4 chunks x 64 tokens lands as 4 consecutive 128-byte-swizzled 8 KB
+    // tiles, one TMA instruction per page for a CTA's latent half.
+    const uint64_t ldims[3] = {64, (uint64_t)num_pages * MLA_PAGE_SIZE, MLA_LATENT_DIM / 64};
+    const uint64_t lstr[2] = {(uint64_t)kRowBytes, 128};
+    const uint32_t lbox[3] = {64, 64, 4};
+    s = make_map(&kv_map, kv_cache, 3, ldims, lstr, lbox, "kv_cache latent chunks");
+    if (s != MLA_OK) return s;
+    const uint64_t dims[2] = {MLA_TOKEN_ELEMS, (uint64_t)num_pages * MLA_PAGE_SIZE};
+    const uint64_t str[1] = {(uint64_t)kRowBytes};
+    const uint32_t rope_box[2] = {32, 64};
+    s = make_map(&rope_map, kv_cache, 2, dims, str, rope_box, "kv_cache RoPE halves", CU_TENSOR_MAP_SWIZZLE_64B);
+    if (s != MLA_OK) return s;
+  }
 
   const mla::PlanLayout L = mla::plan_layout(info->num_clusters, info->num_segments, info->num_split_rows);
   const int32_t* plan = (const int32_t*)plan_dev;
@@ -661,7 +731,8 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
   a.B = info->B;
   a.num_segments = info->num_segments;
   a.num_partials = info->num_partials;
-  cudaError_t e = mla::launch_decode(kv_map, rope_map, a, info->num_clusters, (cudaStream_t)stream);
+  a.kv_scales = fp8 ? kv_scales : nullptr;
+  cudaError_t e = mla::launch_decode(kv_map, rope_map, a, info->num_clusters, fp8, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (info->num_split_rows > 0) {
     mla::CombineArgs c = {};
@@ -677,6 +748,22 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
     if (e != cudaSuccess) return cuda_fail(e, "combine launch");
   }
   return MLA_OK;
+}
+
+mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_cache, int64_t num_pages,
+                            const int32_t* block_table, int32_t max_pages, const void* plan_dev,
+                            const mla_plan_info* info, float scale, void* workspace, size_t ws_bytes, void* o_lat,
+                            float* lse, int32_t* dev_err, void* stream) {
+  return decode_common(q_abs, q_r, kv_cache, nullptr, num_pages, block_table, max_pages, plan_dev, info, scale,
+                       workspace, ws_bytes, o_lat, lse, dev_err, stream, false);
+}
+
+mla_status mla_decode_paged_fp8(const void* q_abs, const void* q_r, const void* rows, const float* scales,
+                                int64_t num_pages, const int32_t* block_table, int32_t max_pages,
+                                const void* plan_dev, const mla_plan_info* info, float scale, void* workspace,
+                                size_t ws_bytes, void* o_lat, float* lse, int32_t* dev_err, void* stream) {
+  return decode_common(q_abs, q_r, rows, scales, num_pages, block_table, max_pages, plan_dev, info, scale,
+                       workspace, ws_bytes, o_lat, lse, dev_err, stream, true);
 }
 
 mla_status mla_check(void* stream, const int32_t* dev_err, int32_t* word_out) {

@@ -35,6 +35,13 @@ def oracle_cache(case: wl.Case) -> np.ndarray:
     return oracle.append(empty, case.c_kv, case.k_r, slots)
 
 
+def oracle_cache_fp8(case: wl.Case):
+    """The oracle's FP8 cache of a case: (rows uint8, scales float64)."""
+    seq, pos = case.positions()
+    slots = oracle.slot_mapping(case.block_table, seq, pos)
+    return oracle.fp8_cache.append(*oracle.fp8_cache.empty_cache(case.num_pages), case.c_kv, case.k_r, slots)
+
+
 def to_bf16(x, device):
     import torch
     return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device=device, dtype=torch.bfloat16)
@@ -52,15 +59,20 @@ class DeviceCase:
     tokens in a second call (step A1 of the path).
     """
 
-    def __init__(self, case: wl.Case, device="cuda:0", with_weights=True):
+    def __init__(self, case: wl.Case, device="cuda:0", with_weights=True, fp8=False):
         import torch
         from mla_latent_kv_02_gb300 import api
         self.case = case
         self.device = torch.device(device)
         dev = self.device
         self.dev_err = torch.zeros(1, dtype=torch.int32, device=dev)
-        self.kv_cache = torch.empty((case.num_pages, wl.PAGE, wl.D_QK), dtype=torch.bfloat16, device=dev)
-        api.mla_cache_init(self.kv_cache)
+        self.fp8 = fp8
+        if fp8:
+            self.rows = torch.zeros((case.num_pages, wl.PAGE, 640), dtype=torch.uint8, device=dev)
+            self.scales = torch.ones((case.num_pages, wl.PAGE), dtype=torch.float32, device=dev)
+        else:
+            self.kv_cache = torch.empty((case.num_pages, wl.PAGE, wl.D_QK), dtype=torch.bfloat16, device=dev)
+            api.mla_cache_init(self.kv_cache)
         self.block_table = torch.from_numpy(case.block_table).to(dev)
         seq, pos = case.positions()
         slots = api.mla_slot_mapping(case.block_table, seq, pos)
@@ -72,8 +84,12 @@ class DeviceCase:
         for idx in (old_idx, new_idx):
             if idx.size == 0:
                 continue
-            api.mla_kv_append(to_bf16(case.c_kv[idx], dev), to_bf16(case.k_r[idx], dev),
-                              torch.from_numpy(slots[idx]).to(dev), self.kv_cache, self.dev_err)
+            if fp8:
+                api.mla_kv_append_fp8(to_bf16(case.c_kv[idx], dev), to_bf16(case.k_r[idx], dev),
+                                      torch.from_numpy(slots[idx]).to(dev), self.rows, self.scales, self.dev_err)
+            else:
+                api.mla_kv_append(to_bf16(case.c_kv[idx], dev), to_bf16(case.k_r[idx], dev),
+                                  torch.from_numpy(slots[idx]).to(dev), self.kv_cache, self.dev_err)
         self.q_c = to_bf16(case.q_c, dev)
         self.q_r = to_bf16(case.q_r, dev)
         self.q_abs = to_bf16(case.q_abs, dev) if case.q_abs is not None else None
@@ -91,7 +107,11 @@ class DeviceCase:
         T = case.T
         o = torch.full((T, wl.H, wl.D_C), float("nan"), dtype=torch.bfloat16, device=self.device)
         lse = torch.full((T, wl.H), float("nan"), dtype=torch.float32, device=self.device)
-        api.mla_decode_paged(q_abs, self.q_r, self.kv_cache, self.block_table, plan, o, self.dev_err, lse=lse)
+        if self.fp8:
+            api.mla_decode_paged_fp8(q_abs, self.q_r, self.rows, self.scales, self.block_table, plan, o,
+                                     self.dev_err, lse=lse)
+        else:
+            api.mla_decode_paged(q_abs, self.q_r, self.kv_cache, self.block_table, plan, o, self.dev_err, lse=lse)
         word = api.mla_check(self.dev_err)
         assert word == 0
         return o, lse, plan

@@ -66,8 +66,16 @@ class Barrier:
         return passed
 
 
-def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2):
+def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv_no_barrier=False,
+              conv_skips_f8_full=False):
+    """fp8: the FP8 layout — the producer's TMA fills stage t mod STAGES with
+    codes, the converter warps read all of their codes, meet at a barrier and
+    write the bf16 rows over them, and QK^T waits for all converter warps.
+    Planted mistakes: converters without the barrier (a warp overwrites codes
+    another warp has not read yet) and converters that do not wait for the
+    codes to land."""
     rnd = random.Random(seed)
+    n_stages = STAGES
     tiles = []
     for si, n in enumerate(segs):
         for i in range(n):
@@ -78,7 +86,12 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2):
     ctas = []
     for _ in range(2):
         ctas.append(dict(
-            kv_full=[Barrier(1) for _ in range(STAGES)], kv_empty=[Barrier(1) for _ in range(STAGES)],
+            kv_full=[Barrier(WARPS if fp8 else 1) for _ in range(n_stages)],
+            kv_empty=[Barrier(1) for _ in range(n_stages)],
+            f8_full=[Barrier(1) for _ in range(n_stages)],
+            stage=[None] * n_stages,        # (tile, "codes" | "bf16") held by a stage
+            codes_read=[set() for _ in range(n_stages)],   # converter warps that have read this tile's codes
+            conv_bar=[0] * n_stages,        # converter warps arrived at the named barrier, per tile
             s_full=[Barrier(1), Barrier(1)], s_free=Barrier(WG_THREADS), p_full=Barrier(WG_THREADS),
             o_done=[Barrier(1), Barrier(1)], q_ready=Barrier(WG_THREADS), o_free=Barrier(WG_THREADS),
             x_full=[Barrier(1) for _ in range(XBUFS)],
@@ -100,13 +113,41 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2):
             if t >= STAGES:
                 while not c["kv_empty"][t % STAGES].test(t // STAGES - 1):
                     yield
-            events.append(("kv", ci, t))
+            events.append(("f8" if fp8 else "kv", ci, t))
+
+    def converter(ci, w):
+        c = ctas[ci]
+        for t in range(G):
+            st = t % n_stages
+            if not conv_skips_f8_full:
+                while not c["f8_full"][st].test(t // n_stages):
+                    yield
+            if c["stage"][st] != (t, "codes"):
+                raise ProtocolError(f"converter {w} reads tile {t}'s codes from a stage holding {c['stage'][st]}")
+            c["codes_read"][st].add(w)
+            yield
+            if not conv_no_barrier:
+                c["conv_bar"][st] += 1
+                while c["conv_bar"][st] < WARPS * (t // n_stages + 1):
+                    yield
+            if c["codes_read"][st] != set(range(WARPS)):
+                raise ProtocolError(f"converter {w} overwrites tile {t}'s codes before every warp read them")
+            yield
+            c["kv_full"][st].arrive()
+            if c["kv_full"][st].pending == WARPS:    # the last converter warp of this tile
+                c["stage"][st] = (t, "bf16")
+                c["codes_read"][st] = set()
 
     def qk(ci):
         c = ctas[ci]
         for t in range(G):
-            while not c["kv_full"][t % STAGES].test(t // STAGES):
+            while not c["kv_full"][t % n_stages].test(t // n_stages):
                 yield
+            if fp8:
+                while not c["f8_full"][t % n_stages].test(t // n_stages):
+                    yield
+                if c["stage"][t % n_stages] != (t, "bf16"):
+                    raise ProtocolError(f"QK^T of tile {t} reads a stage holding {c['stage'][t % n_stages]}")
             if t > 0:
                 while not c["s_free"].test(t - 1):
                     yield
@@ -125,6 +166,8 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2):
             if first:
                 while not c["o_free"].test(seg):
                     yield
+            if fp8 and c["stage"][t % n_stages] != (t, "bf16"):
+                raise ProtocolError(f"P·V of tile {t} reads a stage holding {c['stage'][t % n_stages]}")
             events.append(("o", ci, t))
 
     def softmax_warp(ci, wg, w):
@@ -191,6 +234,9 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2):
         roles[("prod", ci)] = producer(ci)
         roles[("qk", ci)] = qk(ci)
         roles[("pv", ci)] = pv(ci)
+        if fp8:
+            for w in range(WARPS):
+                roles[("conv", ci, w)] = converter(ci, w)
         for wg in range(2):
             for w in range(WARPS):
                 roles[("sm", ci, wg, w)] = softmax_warp(ci, wg, w)
@@ -202,11 +248,20 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2):
             c = ctas[ci]
             if kind == "kv":
                 c["kv_full"][t % STAGES].arrive()
+            elif kind == "f8":
+                st = t % n_stages
+                held = c["stage"][st]
+                if held is not None and held != (t - n_stages, "free"):
+                    raise ProtocolError(f"tile {t}'s codes land over a stage holding {held}")
+                c["stage"][st] = (t, "codes")
+                c["f8_full"][st].arrive()
             elif kind == "s":
                 bar, _ = s_full_bar(c, t)
                 bar.arrive()
             elif kind == "o":
-                c["kv_empty"][t % STAGES].arrive()
+                if fp8:
+                    c["stage"][t % n_stages] = (t, "free")
+                c["kv_empty"][t % n_stages].arrive()
                 bar, _ = o_done_bar(c, t)
                 bar.arrive()
             else:  # a row block's copy lands in the peer's buffer t mod XBUFS
@@ -257,6 +312,24 @@ def test_planted_protocol_mistakes_are_caught(mistake):
     for i, segs in enumerate(_layouts(60, 12)):
         try:
             run_model(segs + [1, 1, 3], seed=i, **mistake)
+        except ProtocolError:
+            caught += 1
+    assert caught > 0, f"the model did not catch {mistake}"
+
+
+def test_fp8_protocol_holds_on_random_interleavings():
+    for i, segs in enumerate(_layouts(120, 21)):
+        run_model(segs, seed=i, fp8=True)
+    for seed in range(60):
+        run_model([1, 1, 1, 1, 2, 2, 3, 3, 11], seed, fp8=True)
+
+
+@pytest.mark.parametrize("mistake", [dict(conv_no_barrier=True), dict(conv_skips_f8_full=True)])
+def test_planted_fp8_protocol_mistakes_are_caught(mistake):
+    caught = 0
+    for i, segs in enumerate(_layouts(60, 22)):
+        try:
+            run_model(segs + [1, 1, 3], seed=i, fp8=True, **mistake)
         except ProtocolError:
             caught += 1
     assert caught > 0, f"the model did not catch {mistake}"
