@@ -502,7 +502,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
           }
         }
       } else {
-#pragma unroll 4
+        // fully unrolled: a dynamically indexed code[] or scale[] would live in local memory
+#pragma unroll
         for (int j = 0; j < kRows; ++j) {
           const uint32_t r = (uint32_t)(kConvWarps * j + cw);
           const uint4 o = dequant8(code[j], fp8_row_scale(scale[j]));
