@@ -186,7 +186,7 @@ def cpu_baseline(case, budget_s: float, max_rows: int = 128):
 
 
 # ------------------------------------------------------------------ GPU arm
-def _time_launches(torch, stream, fn, reps=5, warmup=3):
+def _time_launches(torch, stream, fn, reps=5, warmup=3, per_rep=1):
     """Average device time (us) of one fn() launch: `reps` launches back to
     back between two CUDA events on `stream`, queued behind a short device
     sleep so that host-side call overhead leaves no gaps between them."""
@@ -194,7 +194,7 @@ def _time_launches(torch, stream, fn, reps=5, warmup=3):
         fn(i)
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
-    torch.cuda._sleep(2_000_000 + 60_000 * reps)   # ~30 us of queue time per launch at 2 GHz
+    torch.cuda._sleep(2_000_000 + 60_000 * reps * per_rep)   # ~30 us of queue time per launch at 2 GHz
     a.record(stream)
     for i in range(reps):
         fn(i)
@@ -279,6 +279,27 @@ def measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos_old
                                        frac=round(max(t_f, t_b) / (us * 1e-6), 4),
                                        peak_source=peaks["source"] + " (burst)")
         del rows, scales
+        # NVFP4 cache (E2M1 codes, E4M3 block scales, fp32 tensor scale):
+        # quantising fill of the whole context, then the dequantising gather
+        # of every sequence (B launches queued back to back), 416 B read and
+        # 1152 B written per token.
+        st_nv = 2.0 ** -8
+        rows4 = torch.zeros((case.num_pages, 64, 416), dtype=torch.uint8, device=dev)
+        us = _time_launches(torch, stream, lambda i: api.mla_kv_append_nvfp4(c_old, k_old, slots_old, rows4, st_nv,
+                                                                               dev_err))
+        entry("kv_append_nvfp4_bulk", us, n * (1152 + 8 + 416), tokens=n)
+        gl = [int(x) for x in case.seq_lens]
+        outs = [torch.empty((m, 576), dtype=torch.bfloat16, device=dev) for m in gl]
+
+        def gather_all(i):
+            for b2, m in enumerate(gl):
+                api.mla_gather_paged_nvfp4(rows4, st_nv, bt, b2, m, outs[b2], dev_err)
+
+        us = _time_launches(torch, stream, gather_all, reps=3, warmup=2, per_rep=len(gl))
+        tot = sum(gl)
+        entry("gather_nvfp4_all_sequences", us, tot * (416 + 1152) + sum((m + 63) // 64 * 4 for m in gl),
+              tokens=tot, launches=len(gl))
+        del rows4, outs
     if api.mla_check(dev_err) != 0:
         raise RuntimeError("device error word set while timing the cache-fill, RoPE and FP8 kernels")
     # put the unrotated keys back (the cache holds them for the step above)

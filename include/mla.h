@@ -387,6 +387,34 @@ mla_status mla_decode_paged_fp8(const void* q_abs, const void* q_r, const void* 
                                 const void* plan_dev, const mla_plan_info* info, float scale, void* workspace,
                                 size_t ws_bytes, void* o_lat, float* lse, int32_t* dev_err, void* stream);
 
+/* ---------------------------------------------------------------------------
+ * NVFP4 latent cache ([P1] opening section and §5: the latent is gathered in
+ * NVFP4 with 16-byte vector loads, which fault on a base that is not 16-byte
+ * aligned; here the host rejects such bases with MLA_ERR_MISALIGNED before
+ * any launch).  NVFP4 as NVIDIA defines it: E2M1 elements (magnitudes 0, 0.5,
+ * 1, 1.5, 2, 3, 4, 6), one E4M3 scale per block of 16 elements, one fp32
+ * tensor scale s_t (here a caller constant, finite and > 0).
+ *   block scale s_b = E4M3(fp32(amax_block / fp32(6 * s_t))), nearest even,
+ *                     saturating at 448;
+ *   code            = E2M1(fp32(x / fp32(s_b * s_t))), nearest even,
+ *                     saturating at 6 (all zero when s_b * s_t is zero);
+ *   value           = bf16(fp32(fp32(e2m1 * s_b) * s_t)).
+ * Row layout, rows uint8 [num_pages][64][MLA_NVFP4_ROW_BYTES], 16-byte
+ * aligned: bytes 0..255 the codes (element 2i in the low nibble of byte i),
+ * 256..287 the 32 block scales, 288..415 the 64 bf16 RoPE values.
+ * ------------------------------------------------------------------------- */
+#define MLA_NVFP4_ROW_BYTES 416
+
+/* Quantise and store rows[slots[i]] for i < n (as mla_kv_append_fp8). */
+mla_status mla_kv_append_nvfp4(const void* c_kv_new, const void* k_r_new, const int64_t* slots, int32_t n,
+                               float tensor_scale, void* rows, int64_t num_pages, int32_t* dev_err,
+                               void* stream);
+
+/* Dequantising gather into out bf16 [n_tokens, 576] (errors as mla_gather_paged). */
+mla_status mla_gather_paged_nvfp4(const void* rows, float tensor_scale, int64_t num_pages,
+                                  const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
+                                  void* out, int32_t* dev_err, void* stream);
+
 /*
  * Synchronise `stream`, read the device error word into *word_out (may be
  * NULL) and map it: 0 -> MLA_OK, MLA_DEVERR_TIMEOUT set -> MLA_ERR_TIMEOUT,

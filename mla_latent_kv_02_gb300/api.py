@@ -163,6 +163,34 @@ def mla_gather_paged_fp8(rows, scales, block_table, b: int, n_tokens: int, out, 
                                       _stream(stream)))
 
 
+NVFP4_ROW_BYTES = 416
+
+
+def mla_kv_append_nvfp4(c_kv_new, k_r_new, slots, rows, tensor_scale: float, dev_err, stream=None) -> None:
+    """Quantise new tokens into the NVFP4 cache: rows uint8 [pages, 64, 416]."""
+    n = c_kv_new.shape[0]
+    _need(c_kv_new, "c_kv_new", torch.bfloat16, (n, D_C))
+    _need(k_r_new, "k_r_new", torch.bfloat16, (n, D_R))
+    _need(slots, "slots", torch.int64, (n,))
+    _need(rows, "rows", torch.uint8, (rows.shape[0], PAGE, NVFP4_ROW_BYTES))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_kv_append_nvfp4(_ptr(c_kv_new), _ptr(k_r_new), _ptr(slots), int(n), float(tensor_scale),
+                                     _ptr(rows), rows.shape[0], _ptr(dev_err), _stream(stream)))
+
+
+def mla_gather_paged_nvfp4(rows, tensor_scale: float, block_table, b: int, n_tokens: int, out, dev_err,
+                           stream=None) -> None:
+    _need(rows, "rows", torch.uint8)
+    if rows.dim() != 3 or tuple(rows.shape[1:]) != (PAGE, NVFP4_ROW_BYTES):
+        raise ValueError(f"rows has shape {tuple(rows.shape)}, expected (pages, {PAGE}, {NVFP4_ROW_BYTES})")
+    _need(block_table, "block_table", torch.int32)
+    _need(out, "out", torch.bfloat16, (n_tokens, D_QK))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_gather_paged_nvfp4(_ptr(rows), float(tensor_scale), rows.shape[0], _ptr(block_table),
+                                        block_table.shape[1], int(b), int(n_tokens), _ptr(out), _ptr(dev_err),
+                                        _stream(stream)))
+
+
 def mla_rope_table(max_pos: int, table, base: float = 10000.0, stream=None) -> None:
     _need(table, "table", torch.float32, (max_pos, D_R // 2, 2))
     _check(lib().mla_rope_table(int(max_pos), float(base), _ptr(table), _stream(stream)))

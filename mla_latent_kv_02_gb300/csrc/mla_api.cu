@@ -546,6 +546,55 @@ mla_status mla_gather_paged_fp8(const void* rows, const float* scales, int64_t n
   return MLA_OK;
 }
 
+mla_status mla_kv_append_nvfp4(const void* c_kv_new, const void* k_r_new, const int64_t* slots, int32_t n,
+                               float tensor_scale, void* rows, int64_t num_pages, int32_t* dev_err,
+                               void* stream) {
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (n == 0) return MLA_OK;
+  if (!(tensor_scale > 0.f) || !std::isfinite(tensor_scale))
+    return fail(MLA_ERR_INVALID_ARG, "tensor_scale must be finite and > 0");
+  CHECK_PTR(c_kv_new);
+  CHECK_PTR(k_r_new);
+  CHECK_PTR(slots);
+  CHECK_PTR(rows);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(c_kv_new);
+  CHECK_ALIGN16(k_r_new);
+  CHECK_ALIGN16(rows);
+  if (!aligned(slots, 8)) return fail(MLA_ERR_MISALIGNED, "slots is not 8-byte aligned");
+  if (!aligned(dev_err, 4)) return fail(MLA_ERR_MISALIGNED, "dev_err is not 4-byte aligned");
+  if (num_pages < 1) return fail(MLA_ERR_INVALID_ARG, "num_pages = %lld < 1", (long long)num_pages);
+  cudaError_t e = mla::launch_kv_append_nvfp4((const uint16_t*)c_kv_new, (const uint16_t*)k_r_new, slots, n,
+                                              tensor_scale, (uint8_t*)rows, num_pages * MLA_PAGE_SIZE, dev_err,
+                                              (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "kv_append_nvfp4 launch");
+  return MLA_OK;
+}
+
+mla_status mla_gather_paged_nvfp4(const void* rows, float tensor_scale, int64_t num_pages,
+                                  const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
+                                  void* out, int32_t* dev_err, void* stream) {
+  if (n_tokens < 0) return fail(MLA_ERR_INVALID_ARG, "n_tokens = %d < 0", n_tokens);
+  if (n_tokens == 0) return MLA_OK;
+  if (!(tensor_scale > 0.f) || !std::isfinite(tensor_scale))
+    return fail(MLA_ERR_INVALID_ARG, "tensor_scale must be finite and > 0");
+  CHECK_PTR(rows);
+  CHECK_PTR(block_table);
+  CHECK_PTR(out);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(rows);
+  CHECK_ALIGN16(out);
+  if (!aligned(block_table, 4) || !aligned(dev_err, 4))
+    return fail(MLA_ERR_MISALIGNED, "block_table and dev_err must be 4-byte aligned");
+  if (num_pages < 1 || max_pages < 1 || b < 0) return fail(MLA_ERR_INVALID_ARG, "bad pool/table sizes");
+  if ((n_tokens + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE > max_pages)
+    return fail(MLA_ERR_INVALID_ARG, "n_tokens = %d needs more than max_pages = %d pages", n_tokens, max_pages);
+  cudaError_t e = mla::launch_gather_nvfp4((const uint8_t*)rows, tensor_scale, num_pages, block_table, max_pages, b,
+                                           n_tokens, (uint16_t*)out, dev_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gather_nvfp4 launch");
+  return MLA_OK;
+}
+
 static mla_status head_gemm(mla::HeadGemm kind, const void* a, const void* w, void* c, int32_t T, int32_t* dev_err,
                             void* stream) {
   if (T < 0) return fail(MLA_ERR_INVALID_ARG, "T = %d < 0", T);

@@ -262,3 +262,20 @@ def test_rope_calls_validate_before_any_launch(api):
     assert lib.mla_rope_q(ok, ok, ok, 0, P(0x90000), 1, err, None) == 1
     assert lib.mla_rope_q(ok, ok, ok, 64, P(0x10000 + 16384 - 16), 1, err, None) == 1   # overlaps by 16 B
     assert "overlap" in lib.mla_last_error().decode()
+
+
+def test_nvfp4_calls_validate_before_any_launch(api):
+    lib = _lib.lib()
+    P = C.c_void_p
+    ok, odd, err = P(0x10000), P(0x10008), P(0x20000)
+    f = C.c_float
+    assert lib.mla_kv_append_nvfp4(None, None, None, 0, f(0.01), None, 0, None, None) == 0
+    assert lib.mla_kv_append_nvfp4(ok, ok, ok, -1, f(0.01), ok, 4, err, None) == 1
+    assert lib.mla_kv_append_nvfp4(ok, ok, ok, 1, f(0.0), ok, 4, err, None) == 1
+    assert lib.mla_kv_append_nvfp4(ok, ok, ok, 1, f(float("nan")), ok, 4, err, None) == 1
+    assert lib.mla_kv_append_nvfp4(ok, ok, ok, 1, f(0.01), odd, 4, err, None) == 2
+    assert lib.mla_gather_paged_nvfp4(odd, f(0.01), 4, ok, 2, 0, 10, ok, err, None) == 2
+    assert lib.mla_gather_paged_nvfp4(ok, f(0.01), 4, ok, 2, 0, 10, odd, err, None) == 2
+    assert lib.mla_gather_paged_nvfp4(ok, f(0.01), 4, ok, 1, 0, 65, ok, err, None) == 1
+    assert lib.mla_gather_paged_nvfp4(ok, f(-2.0), 4, ok, 2, 0, 10, ok, err, None) == 1
+    assert lib.mla_gather_paged_nvfp4(None, f(0.01), 4, ok, 2, 0, 0, None, None, None) == 0
