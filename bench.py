@@ -307,6 +307,71 @@ def measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos_old
     return out
 
 
+def measure_decompress(api, torch, dev, stream, peaks):
+    """The decompress branch on its own workload (B4 x 16384 cached + a
+    512-token chunk, q_len >= the 256-token threshold): per-kernel times of
+    one sequence (gather, K/V expansion, attention), the whole branch for the
+    batch, and steps A2-A5 of the absorbed path on the same inputs."""
+    case = wl.workload(4, seed=0)
+
+    def bf(x):
+        return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device=dev, dtype=torch.bfloat16)
+
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    kv = torch.empty((case.num_pages, 64, 576), dtype=torch.bfloat16, device=dev)
+    seq, pos = case.positions()
+    api.mla_kv_append(bf(case.c_kv), bf(case.k_r), torch.from_numpy(api.mla_slot_mapping(case.block_table, seq, pos)).to(dev),
+                      kv, err)
+    bt = torch.from_numpy(case.block_table).to(dev)
+    q_c, q_r, w_uk, w_uv = bf(case.q_c), bf(case.q_r), bf(case.w_uk), bf(case.w_uv)
+    T, N, M = case.T, int(case.seq_lens[0]), int(case.q_lens[0])
+    ws = torch.empty(api.mla_prefill_workspace_size(N), dtype=torch.uint8, device=dev)
+    rows = ws[:N * 1152].view(torch.bfloat16).view(N, 576)
+    k_c = ws[N * 1152:N * 1152 + N * 32768].view(torch.bfloat16).view(128, N, 128)
+    v_c = ws[N * 1152 + N * 32768:N * 1152 + 2 * N * 32768].view(torch.bfloat16).view(128, N, 128)
+    out = torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev)
+    g_us = _time_launches(torch, stream, lambda i: api.mla_gather_paged(kv, bt, 0, N, rows, err))
+    e_us = _time_launches(torch, stream, lambda i: api.mla_expand_kv(rows, w_uk, w_uv, k_c, v_c, err))
+    a_us = _time_launches(torch, stream, lambda i: api.mla_prefill_attention(q_c[:M], q_r[:M], rows, k_c, v_c, out[:M],
+                                                                               err))
+
+    def branch(i):
+        for b in range(case.B):
+            r0 = int(case.q_start[b])
+            api.mla_prefill_decompress(q_c[r0:r0 + M], q_r[r0:r0 + M], kv, bt, b, N, w_uk, w_uv, ws, out[r0:r0 + M],
+                                       err)
+
+    d_us = _time_launches(torch, stream, branch, reps=3, warmup=2, per_rep=3 * case.B)
+    q_abs = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
+    o_lat = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
+    out2 = torch.empty_like(out)
+    plan = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev)
+
+    def absorbed(i):
+        api.mla_absorb_q(q_c, w_uk, q_abs, err)
+        api.mla_decode_paged(q_abs, q_r, kv, bt, plan, o_lat, err, scale=SCALE)
+        api.mla_up_v(o_lat, w_uv, out2, err)
+
+    b_us = _time_launches(torch, stream, absorbed, reps=3, warmup=2, per_rep=4)
+    if api.mla_check(err) != 0:
+        raise RuntimeError("device error word set while timing the decompress branch")
+    exp_fl = N * 128 * 2 * 512 * 256
+    vis = M * (N - M) + M * (M + 1) // 2
+    att_fl = vis * 128 * 2 * 320
+    pk = peaks["bf16_tflops"]
+    return {
+        "workload": case.name, "threshold": api.mla_prefill_threshold(),
+        "gather_us": round(g_us, 2),
+        "expand_us": round(e_us, 1), "expand_tflops": round(exp_fl / e_us / 1e6, 1),
+        "expand_frac": round(exp_fl / e_us / 1e6 / pk, 4),
+        "attention_us": round(a_us, 1), "attention_tflops": round(att_fl / a_us / 1e6, 1),
+        "attention_frac": round(att_fl / a_us / 1e6 / pk, 4),
+        "branch_us_batch": round(d_us, 1), "absorbed_a2_a5_us_batch": round(b_us, 1),
+        "branch_tflops": round(case.B * (exp_fl + att_fl) / d_us / 1e6, 1),
+        "peak_tflops": pk, "peak_source": peaks["source"] + " (burst)",
+    }
+
+
 def run_mla(args):
     import torch
     from mla_latent_kv_02_gb300 import api
@@ -480,6 +545,8 @@ def run_mla(args):
         "clocks": clk,
         "rows": rows,
     }
+    if not args.no_decompress:
+        line["decompress_branch"] = measure_decompress(api, torch, dev, stream, peaks)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(case, args.cpu_budget)
         line["cpu_baseline"].pop("seconds", None)
@@ -538,6 +605,7 @@ def main(argv=None):
     ap.add_argument("--impl", default="mla", choices=["mla", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decompress", action="store_true", help="skip the decompress-branch measurement")
     ap.add_argument("--ref-rows", type=int, default=2, help="query rows per reference-arm step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "mla":

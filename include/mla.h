@@ -339,6 +339,61 @@ mla_status mla_rope_q(const void* q_pe, const int32_t* positions, const float* t
                       void* q_r, int32_t T, int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * Decompress branch ([P1] §3: kPrefillThresh = 256, the plugin's
+ * prefill_absorption_threshold; §4 path A: K = c_KV·W_UK per head; [P2] MLA
+ * section: V = c_KV·W_UV).  A chunk of at least MLA_PREFILL_THRESHOLD query
+ * tokens of one sequence is not absorbed: its cached latent is expanded once
+ * into per-head K_c and V_c, and standard causal attention runs per head,
+ *   s = (q_c[t,h]·K_c[j,h] + q_R[t,h]·k_R[j]) * scale,  out[t,h] = softmax(s)·V_c[.,h],
+ * query t of the chunk (M rows) sitting at position N - M + t of its
+ * sequence (N tokens cached, the chunk included) and seeing [0, N - M + t].
+ * The result equals steps A2-A5 of the absorbed path (the same out).
+ * ------------------------------------------------------------------------- */
+#define MLA_PREFILL_THRESHOLD 256
+#define MLA_BRANCH_ABSORB 0
+#define MLA_BRANCH_DECOMPRESS 1
+
+/* The threshold (256) and the branch a sequence's q_len takes. */
+int32_t mla_prefill_threshold(void);
+int32_t mla_branch_for(int32_t q_len);
+
+/*
+ * Expand n cached rows: rows bf16 [n, 576] (e.g. from mla_gather_paged; only
+ * columns 0..511 are read), W_UK bf16 [128, 128, 512], W_UV bf16 [128, 512, 128];
+ * k_c[h, t, :] = rows[t, 0:512]·W_UK[h]^T and v_c[h, t, :] = rows[t, 0:512]·W_UV[h],
+ * bf16 [128, n, 128], head-major (fp32 accumulation, one rounding).  All
+ * pointers device, 16-byte aligned.  n == 0 is a no-op.
+ */
+mla_status mla_expand_kv(const void* rows, int32_t n, const void* w_uk, const void* w_uv, void* k_c, void* v_c,
+                         int32_t* dev_err, void* stream);
+
+/*
+ * Causal attention of the decompress branch for one sequence: q_c bf16
+ * [M, 128, 128] and q_r bf16 [M, 128, 64] (the chunk's rows), rows bf16
+ * [N, 576] (k_R read from columns 512..575), k_c / v_c from mla_expand_kv,
+ * out bf16 [M, 128, 128].  1 <= M <= N (M == 0 is a no-op); scale finite > 0.
+ */
+mla_status mla_prefill_attention(const void* q_c, const void* q_r, int32_t M, const void* rows, const void* k_c,
+                                 const void* v_c, int32_t N, float scale, void* out, int32_t* dev_err,
+                                 void* stream);
+
+/* Workspace bytes mla_prefill_decompress needs for N cached tokens:
+ * gathered rows [N, 576] (16-byte rounded) + K_c + V_c (2 * N * 32 KiB). */
+mla_status mla_prefill_workspace_size(int32_t N, size_t* bytes);
+
+/*
+ * The whole branch for sequence b of a paged cache: gather its N cached
+ * tokens (mla_gather_paged), expand them (mla_expand_kv) and attend
+ * (mla_prefill_attention) into out bf16 [M, 128, 128].  workspace is
+ * device memory of at least mla_prefill_workspace_size(N) bytes, 16-byte
+ * aligned; the same validation and device error bits as the three calls.
+ */
+mla_status mla_prefill_decompress(const void* q_c, const void* q_r, int32_t M, const void* kv_cache, int64_t num_pages,
+                                  const int32_t* block_table, int32_t max_pages, int32_t b, int32_t N,
+                                  const void* w_uk, const void* w_uv, float scale, void* workspace, size_t ws_bytes,
+                                  void* out, int32_t* dev_err, void* stream);
+
+/* ---------------------------------------------------------------------------
  * FP8 (E4M3) latent cache ([P3] bjbfmj.com/news/60700: quantisation scale
  * factors are stored beside the cached elements; [P1] opening section and
  * §5: a quantised gather with 16-byte vector loads).  E4M3 is the OCP 8-bit

@@ -52,6 +52,12 @@ SIGNATURES = {
     "mla_gather_paged_fp8": (C.c_int, [P, P, I64, P, I32, I32, I32, P, P, P]),
     "mla_kv_append_nvfp4": (C.c_int, [P, P, P, I32, C.c_float, P, I64, P, P]),
     "mla_gather_paged_nvfp4": (C.c_int, [P, C.c_float, I64, P, I32, I32, I32, P, P, P]),
+    "mla_prefill_threshold": (I32, []),
+    "mla_branch_for": (I32, [I32]),
+    "mla_expand_kv": (C.c_int, [P, I32, P, P, P, P, P, P]),
+    "mla_prefill_attention": (C.c_int, [P, P, I32, P, P, P, I32, C.c_float, P, P, P]),
+    "mla_prefill_workspace_size": (C.c_int, [I32, C.POINTER(SZ)]),
+    "mla_prefill_decompress": (C.c_int, [P, P, I32, P, I64, P, I32, I32, I32, P, P, C.c_float, P, SZ, P, P, P]),
     "mla_rope_table": (C.c_int, [I32, C.c_float, P, P]),
     "mla_kv_append_rope": (C.c_int, [P, P, P, P, I32, P, I32, P, I64, P, P]),
     "mla_rope_q": (C.c_int, [P, P, P, I32, P, I32, P, P]),

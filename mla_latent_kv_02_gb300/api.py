@@ -191,6 +191,66 @@ def mla_gather_paged_nvfp4(rows, tensor_scale: float, block_table, b: int, n_tok
                                         _stream(stream)))
 
 
+def mla_prefill_threshold() -> int:
+    return int(lib().mla_prefill_threshold())
+
+
+def mla_branch_for(q_len: int) -> int:
+    """0 = absorbed (steps A2-A5), 1 = decompress branch."""
+    return int(lib().mla_branch_for(int(q_len)))
+
+
+def mla_expand_kv(rows, w_uk, w_uv, k_c, v_c, dev_err, stream=None) -> None:
+    n = rows.shape[0]
+    _need(rows, "rows", torch.bfloat16, (n, D_QK))
+    _need(w_uk, "w_uk", torch.bfloat16, (H, D_HC, D_C))
+    _need(w_uv, "w_uv", torch.bfloat16, (H, D_C, D_HC))
+    _need(k_c, "k_c", torch.bfloat16, (H, n, D_HC))
+    _need(v_c, "v_c", torch.bfloat16, (H, n, D_HC))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_expand_kv(_ptr(rows), int(n), _ptr(w_uk), _ptr(w_uv), _ptr(k_c), _ptr(v_c), _ptr(dev_err),
+                               _stream(stream)))
+
+
+def mla_prefill_attention(q_c, q_r, rows, k_c, v_c, out, dev_err, scale: float = 1.0 / (192 ** 0.5),
+                          stream=None) -> None:
+    M, N = q_c.shape[0], rows.shape[0]
+    _need(q_c, "q_c", torch.bfloat16, (M, H, D_HC))
+    _need(q_r, "q_r", torch.bfloat16, (M, H, D_R))
+    _need(rows, "rows", torch.bfloat16, (N, D_QK))
+    _need(k_c, "k_c", torch.bfloat16, (H, N, D_HC))
+    _need(v_c, "v_c", torch.bfloat16, (H, N, D_HC))
+    _need(out, "out", torch.bfloat16, (M, H, D_HC))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_prefill_attention(_ptr(q_c), _ptr(q_r), int(M), _ptr(rows), _ptr(k_c), _ptr(v_c), int(N),
+                                       float(scale), _ptr(out), _ptr(dev_err), _stream(stream)))
+
+
+def mla_prefill_workspace_size(N: int) -> int:
+    out = C.c_size_t()
+    _check(lib().mla_prefill_workspace_size(int(N), C.byref(out)))
+    return int(out.value)
+
+
+def mla_prefill_decompress(q_c, q_r, kv_cache, block_table, b: int, n_tokens: int, w_uk, w_uv, workspace, out,
+                           dev_err, scale: float = 1.0 / (192 ** 0.5), stream=None) -> None:
+    """The decompress branch for sequence b (n_tokens cached, the chunk's M = q_c.shape[0] rows last)."""
+    M = q_c.shape[0]
+    _need(q_c, "q_c", torch.bfloat16, (M, H, D_HC))
+    _need(q_r, "q_r", torch.bfloat16, (M, H, D_R))
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(w_uk, "w_uk", torch.bfloat16, (H, D_HC, D_C))
+    _need(w_uv, "w_uv", torch.bfloat16, (H, D_C, D_HC))
+    _need(workspace, "workspace", torch.uint8)
+    _need(out, "out", torch.bfloat16, (M, H, D_HC))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_prefill_decompress(_ptr(q_c), _ptr(q_r), int(M), _ptr(kv_cache), kv_cache.shape[0],
+                                        _ptr(block_table), block_table.shape[1], int(b), int(n_tokens), _ptr(w_uk),
+                                        _ptr(w_uv), float(scale), _ptr(workspace), workspace.numel(), _ptr(out),
+                                        _ptr(dev_err), _stream(stream)))
+
+
 def mla_rope_table(max_pos: int, table, base: float = 10000.0, stream=None) -> None:
     _need(table, "table", torch.float32, (max_pos, D_R // 2, 2))
     _check(lib().mla_rope_table(int(max_pos), float(base), _ptr(table), _stream(stream)))

@@ -65,6 +65,16 @@ struct DecodeArgs {
   const float* kv_scales;  // FP8 cache: fp32 [num_pages * 64] token scales (null for bf16)
 };
 
+// Decompress branch: one sequence, M query rows at positions N - M .. N - 1.
+struct PrefillArgs {
+  int32_t M;
+  int32_t N;
+  float scale_log2;     // scale * log2(e)
+  int32_t pad_;
+  uint16_t* out;        // bf16 [M, 128, 128]
+  int32_t* dev_err;
+};
+
 struct CombineArgs {
   const int32_t* split_rows;
   const float* part_o;
@@ -110,8 +120,15 @@ cudaError_t launch_gather_nvfp4(const uint8_t* rows, float tensor_scale, int64_t
 cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                           int32_t b, int32_t n_tokens, uint16_t* out, int32_t* dev_err, cudaStream_t stream);
 
+int prefill_smem_bytes();
+cudaError_t launch_prefill_attn(const CUtensorMap& q_map, const CUtensorMap& r_map, const CUtensorMap& k_map,
+                                const CUtensorMap& kr_map, const CUtensorMap& v_map, const PrefillArgs& args,
+                                cudaStream_t stream);
+
 // Per-head GEMM C[t, h, :] = A[t, h, :] · W[h] (bf16 in, fp32 accumulate, bf16 out).
-enum class HeadGemm { kAbsorbQ, kUpV };
+// kExpandK / kExpandV (decompress branch): A = latent rows shared by all
+// heads; K_c = c·W_UK[h]^T (W_UK read K-major), V_c = c·W_UV[h].
+enum class HeadGemm { kAbsorbQ, kUpV, kExpandK, kExpandV };
 cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
                              int32_t T, int32_t* err, cudaStream_t stream);
 

@@ -595,6 +595,13 @@ mla_status mla_gather_paged_nvfp4(const void* rows, float tensor_scale, int64_t 
   return MLA_OK;
 }
 
+// Decompress-branch workspace: gathered rows [N, 576] (rounded up to 16 B),
+// then K_c and V_c [N, 128, 128] bf16.
+static size_t prefill_rows_bytes(int64_t N) { return ((size_t)N * kRowBytes + 15) / 16 * 16; }
+static size_t prefill_ws_bytes(int64_t N) {
+  return prefill_rows_bytes(N) + 2 * (size_t)N * MLA_NUM_HEADS * MLA_HEAD_DIM_C * 2;
+}
+
 static mla_status head_gemm(mla::HeadGemm kind, const void* a, const void* w, void* c, int32_t T, int32_t* dev_err,
                             void* stream) {
   if (T < 0) return fail(MLA_ERR_INVALID_ARG, "T = %d < 0", T);
@@ -626,6 +633,135 @@ static mla_status head_gemm(mla::HeadGemm kind, const void* a, const void* w, vo
   cudaError_t e = mla::launch_head_gemm(kind, amap, wmap, (uint16_t*)c, T, dev_err, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, absorb ? "absorb_q launch" : "up_v launch");
   return MLA_OK;
+}
+
+// ------------------------------------------------------------------ decompress branch
+int32_t mla_prefill_threshold(void) { return MLA_PREFILL_THRESHOLD; }
+
+int32_t mla_branch_for(int32_t q_len) { return q_len >= MLA_PREFILL_THRESHOLD ? MLA_BRANCH_DECOMPRESS : MLA_BRANCH_ABSORB; }
+
+mla_status mla_expand_kv(const void* rows, int32_t n, const void* w_uk, const void* w_uv, void* k_c, void* v_c,
+                         int32_t* dev_err, void* stream) {
+  if (n < 0) return fail(MLA_ERR_INVALID_ARG, "n = %d < 0", n);
+  if (n == 0) return MLA_OK;
+  CHECK_PTR(rows);
+  CHECK_PTR(w_uk);
+  CHECK_PTR(w_uv);
+  CHECK_PTR(k_c);
+  CHECK_PTR(v_c);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(rows);
+  CHECK_ALIGN16(w_uk);
+  CHECK_ALIGN16(w_uv);
+  CHECK_ALIGN16(k_c);
+  CHECK_ALIGN16(v_c);
+  if (!aligned(dev_err, 4)) return fail(MLA_ERR_MISALIGNED, "dev_err is not 4-byte aligned");
+  if (n > (1 << 24)) return fail(MLA_ERR_INVALID_ARG, "n = %d too large", n);
+  CUtensorMap amap, kmap, vmap;
+  // latent part of the rows [n, 576] as {512, 1 (shared by every head), n}
+  const uint64_t adims[3] = {MLA_LATENT_DIM, 1, (uint64_t)n};
+  const uint64_t astr[2] = {(uint64_t)kRowBytes, (uint64_t)kRowBytes};
+  const uint32_t abox[3] = {64, 1, 128};
+  mla_status s = make_map(&amap, rows, 3, adims, astr, abox, "latent rows");
+  if (s != MLA_OK) return s;
+  // W_UK [128, 128 (d_hc), 512 (d_c)] read K-major: box 64 of d_c x 128 of d_hc x 1 head
+  const uint64_t kdims[3] = {MLA_LATENT_DIM, MLA_HEAD_DIM_C, MLA_NUM_HEADS};
+  const uint64_t kstr[2] = {MLA_LATENT_DIM * 2, (uint64_t)MLA_LATENT_DIM * 2 * MLA_HEAD_DIM_C};
+  const uint32_t kbox[3] = {64, 128, 1};
+  s = make_map(&kmap, w_uk, 3, kdims, kstr, kbox, "W_UK (K-major)");
+  if (s != MLA_OK) return s;
+  // W_UV [128, 512 (d_c), 128 (d_hc)] as in step A5
+  const uint64_t vdims[3] = {MLA_HEAD_DIM_C, MLA_LATENT_DIM, MLA_NUM_HEADS};
+  const uint64_t vstr[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)MLA_HEAD_DIM_C * 2 * MLA_LATENT_DIM};
+  const uint32_t vbox[3] = {64, 64, 1};
+  s = make_map(&vmap, w_uv, 3, vdims, vstr, vbox, "W_UV");
+  if (s != MLA_OK) return s;
+  cudaError_t e = mla::launch_head_gemm(mla::HeadGemm::kExpandK, amap, kmap, (uint16_t*)k_c, n, dev_err,
+                                        (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "expand K launch");
+  e = mla::launch_head_gemm(mla::HeadGemm::kExpandV, amap, vmap, (uint16_t*)v_c, n, dev_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "expand V launch");
+  return MLA_OK;
+}
+
+mla_status mla_prefill_attention(const void* q_c, const void* q_r, int32_t M, const void* rows, const void* k_c,
+                                 const void* v_c, int32_t N, float scale, void* out, int32_t* dev_err,
+                                 void* stream) {
+  if (M < 0 || N < 0) return fail(MLA_ERR_INVALID_ARG, "M = %d, N = %d: negative", M, N);
+  if (M == 0) return MLA_OK;
+  if (M > N) return fail(MLA_ERR_INVALID_ARG, "M = %d query rows exceed the N = %d cached tokens", M, N);
+  if (N > (1 << 24)) return fail(MLA_ERR_INVALID_ARG, "N = %d too large", N);
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and positive");
+  CHECK_PTR(q_c);
+  CHECK_PTR(q_r);
+  CHECK_PTR(rows);
+  CHECK_PTR(k_c);
+  CHECK_PTR(v_c);
+  CHECK_PTR(out);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(q_c);
+  CHECK_ALIGN16(q_r);
+  CHECK_ALIGN16(rows);
+  CHECK_ALIGN16(k_c);
+  CHECK_ALIGN16(v_c);
+  CHECK_ALIGN16(out);
+  if (!aligned(dev_err, 4)) return fail(MLA_ERR_MISALIGNED, "dev_err is not 4-byte aligned");
+  CUtensorMap qm, rm, km, krm, vm;
+  const uint32_t box3[3] = {64, 1, 128};
+  const uint64_t qd[3] = {MLA_HEAD_DIM_C, MLA_NUM_HEADS, (uint64_t)M};
+  const uint64_t qs[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)MLA_HEAD_DIM_C * 2 * MLA_NUM_HEADS};
+  const uint64_t rd[3] = {MLA_ROPE_DIM, MLA_NUM_HEADS, (uint64_t)M};
+  const uint64_t rs[2] = {MLA_ROPE_DIM * 2, (uint64_t)MLA_ROPE_DIM * 2 * MLA_NUM_HEADS};
+  const uint64_t kd[3] = {MLA_HEAD_DIM_C, (uint64_t)N, MLA_NUM_HEADS};   // head-major K_c / V_c
+  const uint64_t ks[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)MLA_HEAD_DIM_C * 2 * (uint64_t)N};
+  const uint32_t kbox[3] = {64, 128, 1};
+  const uint64_t krd[2] = {MLA_TOKEN_ELEMS, (uint64_t)N};
+  const uint64_t krs[1] = {(uint64_t)kRowBytes};
+  const uint32_t box2[2] = {64, 128};
+  mla_status s = make_map(&qm, q_c, 3, qd, qs, box3, "q_c");
+  if (s == MLA_OK) s = make_map(&rm, q_r, 3, rd, rs, box3, "q_r");
+  if (s == MLA_OK) s = make_map(&km, k_c, 3, kd, ks, kbox, "K_c");
+  if (s == MLA_OK) s = make_map(&vm, v_c, 3, kd, ks, kbox, "V_c");
+  if (s == MLA_OK) s = make_map(&krm, rows, 2, krd, krs, box2, "k_R rows");
+  if (s != MLA_OK) return s;
+  mla::PrefillArgs a = {};
+  a.M = M;
+  a.N = N;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.out = (uint16_t*)out;
+  a.dev_err = dev_err;
+  cudaError_t e = mla::launch_prefill_attn(qm, rm, km, krm, vm, a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+  return MLA_OK;
+}
+
+mla_status mla_prefill_workspace_size(int32_t N, size_t* bytes) {
+  CHECK_PTR(bytes);
+  if (N < 0) return fail(MLA_ERR_INVALID_ARG, "N = %d < 0", N);
+  *bytes = prefill_ws_bytes(N);
+  return MLA_OK;
+}
+
+mla_status mla_prefill_decompress(const void* q_c, const void* q_r, int32_t M, const void* kv_cache, int64_t num_pages,
+                                  const int32_t* block_table, int32_t max_pages, int32_t b, int32_t N,
+                                  const void* w_uk, const void* w_uv, float scale, void* workspace, size_t ws_bytes,
+                                  void* out, int32_t* dev_err, void* stream) {
+  if (M < 0 || N < 0) return fail(MLA_ERR_INVALID_ARG, "M = %d, N = %d: negative", M, N);
+  if (M == 0) return MLA_OK;
+  if (M > N) return fail(MLA_ERR_INVALID_ARG, "M = %d query rows exceed the N = %d cached tokens", M, N);
+  CHECK_PTR(workspace);
+  CHECK_ALIGN16(workspace);
+  if (N < 0 || ws_bytes < prefill_ws_bytes(N))
+    return fail(MLA_ERR_INVALID_ARG, "workspace holds %zu bytes, N = %d needs %zu", ws_bytes, N,
+                prefill_ws_bytes(N < 0 ? 0 : N));
+  uint8_t* ws = (uint8_t*)workspace;
+  void* rows = ws;
+  void* k_c = ws + prefill_rows_bytes(N);
+  void* v_c = (uint8_t*)k_c + (size_t)N * MLA_NUM_HEADS * MLA_HEAD_DIM_C * 2;
+  mla_status s = mla_gather_paged(kv_cache, num_pages, block_table, max_pages, b, N, rows, dev_err, stream);
+  if (s == MLA_OK) s = mla_expand_kv(rows, N, w_uk, w_uv, k_c, v_c, dev_err, stream);
+  if (s == MLA_OK) s = mla_prefill_attention(q_c, q_r, M, rows, k_c, v_c, N, scale, out, dev_err, stream);
+  return s;
 }
 
 mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t T, int32_t* dev_err, void* stream) {

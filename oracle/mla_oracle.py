@@ -271,6 +271,15 @@ def naive_attention_row(q_c_row, q_r_row, c_kv, k_r, w_uk, w_uv, scale):
     return out, lse
 
 
+def expand_kv(c_kv: np.ndarray, w_uk: np.ndarray, w_uv: np.ndarray) -> Tuple[np.ndarray, np.ndarray]:
+    """[P1] §4 path A expansion, every head at once:
+    K_c[t, h, d] = Σ_c c_KV[t, c]·W_UK[h, d, c],  V_c[t, h, e] = Σ_c c_KV[t, c]·W_UV[h, c, e]."""
+    c = np.asarray(c_kv, dtype=np.float64)
+    k = np.einsum("tc,hdc->thd", c, np.asarray(w_uk, dtype=np.float64))
+    v = np.einsum("tc,hce->the", c, np.asarray(w_uv, dtype=np.float64))
+    return k, v
+
+
 def naive_scores(q_c_row, q_r_row, c_kv, k_r, w_uk, scale):
     """[P1] §4 path A scores [H, n]."""
     c = np.asarray(c_kv, dtype=np.float64)

@@ -339,3 +339,31 @@ def test_planted_mistakes_are_caught():
     assert not _pin_absorbed_vs_naive(up_fn=bad_up)
     # off-by-one visibility would change the causal pin
     assert oracle.visible_tokens(100, 3, 0) == 98
+
+
+# ------------------------------------------------------------------ decompress-branch expansion
+def test_expand_kv_closed_forms_and_absorption():
+    """K_c/V_c against closed forms: identity blocks pick latent columns; and
+    q_c·K_c equals the absorbed q_abs·c_KV (the associativity the pages use)."""
+    rng = np.random.default_rng(21)
+    n, H, d, dc = 7, 3, 4, 10
+    c = rng.standard_normal((n, dc))
+    w_uk = np.zeros((H, d, dc))
+    w_uv = np.zeros((H, dc, d))
+    for h in range(H):
+        w_uk[h, :, h:h + d] = np.eye(d)
+        w_uv[h, h:h + d, :] = np.eye(d)
+    k, v = oracle.expand_kv(c, w_uk, w_uv)
+    for h in range(H):
+        assert np.array_equal(k[:, h], c[:, h:h + d]) and np.array_equal(v[:, h], c[:, h:h + d])
+    w_uk = rng.standard_normal((H, d, dc))
+    w_uv = rng.standard_normal((H, dc, d))
+    k, v = oracle.expand_kv(c, w_uk, w_uv)
+    q = rng.standard_normal((H, d))
+    qa = oracle.absorb_q(q[None], w_uk)[0]
+    for h in range(H):
+        assert np.allclose(k[:, h] @ q[h], c @ qa[h], rtol=1e-12, atol=1e-12)
+        assert np.allclose(v[:, h], c @ w_uv[h], rtol=1e-12, atol=1e-12)
+    # the plausible mistake, contracting over W_UK's other axis (square block), changes the result
+    sq = w_uk[:, :, :d]
+    assert not np.allclose(np.einsum("tc,hcd->thd", c[:, :d], sq), np.einsum("tc,hdc->thd", c[:, :d], sq))
