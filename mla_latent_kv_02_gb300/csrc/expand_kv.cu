@@ -1,0 +1,178 @@
+// Decompress branch (f2): expansion of the cached latent into per-head keys
+// and values in one pass ([P1] "撕开 DeepSeek MLA 源码…" §4 path A,
+// K = c_KV·W_UK per head; [P2] MLA section, V = c_KV·W_UV):
+//   K_c[h, t, :] = c[t, :]·W_UK[h]^T,   V_c[h, t, :] = c[t, :]·W_UV[h]
+// (head-major outputs, one head's rows contiguous for the attention's loads).
+//
+// One CTA = one head and 256 tokens: four 128 x 128 fp32 accumulators in
+// TMEM (K and V for each 128-token half, all 512 columns).  Each 64-wide
+// K-chunk of the latent is loaded once for both outputs and both W tiles
+// once for both token halves, so a CTA moves 512 KB for 67 MFLOP.  Warp 0
+// lane 0 issues TMA, warp 1 lane 0 the MMAs; all four warps run the
+// epilogue (thread = token row = TMEM lane).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+#include "ptx.cuh"
+
+namespace mla {
+namespace expand {
+
+using namespace mla::dev;
+
+constexpr int kM = 256, kKCh = 512 / 64;
+constexpr int kTile = 128 * 64 * 2;              // 16 KB: 128 rows x 64, 128-byte swizzle
+constexpr int kStage = 4 * kTile;                // A rows 0-127 | A rows 128-255 | W_UK chunk | W_UV chunk
+constexpr int kStages = 3;
+constexpr int kOffBar = kStages * kStage;
+constexpr int kOffMisc = kOffBar + 8 * (2 * kStages + 1);
+constexpr int kSmem = kOffMisc + 16 + 1024;
+static_assert(kSmem <= 232448, "shared memory layout does not fit");
+constexpr uint32_t kIdescK = idesc_bf16_f32(128, 128, false, false);  // W_UK read K-major
+constexpr uint32_t kIdescV = idesc_bf16_f32(128, 128, false, true);   // W_UV read MN-major
+
+// a_map: latent rows {512, 1, n} (box 64 x 1 x 128); k_map: W_UK {512, 128, 128 heads}
+// (box 64 x 128 x 1); v_map: W_UV {128, 512, 128 heads} (box 64 x 64 x 1).
+__global__ void __launch_bounds__(128, 1)
+    expand_kv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap k_map,
+                     const __grid_constant__ CUtensorMap v_map, uint16_t* __restrict__ k_c,
+                     uint16_t* __restrict__ v_c, int32_t n, int32_t* err) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t bars = base + kOffBar;
+  const uint32_t full0 = bars, empty0 = bars + 8 * kStages, done = bars + 16 * kStages;
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + kOffMisc);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kOffMisc + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y;
+  const int m0 = blockIdx.x * kM;
+
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&a_map);
+      prefetch_tmap(&k_map);
+      prefetch_tmap(&v_map);
+      int issued = 0;
+      for (int kc = 0; kc < kKCh; ++kc) {
+        const int st = kc % kStages, use = kc / kStages;
+        if (use > 0 && !wait_phase(empty0 + 8 * st, (use - 1) & 1, err, abort_flag)) break;
+        const uint32_t dst = base + st * kStage;
+        const uint32_t fb = full0 + 8 * st;
+        mbar_arrive_expect_tx(fb, (uint32_t)kStage);
+        tma_load_3d(dst, &a_map, kc * 64, 0, m0, fb);
+        tma_load_3d(dst + kTile, &a_map, kc * 64, 0, m0 + 128, fb);
+        tma_load_3d(dst + 2 * kTile, &k_map, kc * 64, 0, h, fb);
+        tma_load_3d(dst + 3 * kTile, &v_map, 0, kc * 64, h, fb);
+        tma_load_3d(dst + 3 * kTile + 8192, &v_map, 64, kc * 64, h, fb);
+        ++issued;
+      }
+      for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
+        wait_phase_drain(full0 + 8 * (k % kStages), (k / kStages) & 1);
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      bool ok = true;
+      for (int kc = 0; kc < kKCh; ++kc) {
+        const int st = kc % kStages;
+        if (!wait_phase(full0 + 8 * st, (kc / kStages) & 1, err, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sa = base + st * kStage;
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (kc | kk) ? 1u : 0u;
+          const uint64_t a0 = sdesc_sw128(sa + kk * 32, 16, 1024);
+          const uint64_t a1 = sdesc_sw128(sa + kTile + kk * 32, 16, 1024);
+          const uint64_t bk = sdesc_sw128(sa + 2 * kTile + kk * 32, 16, 1024);
+          const uint64_t bv = sdesc_sw128(sa + 3 * kTile + kk * 2048, 8192, 1024);
+          mma_ss(tmem + 0, a0, bk, kIdescK, acc);
+          mma_ss(tmem + 128, a0, bv, kIdescV, acc);
+          mma_ss(tmem + 256, a1, bk, kIdescK, acc);
+          mma_ss(tmem + 384, a1, bv, kIdescV, acc);
+        }
+        tc_commit(empty0 + 8 * st);
+      }
+      tc_commit(done);
+      if (!ok) wait_phase_drain(done, 0);
+    }
+    __syncwarp();
+  }
+
+  // Epilogue: thread = token row of each 128-token half, all four warps.
+  bool w = wait_phase(done, 0, err, abort_flag) && !*abort_flag;
+  w = __all_sync(0xffffffffu, w);
+  tc_fence_after();
+  if (w) {
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+#pragma unroll 1
+    for (int q = 0; q < 4; ++q) {              // K rows 0-127, V rows 0-127, K rows 128-255, V rows 128-255
+      const int t = m0 + (q >> 1) * 128 + warp * 32 + lane;
+      uint16_t* outp = (q & 1) ? v_c : k_c;
+      uint4* dst = reinterpret_cast<uint4*>(outp + ((size_t)h * n + t) * 128);
+#pragma unroll 1
+      for (int col = 0; col < 128; col += 32) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32_sync(tl + q * 128 + col, r);
+        if (t < n) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v)
+            dst[col / 8 + v] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
+                                          pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
+                                          pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
+                                          pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace expand
+
+cudaError_t launch_expand_kv(const CUtensorMap& a_map, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                             uint16_t* k_c, uint16_t* v_c, int32_t n, int32_t* err, cudaStream_t stream) {
+  if (n <= 0) return cudaSuccess;
+  cudaError_t e = cudaFuncSetAttribute(expand::expand_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       expand::kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((n + expand::kM - 1) / expand::kM, 128);
+  expand::expand_kv_kernel<<<grid, 128, expand::kSmem, stream>>>(a_map, k_map, v_map, k_c, v_c, n, err);
+  return cudaGetLastError();
+}
+
+}  // namespace mla

@@ -5,12 +5,6 @@
 //   A5  out[t, h, :]   = o_lat[t, h, :] · W_UV[h]   (K = 512 -> N = 128)
 //       ([P2] "DeepSeek的推理为什么比别人便宜一个数量级？…", MLA section: V = c·W_UV)
 //
-// The decompress branch (f2) expands the cached latent per head with the same
-// kernel, A shared by all heads (SHARED_A), W either row-major [K x N] or,
-// for K = c·W_UK^T, stored [N x K] and read K-major (B_KMAJOR), and the
-// output head-major (one head's rows contiguous, for the attention's loads):
-//   K_c[h, t, :] = c_KV[t, :] · W_UK[h]^T,   V_c[h, t, :] = c_KV[t, :] · W_UV[h].
-//
 // One CTA computes a 128-row tile of tokens for one head and one of NSPLIT
 // column blocks: D[128 x N/NSPLIT] fp32 in TMEM, A (activation rows,
 // K-major) and W (row-major [K x N], read as an MN-major operand) staged by
@@ -31,7 +25,7 @@ namespace gemm {
 
 using namespace mla::dev;
 
-template <int N, int K, int STAGES, int NSPLIT, bool B_KMAJOR = false>
+template <int N, int K, int STAGES, int NSPLIT>
 struct Cfg {
   static constexpr int kNC = N / NSPLIT;  // columns of this CTA
   static constexpr int kKCh = K / 64;
@@ -42,16 +36,16 @@ struct Cfg {
   static constexpr int kOffMisc = kOffBar + 8 * (2 * STAGES + 1);
   static constexpr int kSmem = kOffMisc + 16 + 1024;
   static constexpr int kMmaN = kNC < 256 ? kNC : 256;
-  static constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN, false, !B_KMAJOR);
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN, false, true);
   static_assert((NSPLIT == 1 ? 1 : 2) * kSmem <= 232448, "a split head GEMM needs two CTAs per SM");
   static_assert(kNC % 64 == 0 && kNC >= 64, "column block is a multiple of 64");
 };
 
-template <int N, int K, int STAGES, int NSPLIT, bool SHARED_A = false, bool B_KMAJOR = false>
+template <int N, int K, int STAGES, int NSPLIT>
 __global__ void __launch_bounds__(128, 2)
     head_gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
                      uint16_t* __restrict__ c, int32_t T, int32_t* err) {
-  using C = Cfg<N, K, STAGES, NSPLIT, B_KMAJOR>;
+  using C = Cfg<N, K, STAGES, NSPLIT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -95,15 +89,10 @@ __global__ void __launch_bounds__(128, 2)
         if (use > 0 && !wait_phase(empty0 + 8 * st, (use - 1) & 1, err, abort_flag)) break;
         const uint32_t dst = base + st * C::kStage;
         mbar_arrive_expect_tx(full0 + 8 * st, (uint32_t)C::kStage);
-        tma_load_3d(dst, &a_map, kc * 64, SHARED_A ? 0 : h, m0, full0 + 8 * st);
-        if constexpr (B_KMAJOR) {
-          // W[h] stored [N x K]: one box of 64 K-elements x kNC rows (K-major, 128-byte swizzle)
-          tma_load_3d(dst + C::kABytes, &w_map, kc * 64, n0, h, full0 + 8 * st);
-        } else {
+        tma_load_3d(dst, &a_map, kc * 64, h, m0, full0 + 8 * st);
 #pragma unroll
-          for (int nb = 0; nb < C::kNC / 64; ++nb)
-            tma_load_3d(dst + C::kABytes + nb * 8192, &w_map, n0 + nb * 64, kc * 64, h, full0 + 8 * st);
-        }
+        for (int nb = 0; nb < C::kNC / 64; ++nb)
+          tma_load_3d(dst + C::kABytes + nb * 8192, &w_map, n0 + nb * 64, kc * 64, h, full0 + 8 * st);
         ++issued;
       }
       for (int k = (issued > STAGES ? issued - STAGES : 0); k < issued; ++k)
@@ -125,11 +114,10 @@ __global__ void __launch_bounds__(128, 2)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
 #pragma unroll
-          for (int nh = 0; nh < C::kNC / C::kMmaN; ++nh) {
-            const uint64_t bdesc = B_KMAJOR ? sdesc_sw128(sb + nh * C::kMmaN * 128 + kk * 32, 16, 1024)
-                                            : sdesc_sw128(sb + nh * (C::kMmaN / 64) * 8192 + kk * 2048, 8192, 1024);
-            mma_ss(tmem + nh * C::kMmaN, sdesc_sw128(sa + kk * 32, 16, 1024), bdesc, C::kIdesc, (kc | kk) ? 1u : 0u);
-          }
+          for (int nh = 0; nh < C::kNC / C::kMmaN; ++nh)
+            mma_ss(tmem + nh * C::kMmaN, sdesc_sw128(sa + kk * 32, 16, 1024),
+                   sdesc_sw128(sb + nh * (C::kMmaN / 64) * 8192 + kk * 2048, 8192, 1024), C::kIdesc,
+                   (kc | kk) ? 1u : 0u);
         tc_commit(empty0 + 8 * st);
       }
       tc_commit(done);  // also fires (after in-flight MMAs) when the loop stopped early
@@ -145,8 +133,7 @@ __global__ void __launch_bounds__(128, 2)
   if (w) {
     const int t = m0 + warp * 32 + lane;
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-    const size_t orow = SHARED_A ? (size_t)h * T + t : (size_t)t * 128 + h;  // head-major for the expansion
-    uint4* dst = reinterpret_cast<uint4*>(c + orow * N + n0);
+    uint4* dst = reinterpret_cast<uint4*>(c + ((size_t)t * 128 + h) * N + n0);
 #pragma unroll 1
     for (int col = 0; col < C::kNC; col += 32) {
       uint32_t r[32];
@@ -171,11 +158,11 @@ __global__ void __launch_bounds__(128, 2)
   }
 }
 
-template <int N, int K, int STAGES, int NSPLIT, bool SHARED_A = false, bool B_KMAJOR = false>
+template <int N, int K, int STAGES, int NSPLIT>
 cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c, int32_t T, int32_t* err,
                 cudaStream_t stream) {
-  using C = Cfg<N, K, STAGES, NSPLIT, B_KMAJOR>;
-  auto* kern = head_gemm_kernel<N, K, STAGES, NSPLIT, SHARED_A, B_KMAJOR>;
+  using C = Cfg<N, K, STAGES, NSPLIT>;
+  auto* kern = head_gemm_kernel<N, K, STAGES, NSPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((T + 127) / 128, 128, NSPLIT);
@@ -187,13 +174,8 @@ cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
 
 cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
                              int32_t T, int32_t* err, cudaStream_t stream) {
-  switch (kind) {
-    case HeadGemm::kAbsorbQ: return gemm::run<512, 128, 2, 2>(a_map, w_map, c, T, err, stream);
-    case HeadGemm::kUpV: return gemm::run<128, 512, 4, 1>(a_map, w_map, c, T, err, stream);
-    case HeadGemm::kExpandK: return gemm::run<128, 512, 4, 1, true, true>(a_map, w_map, c, T, err, stream);
-    case HeadGemm::kExpandV: return gemm::run<128, 512, 4, 1, true, false>(a_map, w_map, c, T, err, stream);
-  }
-  return cudaErrorInvalidValue;
+  if (kind == HeadGemm::kAbsorbQ) return gemm::run<512, 128, 2, 2>(a_map, w_map, c, T, err, stream);
+  return gemm::run<128, 512, 4, 1>(a_map, w_map, c, T, err, stream);
 }
 
 }  // namespace mla

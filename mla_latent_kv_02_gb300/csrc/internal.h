@@ -120,15 +120,16 @@ cudaError_t launch_gather_nvfp4(const uint8_t* rows, float tensor_scale, int64_t
 cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                           int32_t b, int32_t n_tokens, uint16_t* out, int32_t* dev_err, cudaStream_t stream);
 
+// Decompress-branch expansion: K_c and V_c in one pass (head-major outputs).
+cudaError_t launch_expand_kv(const CUtensorMap& a_map, const CUtensorMap& k_map, const CUtensorMap& v_map,
+                             uint16_t* k_c, uint16_t* v_c, int32_t n, int32_t* err, cudaStream_t stream);
 int prefill_smem_bytes();
 cudaError_t launch_prefill_attn(const CUtensorMap& q_map, const CUtensorMap& r_map, const CUtensorMap& k_map,
                                 const CUtensorMap& kr_map, const CUtensorMap& v_map, const PrefillArgs& args,
                                 cudaStream_t stream);
 
 // Per-head GEMM C[t, h, :] = A[t, h, :] · W[h] (bf16 in, fp32 accumulate, bf16 out).
-// kExpandK / kExpandV (decompress branch): A = latent rows shared by all
-// heads; K_c = c·W_UK[h]^T (W_UK read K-major), V_c = c·W_UV[h].
-enum class HeadGemm { kAbsorbQ, kUpV, kExpandK, kExpandV };
+enum class HeadGemm { kAbsorbQ, kUpV };
 cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
                              int32_t T, int32_t* err, cudaStream_t stream);
 

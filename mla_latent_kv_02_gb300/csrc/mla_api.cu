@@ -676,11 +676,9 @@ mla_status mla_expand_kv(const void* rows, int32_t n, const void* w_uk, const vo
   const uint32_t vbox[3] = {64, 64, 1};
   s = make_map(&vmap, w_uv, 3, vdims, vstr, vbox, "W_UV");
   if (s != MLA_OK) return s;
-  cudaError_t e = mla::launch_head_gemm(mla::HeadGemm::kExpandK, amap, kmap, (uint16_t*)k_c, n, dev_err,
+  cudaError_t e = mla::launch_expand_kv(amap, kmap, vmap, (uint16_t*)k_c, (uint16_t*)v_c, n, dev_err,
                                         (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "expand K launch");
-  e = mla::launch_head_gemm(mla::HeadGemm::kExpandV, amap, vmap, (uint16_t*)v_c, n, dev_err, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "expand V launch");
+  if (e != cudaSuccess) return cuda_fail(e, "expand_kv launch");
   return MLA_OK;
 }
 
