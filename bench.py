@@ -453,40 +453,73 @@ def run_mla(args):
     if api.mla_check(dev_err) != 0:
         raise RuntimeError("device error word set during the timed steps")
 
-    # ---- end to end through the API: pinned host inputs in, result out, plan rebuilt each step
+    # ---- end to end through the API: pinned host inputs in, result out, plan rebuilt each step.
+    # Two steps in flight, as a serving loop runs: the host plans and enqueues
+    # step i+1 before it waits for step i's result and reads it; the copies
+    # in and out run on their own stream (double-buffered device inputs and
+    # outputs), so they overlap the neighbouring steps' kernels.
     h_q_c = torch.from_numpy(case.q_c).to(torch.bfloat16).pin_memory()
     h_q_r = torch.from_numpy(case.q_r).to(torch.bfloat16).pin_memory()
     h_c_new = c_new.cpu().pin_memory()
     h_k_new = k_new.cpu().pin_memory()
     h_slots = slots_new.cpu().pin_memory()
-    h_out = torch.empty((T, 128, 128), dtype=torch.bfloat16).pin_memory()
-    d_q_c, d_q_r = torch.empty_like(q_c), torch.empty_like(q_r)
-    d_c_new, d_k_new, d_slots = torch.empty_like(c_new), torch.empty_like(k_new), torch.empty_like(slots_new)
+    h_out = [torch.empty((T, 128, 128), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d_in = [(torch.empty_like(q_c), torch.empty_like(q_r), torch.empty_like(c_new), torch.empty_like(k_new),
+             torch.empty_like(slots_new)) for _ in range(2)]
+    d_out = [torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (h_q_c, h_q_r, h_c_new, h_k_new, h_slots))
-    d2h = h_out.numel() * h_out.element_size()
+    d2h = h_out[0].numel() * h_out[0].element_size()
+    copy_stream = torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of slot s landed
+    ev_used = [torch.cuda.Event() for _ in range(2)]   # the kernels of slot s are done with its buffers
+    ev_done = [torch.cuda.Event() for _ in range(2)]   # slot s's result is on the host
+    for e in ev_used:
+        e.record(stream)
+    checksum = [0.0]
+    e2e_plans = [api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, num_clusters=plan.num_clusters)
+                 for _ in range(2)]
 
-    def e2e_step():
-        d_q_c.copy_(h_q_c, non_blocking=True)
-        d_q_r.copy_(h_q_r, non_blocking=True)
-        d_c_new.copy_(h_c_new, non_blocking=True)
-        d_k_new.copy_(h_k_new, non_blocking=True)
-        d_slots.copy_(h_slots, non_blocking=True)
-        p = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, num_clusters=plan.num_clusters)
-        api.mla_kv_append(d_c_new, d_k_new, d_slots, kv, dev_err)
-        api.mla_absorb_q(d_q_c, w_uk, q_abs, dev_err)
-        api.mla_decode_paged(q_abs, d_q_r, kv, bt, p, o_lat, dev_err, lse=lse, scale=SCALE)
-        api.mla_up_v(o_lat, w_uv, out, dev_err)
-        h_out.copy_(out, non_blocking=True)
-        torch.cuda.current_stream(dev).synchronize()
+    def e2e_issue(i):
+        sl = i % 2
+        dq_c, dq_r, dc_new, dk_new, dslots = d_in[sl]
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_used[sl])
+            dq_c.copy_(h_q_c, non_blocking=True)
+            dq_r.copy_(h_q_r, non_blocking=True)
+            dc_new.copy_(h_c_new, non_blocking=True)
+            dk_new.copy_(h_k_new, non_blocking=True)
+            dslots.copy_(h_slots, non_blocking=True)
+            ev_in[sl].record(copy_stream)
+        # the plan is rebuilt every step into its slot's pinned buffer: that
+        # slot's previous step has finished (its result was collected)
+        p = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, into=e2e_plans[sl])
+        stream.wait_event(ev_in[sl])
+        api.mla_kv_append(dc_new, dk_new, dslots, kv, dev_err)
+        api.mla_absorb_q(dq_c, w_uk, q_abs, dev_err)
+        api.mla_decode_paged(q_abs, dq_r, kv, bt, p, o_lat, dev_err, lse=lse, scale=SCALE)
+        api.mla_up_v(o_lat, w_uv, d_out[sl], dev_err)
+        ev_used[sl].record(stream)
+        with torch.cuda.stream(copy_stream):
+            copy_stream.wait_event(ev_used[sl])
+            h_out[sl].copy_(d_out[sl], non_blocking=True)
+            ev_done[sl].record(copy_stream)
 
-    for _ in range(max(1, args.warmup)):
-        e2e_step()
+    def e2e_collect(i):
+        ev_done[i % 2].synchronize()
+        checksum[0] += float(h_out[i % 2][0, 0, 0])   # the host reads this step's result
+
+    def e2e_run(n):
+        for i in range(n):
+            e2e_issue(i)
+            if i > 0:
+                e2e_collect(i - 1)
+        e2e_collect(n - 1)
+
+    e2e_run(max(2, args.warmup))
     barrier(ws)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
-    for _ in range(K):
-        e2e_step()
-    torch.cuda.synchronize(dev)
+    e2e_run(K)
     e2e_s = reduce_max(time.perf_counter() - t0, ws, dev)
     if api.mla_check(dev_err) != 0:
         raise RuntimeError("device error word set during the end-to-end steps")
@@ -540,7 +573,7 @@ def run_mla(args):
             "algorithmic": {"flops": st["flops"], "bytes": st["bytes"]},
         },
         "e2e": {"value": round(tokens * K / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h), "steps_in_flight": 2},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "rows": rows,

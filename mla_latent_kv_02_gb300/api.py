@@ -350,6 +350,7 @@ class DecodePlan:
     plan: torch.Tensor          # int32 device buffer
     info: mla_plan_info
     workspace: torch.Tensor     # uint8 device buffer
+    host: Optional[torch.Tensor] = None   # pinned int32 staging of the plan (reused by `into=`)
 
     @property
     def num_clusters(self) -> int:
@@ -357,22 +358,38 @@ class DecodePlan:
 
 
 def mla_decode_plan(seq_lens: Sequence[int], q_lens: Sequence[int], device=None, num_clusters: Optional[int] = None,
-                    stream=None) -> DecodePlan:
+                    stream=None, into: Optional[DecodePlan] = None) -> DecodePlan:
+    """Plan on the host into a pinned buffer and upload it with an
+    asynchronous copy on `stream` (a copy from pageable memory would make
+    the host wait for the stream).  `into` reuses a previous plan's buffers
+    when they are large enough; the caller must not reuse a plan whose
+    previous upload or decode may still be running."""
     sl = np.ascontiguousarray(seq_lens, dtype=np.int32)
     ql = np.ascontiguousarray(q_lens, dtype=np.int32)
     T = int(ql.sum()) if ql.size else 0
     if num_clusters is None:
-        num_clusters = mla_decode_max_clusters()
+        num_clusters = into.num_clusters if into is not None else mla_decode_max_clusters()
     nbytes = mla_decode_plan_bytes(T, num_clusters)
+    words = (nbytes + 15) // 16 * 4
     device = device or torch.device("cuda", torch.cuda.current_device())
-    plan = torch.zeros((nbytes + 15) // 16 * 4, dtype=torch.int32, device=device)
+    ws_bytes = max(mla_decode_workspace_size(num_clusters), 16)
+    if (into is not None and into.host is not None and into.plan.numel() >= words
+            and into.workspace.numel() >= ws_bytes and into.plan.device == torch.device(device)):
+        plan, ws, host = into.plan, into.workspace, into.host
+    else:
+        plan = torch.empty(words, dtype=torch.int32, device=device)
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+        host = torch.zeros(words, dtype=torch.int32).pin_memory()
     info = mla_plan_info()
     P32 = C.POINTER(C.c_int32)
-    _check(lib().mla_decode_plan(sl.ctypes.data_as(P32), ql.ctypes.data_as(P32), int(sl.size), int(num_clusters),
-                                 _ptr(plan), nbytes, C.byref(info), _stream(stream)))
-    ws_bytes = mla_decode_workspace_size(num_clusters)
-    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=device)
-    return DecodePlan(plan=plan, info=info, workspace=ws)
+    _check(lib().mla_decode_plan_host(sl.ctypes.data_as(P32), ql.ctypes.data_as(P32), int(sl.size),
+                                      int(num_clusters), C.c_void_p(host.data_ptr()), nbytes, C.byref(info)))
+    if stream is None:
+        plan[:words].copy_(host[:words], non_blocking=True)
+    else:
+        with torch.cuda.stream(stream):
+            plan[:words].copy_(host[:words], non_blocking=True)
+    return DecodePlan(plan=plan, info=info, workspace=ws, host=host)
 
 
 def mla_decode_paged(q_abs, q_r, kv_cache, block_table, plan: DecodePlan, o_lat, dev_err, lse=None,
