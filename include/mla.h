@@ -72,6 +72,7 @@ typedef enum mla_status {
 #define MLA_DEVERR_TIMEOUT 4u  /* an mbarrier wait exceeded its limit; the kernel stopped early */
 #define MLA_DEVERR_PLAN 8u     /* the plan buffer is not a valid decode plan */
 #define MLA_DEVERR_POS_OOB 16u /* RoPE position outside [0, max_pos): that token / row skipped */
+#define MLA_DEVERR_FP8_RANGE 32u /* FP8 decode: a token scale outside [2^-15, 2^7]; that row was clamped */
 
 /* Thread-local message of the last failing call (never NULL). */
 const char* mla_last_error(void);
@@ -431,11 +432,14 @@ mla_status mla_gather_paged_fp8(const void* rows, const float* scales, int64_t n
 
 /*
  * Steps A3 and A4 over the FP8 cache: as mla_decode_paged with kv_cache
- * replaced by (rows, scales) above.  The latent is dequantised exactly to
- * bf16 on chip (code * 2^k), so the attention sees the same values the
- * dequantising gather returns; the same plan and workspace serve both
- * formats.  Every slot read must hold finite codes (E4M3 NaN codes are never
- * written by mla_kv_append_fp8) and a power-of-two scale.
+ * replaced by (rows, scales) above.  The tensor-core operands are f16: the
+ * latent is dequantised exactly on chip (code * 2^k is an exact f16 while
+ * 2^-15 <= 2^k <= 2^7, i.e. max|c| of a token in [448 * 2^-16, 448 * 2^7];
+ * all-zero tokens have k = 0), q_abs, q_R and the RoPE key are rounded from
+ * bf16 to f16, and P is f16.  A token whose scale is outside that range is
+ * clamped to it and sets MLA_DEVERR_FP8_RANGE.  The same plan and workspace
+ * serve both formats.  Every slot read must hold finite codes (E4M3 NaN
+ * codes are never written by mla_kv_append_fp8) and a power-of-two scale.
  */
 mla_status mla_decode_paged_fp8(const void* q_abs, const void* q_r, const void* rows, const float* scales,
                                 int64_t num_pages, const int32_t* block_table, int32_t max_pages,

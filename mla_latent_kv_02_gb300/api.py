@@ -21,7 +21,7 @@ D_QK = D_C + D_R
 
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_MISALIGNED", 3: "MLA_ERR_UNSUPPORTED",
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE", 6: "MLA_ERR_TIMEOUT", 7: "MLA_ERR_NO_SPACE"}
-DEVERR_PAGE_OOB, DEVERR_SLOT_OOB, DEVERR_TIMEOUT, DEVERR_PLAN, DEVERR_POS_OOB = 1, 2, 4, 8, 16
+DEVERR_PAGE_OOB, DEVERR_SLOT_OOB, DEVERR_TIMEOUT, DEVERR_PLAN, DEVERR_POS_OOB, DEVERR_FP8_RANGE = 1, 2, 4, 8, 16, 32
 
 
 class MlaError(RuntimeError):

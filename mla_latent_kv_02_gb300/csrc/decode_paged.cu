@@ -161,9 +161,14 @@ constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 4
 constexpr bool kIssueSuspend = false;
 constexpr uint32_t kTileThreads = 128;                    // the warpgroup that handles one tile
 
-constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 64, false, false);
-constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 256, false, true);
-constexpr uint32_t kIdescSum = idesc_bf16_f32(128, 16, false, false);
+// bf16 operands for the bf16 cache; f16 for the FP8 cache (an E4M3 value is
+// an exact f16, and P is computed in f16 in both).
+template <bool kF8>
+struct Idesc {
+  static constexpr uint32_t kQK = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
+  static constexpr uint32_t kPV = kF8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
+  static constexpr uint32_t kSum = kF8 ? idesc_f16_f32(128, 16, false, false) : idesc_bf16_f32(128, 16, false, false);
+};
 
 // Walks the 64-token tiles of a cluster's segments in order; a segment's
 // fields are read from the plan once, when the cursor enters it.
@@ -218,6 +223,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
                 B_O_DONE0 = L::B_O_DONE0, B_O_DONE1 = L::B_O_DONE1, B_Q_READY = L::B_Q_READY,
                 B_O_FREE = L::B_O_FREE, B_X_FULL0 = L::B_X_FULL0, B_DRAIN = L::B_DRAIN, B_DRAIN_PV = L::B_DRAIN_PV,
                 B_F8_FULL = L::B_F8_FULL;
+  constexpr uint32_t kIdescQK = Idesc<kF8>::kQK, kIdescPV = Idesc<kF8>::kPV, kIdescSum = Idesc<kF8>::kSum;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t bars = raw + kSmallBar;
@@ -279,7 +285,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
   for (int i = threadIdx.x; i < 4 * kH; i += kThreads) st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
   if (layout_fits) {
     uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + kOffOnes);
-    for (int i = threadIdx.x; i < kOnesBytes / 4; i += kThreads) ones[i] = 0x3F803F80u;  // bf16 1.0 pairs
+    const uint32_t one2 = kF8 ? 0x3C003C00u : 0x3F803F80u;  // f16 / bf16 1.0 pairs
+    for (int i = threadIdx.x; i < kOnesBytes / 4; i += kThreads) ones[i] = one2;
     fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
@@ -442,8 +449,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     // ---------------------------------------------------------------- FP8 converters
     // Tile t, stage t mod kStages.  Warp cw takes token rows cw, cw+4, ...;
     // lane l the row's output chunk l (latent dims 8l..8l+7 of this CTA's
-    // half): 8 codes in, one 16-byte bf16 chunk out, written in the 128-byte
-    // swizzled layout the tensor core reads.  The bf16 rows overwrite the
+    // half): 8 codes in, one 16-byte f16 chunk out, written in the 128-byte
+    // swizzled layout the tensor core reads.  The f16 rows overwrite the
     // codes, so every converter thread reads all of its codes first and the
     // four warps meet at a named barrier before the first store.
     const int cw = warp - kConvWarp0;
@@ -451,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
     const uint32_t ct = (uint32_t)lane >> 3, cc = (uint32_t)lane & 7u;
     constexpr int kRows = kPage / kConvWarps;
-    constexpr int kBatch = 8;
+    constexpr int kBatch = 4;
     for (uint32_t t = 0; t < G; ++t) {
       const uint32_t st = t % kStages;
       const bool w = wait_phase<false, true>(BAR(B_F8_FULL + st), (t / kStages) & 1u, err, abort_flag);
@@ -470,45 +477,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
         code[j] = ld_shared_v2(stage + r * 256u + (uint32_t)lane * 8u);
         scale[j] = ld_shared_f32(stage + kF8ScaleOff + 4u * r);
       }
-      // Rows whose scale leaves [2^-126, 2^15] take the general two-multiply
-      // path; the common case is one conversion and one multiply per pair,
-      // issued kBatch rows at a time so that one warp keeps many in flight.
-      bool fast = true;
+      // f16 operands: one conversion (exact) and one multiply by the row's
+      // 2^k per pair, issued kBatch rows at a time so that one warp keeps
+      // many in flight.  A scale outside [2^-15, 2^7] is clamped and flagged.
+      uint32_t fac[kRows];
+      bool in_range = true;
 #pragma unroll
-      for (int j = 0; j < kRows; ++j) fast = fast && fp8_fast_scale(scale[j]);
+      for (int j = 0; j < kRows; ++j) {
+        bool ok_j;
+        fac[j] = fp8_f16_factor(scale[j], ok_j);
+        in_range = in_range && ok_j;
+      }
+      if (!in_range && lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_FP8_RANGE);  // warp-uniform
       named_bar_sync(kConvBarrier, kConvWarps * 32);
-      if (fast) {
 #pragma unroll
-        for (int j0 = 0; j0 < kRows; j0 += kBatch) {
-          uint32_t h[kBatch][4];
+      for (int j0 = 0; j0 < kRows; j0 += kBatch) {
+        uint32_t h[kBatch][4];
 #pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            h[j][0] = e4m3x2_to_f16x2(code[j0 + j].x & 0xFFFFu);
-            h[j][1] = e4m3x2_to_f16x2(code[j0 + j].x >> 16);
-            h[j][2] = e4m3x2_to_f16x2(code[j0 + j].y & 0xFFFFu);
-            h[j][3] = e4m3x2_to_f16x2(code[j0 + j].y >> 16);
-          }
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            const uint32_t f = fp8_fast_factor(scale[j0 + j]);
-#pragma unroll
-            for (int q = 0; q < 4; ++q) h[j][q] = mul_bf16x2(f16x2_to_bf16_pattern(h[j][q]), f);
-          }
-#pragma unroll
-          for (int j = 0; j < kBatch; ++j) {
-            const uint32_t r = (uint32_t)(kConvWarps * (j0 + j) + cw);
-            st_shared_v4(stage + ct * kChunkBytes + r * 128u + ((cc ^ (r & 7u)) << 4), h[j][0], h[j][1], h[j][2],
-                         h[j][3]);
-          }
+        for (int j = 0; j < kBatch; ++j) {
+          h[j][0] = e4m3x2_to_f16x2(code[j0 + j].x & 0xFFFFu);
+          h[j][1] = e4m3x2_to_f16x2(code[j0 + j].x >> 16);
+          h[j][2] = e4m3x2_to_f16x2(code[j0 + j].y & 0xFFFFu);
+          h[j][3] = e4m3x2_to_f16x2(code[j0 + j].y >> 16);
         }
-      } else {
-        // fully unrolled: a dynamically indexed code[] or scale[] would live in local memory
 #pragma unroll
-        for (int j = 0; j < kRows; ++j) {
-          const uint32_t r = (uint32_t)(kConvWarps * j + cw);
-          const uint4 o = dequant8(code[j], fp8_row_scale(scale[j]));
-          st_shared_v4(stage + ct * kChunkBytes + r * 128u + ((cc ^ (r & 7u)) << 4), o.x, o.y, o.z, o.w);
+        for (int j = 0; j < kBatch; ++j)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) h[j][q] = mul_f16x2(h[j][q], fac[j0 + j]);
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j) {
+          const uint32_t r = (uint32_t)(kConvWarps * (j0 + j) + cw);
+          st_shared_v4(stage + ct * kChunkBytes + r * 128u + ((cc ^ (r & 7u)) << 4), h[j][0], h[j][1], h[j][2],
+                       h[j][3]);
         }
+      }
+      // the RoPE half (bf16 from the cache) becomes f16 in place: 256 16-byte
+      // chunks, two per thread; an element keeps its place in the swizzled layout
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+        const uint32_t at = stage + kF8RopeOff + (uint32_t)(k * 128 + cw * 32 + lane) * 16u;
+        const float4 v = ld_shared_v4(at);
+        st_shared_v4(at, bf16x2_to_f16x2(__float_as_uint(v.x)), bf16x2_to_f16x2(__float_as_uint(v.y)),
+                     bf16x2_to_f16x2(__float_as_uint(v.z)), bf16x2_to_f16x2(__float_as_uint(v.w)));
       }
       fence_proxy_async_smem();
       __syncwarp();
@@ -562,6 +572,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
             r[4 * j + 2] = v[ci * 8 + j].z;
             r[4 * j + 3] = v[ci * 8 + j].w;
           }
+          if constexpr (kF8) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = bf16x2_to_f16x2(r[j]);
+          }
           tmem_st32(tl + kColQ + half * 64 + ci * 32, r);
         }
         if (half == 0) {
@@ -572,6 +586,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
             r[4 * j + 1] = v[16 + j].y;
             r[4 * j + 2] = v[16 + j].z;
             r[4 * j + 3] = v[16 + j].w;
+          }
+          if constexpr (kF8) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = bf16x2_to_f16x2(r[j]);
           }
           tmem_st16(tl + kColQ + 128, r);
         }
@@ -714,12 +732,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       st_shared_v2_volatile(pair + 8u * ((g & 3u) * kH + h), __float_as_uint(m), g);
 
       // ---- P = 2^(c2 (s - m)) in fp16 pairs (one fused multiply-add for the
-      //      exponent), stored as bf16 for the tensor core
+      //      exponent), stored as bf16 for the tensor core (the FP8 cache's
+      //      f16 operands take the fp16 P as it is)
       const __half2 mc2 = __float2half2_rn(-m * c2);
 #pragma unroll
       for (int j = 0; j < kWords; ++j) {
-        const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hfma2(as_h2(own[j]), c2h, mc2)))));
-        own[j] = pack_bf16x2(p.x, p.y);
+        const uint32_t p16 = ex2_f16x2(as_u32(__hfma2(as_h2(own[j]), c2h, mc2)));
+        if constexpr (kF8) {
+          own[j] = p16;
+        } else {
+          const float2 p = __half22float2(as_h2(p16));
+          own[j] = pack_bf16x2(p.x, p.y);
+        }
       }
       // Writing P (single TMEM buffer) and a rescale both need P·V of tile g-1 done.
       if (g > 0) {

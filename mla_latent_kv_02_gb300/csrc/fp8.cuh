@@ -94,20 +94,30 @@ __device__ __forceinline__ Fp8Scale fp8_row_scale(float s) {
   return r;
 }
 
-// The bf16x2 factor 2^(112+k) of a row whose scale s = 2^k is a normal fp32
-// with k <= 15: the bf16 exponent field is s's exponent field + 112.
-__device__ __forceinline__ uint32_t fp8_fast_factor(float s) {
-  const uint32_t f = ((__float_as_uint(s) >> 23) + 112u) << 7;
+// The decode over the FP8 cache runs its tensor-core operands in f16: an
+// E4M3 value is an exact f16, and code * 2^k stays exact in f16 while
+// 2^-15 <= s = 2^k <= 2^7 (the smallest code 2^-9 * 2^-15 = 2^-24 is f16's
+// smallest subnormal; 448 * 2^7 = 57344 < 65504).  fp8_f16_factor returns
+// the f16x2 splat of s clamped to that range and whether s was inside it.
+__device__ __forceinline__ uint32_t fp8_f16_factor(float s, bool& in_range) {
+  const int e = (int)((__float_as_uint(s) >> 23) & 0xFFu) - 127;  // s = 2^e (normal s)
+  in_range = e >= -15 && e <= 7 && (__float_as_uint(s) & 0x7FFFFFu) == 0u;
+  const int k = e < -15 ? -15 : (e > 7 ? 7 : e);
+  const uint32_t f = k >= -14 ? (uint32_t)(k + 15) << 10 : 0x0200u;  // 2^-15 is the subnormal 0x0200
   return f | (f << 16);
 }
-// True when fp8_fast_factor applies (k in [-126, 15]).
-__device__ __forceinline__ bool fp8_fast_scale(float s) {
-  const uint32_t e = (__float_as_uint(s) >> 23) & 0xFFu;
-  return e != 0u && e <= 142u;
+
+// A bf16 pair to an f16 pair (nearest even, saturating at 65504).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t u) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %2, %1;" : "=r"(r) : "f"(__uint_as_float(u << 16)), "f"(__uint_as_float(u & 0xFFFF0000u)));
+  return r;
 }
-// Shifted f16 pattern of two codes (value * 2^-112 as bf16 bits).
-__device__ __forceinline__ uint32_t f16x2_to_bf16_pattern(uint32_t h) {
-  return ((h >> 3) & 0x0FFF0FFFu) | (h & 0x80008000u);
+
+__device__ __forceinline__ uint32_t mul_f16x2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
 }
 
 // Two codes to two bf16 (one word, low element first), exact.

@@ -330,6 +330,15 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, b
          | ((uint32_t)(M >> 4) << 24);  // M / 16
 }
 
+// kind::f16 with f16 A and B (format 0), fp32 D.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4)                      // D format fp32
+         | ((a_mn ? 1u : 0u) << 15)     // A major
+         | ((b_mn ? 1u : 0u) << 16)     // B major
+         | ((uint32_t)(N >> 3) << 17)   // N / 8
+         | ((uint32_t)(M >> 4) << 24);  // M / 16
+}
+
 #define MLA_R8(p, i) "=r"(p[i]), "=r"(p[i + 1]), "=r"(p[i + 2]), "=r"(p[i + 3]), "=r"(p[i + 4]), "=r"(p[i + 5]), "=r"(p[i + 6]), "=r"(p[i + 7])
 #define MLA_W8(p, i) "r"(p[i]), "r"(p[i + 1]), "r"(p[i + 2]), "r"(p[i + 3]), "r"(p[i + 4]), "r"(p[i + 5]), "r"(p[i + 6]), "r"(p[i + 7])
 

@@ -193,8 +193,10 @@ def test_decode_fp8_split_rows_mtp_and_prefill(api):
 
 
 def test_decode_fp8_matches_decode_on_dequantised_bf16_cache(api):
-    """The FP8 kernel sees exactly the values the dequantising gather returns:
-    the bf16 kernel run on that gathered cache gives bit-identical results."""
+    """The FP8 kernel sees exactly the latent values the dequantising gather
+    returns (its f16 operands differ from the bf16 kernel's only in how q,
+    the RoPE key and P are rounded): the bf16 kernel run on that gathered
+    cache agrees within the floating tolerance."""
     case = wl.make_case([130, 700, 64], [1, 2, 1], seed=61, with_weights=False, with_q_abs=True)
     dc8 = DeviceCase(case, with_weights=False, fp8=True)
     o8, l8, _ = dc8.decode(num_clusters=3)
@@ -208,7 +210,28 @@ def test_decode_fp8_matches_decode_on_dequantised_bf16_cache(api):
         for j in range(n):
             flat[int(pages[j // 64]) * 64 + j % 64] = rows[j]
     o, l, _ = dc.decode(num_clusters=3)
-    assert torch.equal(o8, o) and torch.equal(l8, l)
+    assert_close(to_np(o8), to_np(o).astype(np.float64), "fp8 vs bf16 kernel on the gathered cache")
+    assert_close(l8.cpu().numpy(), l.cpu().numpy().astype(np.float64), "lse", max_frac=2e-3, mean_rel=5e-4)
+
+
+def test_decode_fp8_flags_scales_outside_the_f16_range(api):
+    """A token whose scale leaves [2^-15, 2^7] cannot be an exact f16 operand:
+    the decode clamps it and sets MLA_DEVERR_FP8_RANGE; in-range tokens do not.
+    (A tiny token, max|c| = 1e-3, scale 2^-18: clamping keeps the outputs finite.)"""
+    case = wl.make_case([130], [1], seed=64, with_weights=False, with_q_abs=True)
+    dc = DeviceCase(case, with_weights=False, fp8=True)
+    o, _, _ = dc.decode(num_clusters=2)                     # all in range: no flag (checked inside)
+    tiny = torch.full((1, 512), 1e-3, dtype=torch.bfloat16, device="cuda")
+    api.mla_kv_append_fp8(tiny, torch.zeros((1, 64), dtype=torch.bfloat16, device="cuda"),
+                          torch.tensor([int(dc.slots_all[5])], dtype=torch.int64, device="cuda"), dc.rows, dc.scales,
+                          dc.dev_err)
+    assert api.mla_check(dc.dev_err) == 0                    # the append itself is exact at any scale
+    plan = api.mla_decode_plan(case.seq_lens, case.q_lens, num_clusters=2)
+    o2 = torch.empty_like(o)
+    api.mla_decode_paged_fp8(dc.q_abs, dc.q_r, dc.rows, dc.scales, dc.block_table, plan, o2, dc.dev_err)
+    torch.cuda.synchronize()
+    assert int(dc.dev_err.item()) & api.DEVERR_FP8_RANGE
+    assert torch.isfinite(o2.float()).all()
 
 
 def test_decode_fp8_page_permutation_invariance(api):
