@@ -279,3 +279,41 @@ def test_nvfp4_calls_validate_before_any_launch(api):
     assert lib.mla_gather_paged_nvfp4(ok, f(0.01), 4, ok, 1, 0, 65, ok, err, None) == 1
     assert lib.mla_gather_paged_nvfp4(ok, f(-2.0), 4, ok, 2, 0, 10, ok, err, None) == 1
     assert lib.mla_gather_paged_nvfp4(None, f(0.01), 4, ok, 2, 0, 0, None, None, None) == 0
+
+
+def test_fp8_and_decompress_calls_validate_before_any_launch(api):
+    lib = _lib.lib()
+    P = C.c_void_p
+    ok, odd, err = P(0x10000), P(0x10008), P(0x20000)
+    f = C.c_float
+    # FP8 decode: a zeroed info is not a plan; the scales pointer is required and 16-byte aligned
+    info = _lib.mla_plan_info()
+    assert lib.mla_decode_paged_fp8(ok, ok, ok, ok, 4, ok, 4, ok, C.byref(info), f(0.07), ok, 1 << 20, ok, None,
+                                    err, None) == 1
+    buf, pinfo = api.mla_decode_plan_host([700], [1], 4)
+    assert lib.mla_decode_paged_fp8(ok, ok, ok, None, 64, ok, 11, ok, C.byref(pinfo), f(0.07), ok, 1 << 30, ok, None,
+                                    err, None) == 1
+    assert lib.mla_decode_paged_fp8(ok, ok, ok, odd, 64, ok, 11, ok, C.byref(pinfo), f(0.07), ok, 1 << 30, ok, None,
+                                    err, None) == 2
+    # FP8 append / gather
+    assert lib.mla_kv_append_fp8(ok, ok, ok, 1, ok, odd, 4, err, None) == 2
+    assert lib.mla_kv_append_fp8(ok, ok, ok, -1, ok, ok, 4, err, None) == 1
+    assert lib.mla_gather_paged_fp8(ok, ok, 4, ok, 1, 0, 65, ok, err, None) == 1
+    # expansion and prefill attention
+    assert lib.mla_expand_kv(None, 0, None, None, None, None, None, None) == 0
+    assert lib.mla_expand_kv(ok, -1, ok, ok, ok, ok, err, None) == 1
+    assert lib.mla_expand_kv(ok, 10, ok, ok, odd, ok, err, None) == 2
+    assert lib.mla_prefill_attention(ok, ok, 0, ok, ok, ok, 10, f(0.07), ok, err, None) == 0
+    assert lib.mla_prefill_attention(ok, ok, 11, ok, ok, ok, 10, f(0.07), ok, err, None) == 1   # M > N
+    assert lib.mla_prefill_attention(ok, ok, 5, ok, ok, ok, 10, f(-1.0), ok, err, None) == 1
+    assert lib.mla_prefill_attention(ok, odd, 5, ok, ok, ok, 10, f(0.07), ok, err, None) == 2
+    # the whole branch: M > N, short workspace
+    ws = C.c_size_t()
+    assert lib.mla_prefill_workspace_size(100, C.byref(ws)) == 0
+    assert ws.value == (100 * 1152 + 15) // 16 * 16 + 2 * 100 * 128 * 128 * 2
+    assert lib.mla_prefill_decompress(ok, ok, 60, ok, 4, ok, 2, 0, 50, ok, ok, f(0.07), ok, ws.value, ok, err,
+                                      None) == 1
+    assert lib.mla_prefill_decompress(ok, ok, 20, ok, 4, ok, 2, 0, 100, ok, ok, f(0.07), ok, 100, ok, err,
+                                      None) == 1
+    assert "workspace" in lib.mla_last_error().decode()
+    assert lib.mla_branch_for(300) == 1 and lib.mla_branch_for(10) == 0 and lib.mla_prefill_threshold() == 256
