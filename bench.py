@@ -456,8 +456,9 @@ def run_mla(args):
     # ---- end to end through the API: pinned host inputs in, result out, plan rebuilt each step.
     # Two steps in flight, as a serving loop runs: the host plans and enqueues
     # step i+1 before it waits for step i's result and reads it; the copies
-    # in and out run on their own stream (double-buffered device inputs and
-    # outputs), so they overlap the neighbouring steps' kernels.
+    # in and the copies out run on two streams of their own (double-buffered
+    # device inputs and outputs), so that step i+1's inputs never queue behind
+    # step i's result and both overlap the neighbouring steps' kernels.
     h_q_c = torch.from_numpy(case.q_c).to(torch.bfloat16).pin_memory()
     h_q_r = torch.from_numpy(case.q_r).to(torch.bfloat16).pin_memory()
     h_c_new = c_new.cpu().pin_memory()
@@ -469,7 +470,8 @@ def run_mla(args):
     d_out = [torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (h_q_c, h_q_r, h_c_new, h_k_new, h_slots))
     d2h = h_out[0].numel() * h_out[0].element_size()
-    copy_stream = torch.cuda.Stream(device=dev)
+    in_stream = torch.cuda.Stream(device=dev)
+    out_stream = torch.cuda.Stream(device=dev)
     ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of slot s landed
     ev_used = [torch.cuda.Event() for _ in range(2)]   # the kernels of slot s are done with its buffers
     ev_done = [torch.cuda.Event() for _ in range(2)]   # slot s's result is on the host
@@ -482,14 +484,14 @@ def run_mla(args):
     def e2e_issue(i):
         sl = i % 2
         dq_c, dq_r, dc_new, dk_new, dslots = d_in[sl]
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(ev_used[sl])
+        with torch.cuda.stream(in_stream):
+            in_stream.wait_event(ev_used[sl])
             dq_c.copy_(h_q_c, non_blocking=True)
             dq_r.copy_(h_q_r, non_blocking=True)
             dc_new.copy_(h_c_new, non_blocking=True)
             dk_new.copy_(h_k_new, non_blocking=True)
             dslots.copy_(h_slots, non_blocking=True)
-            ev_in[sl].record(copy_stream)
+            ev_in[sl].record(in_stream)
         # the plan is rebuilt every step into its slot's pinned buffer: that
         # slot's previous step has finished (its result was collected)
         p = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, into=e2e_plans[sl])
@@ -499,10 +501,10 @@ def run_mla(args):
         api.mla_decode_paged(q_abs, dq_r, kv, bt, p, o_lat, dev_err, lse=lse, scale=SCALE)
         api.mla_up_v(o_lat, w_uv, d_out[sl], dev_err)
         ev_used[sl].record(stream)
-        with torch.cuda.stream(copy_stream):
-            copy_stream.wait_event(ev_used[sl])
+        with torch.cuda.stream(out_stream):
+            out_stream.wait_event(ev_used[sl])
             h_out[sl].copy_(d_out[sl], non_blocking=True)
-            ev_done[sl].record(copy_stream)
+            ev_done[sl].record(out_stream)
 
     def e2e_collect(i):
         ev_done[i % 2].synchronize()

@@ -797,15 +797,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
                   pack_bf16x2(__uint_as_float(o[8 * v + 6]) * inv, __uint_as_float(o[8 * v + 7]) * inv));
           }
         } else {
+          // Partials are read once, by the combine right after this kernel: kept
+          // in L2 with evict-last priority through the rest of the KV stream.
           float4* dst = reinterpret_cast<float4*>(a.part_o + ((size_t)slot * kH + h) * kDC + rank * 256);
+          const uint64_t keep = l2_policy_evict_last();
 #pragma unroll 1
           for (int c = 0; c < 256; c += 32) {
             uint32_t o[32];
             tmem_ld32_sync(tl + kColO + c, o);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
-              dst[c / 4 + v] = make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
-                                           __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv);
+              st_global_v4_hint(dst + c / 4 + v,
+                                make_float4(__uint_as_float(o[4 * v]) * inv, __uint_as_float(o[4 * v + 1]) * inv,
+                                            __uint_as_float(o[4 * v + 2]) * inv, __uint_as_float(o[4 * v + 3]) * inv),
+                                keep);
           }
         }
         tc_fence_before();
@@ -870,9 +875,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const CombineArgs a) {
   for (int i = 0; i < n; ++i) mx = fmaxf(mx, __ldg(a.part_lse + (size_t)(s0 + i) * kH + h));
   float wsum = 0.f;
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  const uint64_t last_use = l2_policy_evict_first();  // the partials' only read
   for (int i = 0; i < n; ++i) {
     const float w = exp2f(__ldg(a.part_lse + (size_t)(s0 + i) * kH + h) - mx);
-    const float4 v = __ldg(reinterpret_cast<const float4*>(a.part_o + ((size_t)(s0 + i) * kH + h) * kDC) + tid);
+    const float4 v =
+        ld_global_v4_hint(reinterpret_cast<const float4*>(a.part_o + ((size_t)(s0 + i) * kH + h) * kDC) + tid, last_use);
     wsum += w;
     acc.x += w * v.x;
     acc.y += w * v.y;

@@ -9,7 +9,9 @@
 // K-chunk of the latent is loaded once for both outputs and both W tiles
 // once for both token halves, so a CTA moves 512 KB for 67 MFLOP.  Warp 0
 // lane 0 issues TMA, warp 1 lane 0 the MMAs; all four warps run the
-// epilogue (thread = token row = TMEM lane).
+// epilogue (thread = token row = TMEM lane), which rounds each accumulator
+// to bf16 into the drained ring as two 128-token x 64-column boxes in the
+// TMA's 128-byte-swizzled layout and writes each with one TMA store.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -34,12 +36,16 @@ static_assert(kSmem <= 232448, "shared memory layout does not fit");
 constexpr uint32_t kIdescK = idesc_bf16_f32(128, 128, false, false);  // W_UK read K-major
 constexpr uint32_t kIdescV = idesc_bf16_f32(128, 128, false, true);   // W_UV read MN-major
 
+constexpr int kBoxBytes = 128 * 64 * 2;         // one [128 tokens x 64] bf16 output box
+static_assert(8 * kBoxBytes <= kStages * kStage, "the output boxes are staged in the drained ring");
+
 // a_map: latent rows {512, 1, n} (box 64 x 1 x 128); k_map: W_UK {512, 128, 128 heads}
-// (box 64 x 128 x 1); v_map: W_UV {128, 512, 128 heads} (box 64 x 64 x 1).
+// (box 64 x 128 x 1); v_map: W_UV {128, 512, 128 heads} (box 64 x 64 x 1);
+// kc_map / vc_map: K_c and V_c {128, n, 128 heads} (box 64 x 128 x 1, stores).
 __global__ void __launch_bounds__(128, 1)
     expand_kv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap k_map,
-                     const __grid_constant__ CUtensorMap v_map, uint16_t* __restrict__ k_c,
-                     uint16_t* __restrict__ v_c, int32_t n, int32_t* err) {
+                     const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap kc_map,
+                     const __grid_constant__ CUtensorMap vc_map, int32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -77,6 +83,8 @@ __global__ void __launch_bounds__(128, 1)
       prefetch_tmap(&a_map);
       prefetch_tmap(&k_map);
       prefetch_tmap(&v_map);
+      prefetch_tmap(&kc_map);
+      prefetch_tmap(&vc_map);
       int issued = 0;
       for (int kc = 0; kc < kKCh; ++kc) {
         const int st = kc % kStages, use = kc / kStages;
@@ -126,32 +134,38 @@ __global__ void __launch_bounds__(128, 1)
     __syncwarp();
   }
 
-  // Epilogue: thread = token row of each 128-token half, all four warps.
+  // Epilogue: thread = token row of each 128-token half, all four warps; the
+  // decision to store is the whole CTA's, since a box holds every warp's rows.
   bool w = wait_phase(done, 0, err, abort_flag) && !*abort_flag;
-  w = __all_sync(0xffffffffu, w);
+  w = __syncthreads_and(w) != 0;
   tc_fence_after();
   if (w) {
+    // Every MMA has completed (done), so no load is in flight and the ring is free.
+    const uint32_t r = (uint32_t)(warp * 32 + lane);
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
     for (int q = 0; q < 4; ++q) {              // K rows 0-127, V rows 0-127, K rows 128-255, V rows 128-255
-      const int t = m0 + (q >> 1) * 128 + warp * 32 + lane;
-      uint16_t* outp = (q & 1) ? v_c : k_c;
-      uint4* dst = reinterpret_cast<uint4*>(outp + ((size_t)h * n + t) * 128);
-#pragma unroll 1
-      for (int col = 0; col < 128; col += 32) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32_sync(tl + q * 128 + col, r);
-        if (t < n) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v)
-            dst[col / 8 + v] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
-                                          pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-                                          pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-                                          pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+      for (int b = 0; b < 2; ++b) {
+        const uint32_t box = base + (q * 2 + b) * kBoxBytes;
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          uint32_t v[32];
+          tmem_ld32_sync(tl + q * 128 + b * 64 + hf * 32, v);
+          stage_row_bf16_sw128(box, r, hf, v);
         }
       }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        const CUtensorMap* out = (q & 1) ? &vc_map : &kc_map;
+        const int t0 = m0 + (q >> 1) * 128;
+        tma_store_3d(out, base + (q * 2) * kBoxBytes, 0, t0, h);
+        tma_store_3d(out, base + (q * 2 + 1) * kBoxBytes, 64, t0, h);
+        bulk_commit_group();
+      }
     }
+    if (threadIdx.x == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -165,13 +179,14 @@ __global__ void __launch_bounds__(128, 1)
 }  // namespace expand
 
 cudaError_t launch_expand_kv(const CUtensorMap& a_map, const CUtensorMap& k_map, const CUtensorMap& v_map,
-                             uint16_t* k_c, uint16_t* v_c, int32_t n, int32_t* err, cudaStream_t stream) {
+                             const CUtensorMap& kc_map, const CUtensorMap& vc_map, int32_t n, int32_t* err,
+                             cudaStream_t stream) {
   if (n <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(expand::expand_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        expand::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((n + expand::kM - 1) / expand::kM, 128);
-  expand::expand_kv_kernel<<<grid, 128, expand::kSmem, stream>>>(a_map, k_map, v_map, k_c, v_c, n, err);
+  expand::expand_kv_kernel<<<grid, 128, expand::kSmem, stream>>>(a_map, k_map, v_map, kc_map, vc_map, err);
   return cudaGetLastError();
 }
 

@@ -9,9 +9,13 @@
 // column blocks: D[128 x N/NSPLIT] fp32 in TMEM, A (activation rows,
 // K-major) and W (row-major [K x N], read as an MN-major operand) staged by
 // TMA with 128-byte swizzle through a K-chunk ring.  When split, two CTAs
-// fit on an SM, so one CTA's stores overlap another's loads.  Rows past T are zero-filled
-// by TMA and never stored.  For small T the kernel streams the 16 MiB of
-// weights once (HBM bound).
+// fit on an SM, so one CTA's stores overlap another's loads.  The epilogue
+// rounds D to bf16 into the drained ring, one 64-column box at a time in the
+// TMA's 128-byte-swizzled layout, and writes each box with one TMA store
+// (whole 128-byte lines; a thread-per-row store would put 32 rows, 128 KiB
+// apart, in every warp instruction).  Rows past T are zero-filled by the
+// loads and clipped by the stores.  For small T the kernel streams the
+// 16 MiB of weights once (HBM bound).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -39,12 +43,14 @@ struct Cfg {
   static constexpr uint32_t kIdesc = idesc_bf16_f32(128, kMmaN, false, true);
   static_assert((NSPLIT == 1 ? 1 : 2) * kSmem <= 232448, "a split head GEMM needs two CTAs per SM");
   static_assert(kNC % 64 == 0 && kNC >= 64, "column block is a multiple of 64");
+  static constexpr int kBoxBytes = 128 * 64 * 2;  // one [128 x 64] bf16 output box
+  static_assert((kNC / 64) * kBoxBytes <= STAGES * kStage, "the output boxes are staged in the drained ring");
 };
 
 template <int N, int K, int STAGES, int NSPLIT>
 __global__ void __launch_bounds__(128, 2)
     head_gemm_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
-                     uint16_t* __restrict__ c, int32_t T, int32_t* err) {
+                     const __grid_constant__ CUtensorMap c_map, int32_t* err) {
   using C = Cfg<N, K, STAGES, NSPLIT>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -83,6 +89,7 @@ __global__ void __launch_bounds__(128, 2)
     if (lane == 0) {
       prefetch_tmap(&a_map);
       prefetch_tmap(&w_map);
+      prefetch_tmap(&c_map);
       int issued = 0;
       for (int kc = 0; kc < C::kKCh; ++kc) {
         const int st = kc % STAGES, use = kc / STAGES;
@@ -126,28 +133,32 @@ __global__ void __launch_bounds__(128, 2)
     __syncwarp();
   }
 
-  // Epilogue: thread = output row (TMEM lane), all four warps.
+  // Epilogue: thread = tile row (TMEM lane), all four warps; the decision to
+  // store is taken by the whole CTA, since the boxes need every warp's rows.
   bool w = wait_phase(done, 0, err, abort_flag) && !*abort_flag;
-  w = __all_sync(0xffffffffu, w);
+  w = __syncthreads_and(w) != 0;
   tc_fence_after();
   if (w) {
-    const int t = m0 + warp * 32 + lane;
+    // Every MMA has completed (done), so no load is in flight and the ring is free.
+    const uint32_t r = (uint32_t)(warp * 32 + lane);
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-    uint4* dst = reinterpret_cast<uint4*>(c + ((size_t)t * 128 + h) * N + n0);
 #pragma unroll 1
-    for (int col = 0; col < C::kNC; col += 32) {
-      uint32_t r[32];
-      __syncwarp();
-      tmem_ld32_sync(tl + col, r);
-      if (t < T) {
+    for (int b = 0; b < C::kNC / 64; ++b) {
+      const uint32_t box = base + b * C::kBoxBytes;
 #pragma unroll
-        for (int v = 0; v < 4; ++v)
-          dst[col / 8 + v] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * v]), __uint_as_float(r[8 * v + 1])),
-                                        pack_bf16x2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3])),
-                                        pack_bf16x2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5])),
-                                        pack_bf16x2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7])));
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t v[32];
+        tmem_ld32_sync(tl + b * 64 + hf * 32, v);
+        stage_row_bf16_sw128(box, r, hf, v);
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        tma_store_3d(&c_map, box, n0 + b * 64, h, m0);
+        bulk_commit_group();
       }
     }
+    if (threadIdx.x == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -159,23 +170,23 @@ __global__ void __launch_bounds__(128, 2)
 }
 
 template <int N, int K, int STAGES, int NSPLIT>
-cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c, int32_t T, int32_t* err,
-                cudaStream_t stream) {
+cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, const CUtensorMap& c_map, int32_t T,
+                int32_t* err, cudaStream_t stream) {
   using C = Cfg<N, K, STAGES, NSPLIT>;
   auto* kern = head_gemm_kernel<N, K, STAGES, NSPLIT>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
   if (e != cudaSuccess) return e;
   dim3 grid((T + 127) / 128, 128, NSPLIT);
-  kern<<<grid, 128, C::kSmem, stream>>>(a_map, w_map, c, T, err);
+  kern<<<grid, 128, C::kSmem, stream>>>(a_map, w_map, c_map, err);
   return cudaGetLastError();
 }
 
 }  // namespace gemm
 
-cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
-                             int32_t T, int32_t* err, cudaStream_t stream) {
-  if (kind == HeadGemm::kAbsorbQ) return gemm::run<512, 128, 2, 2>(a_map, w_map, c, T, err, stream);
-  return gemm::run<128, 512, 4, 1>(a_map, w_map, c, T, err, stream);
+cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map,
+                             const CUtensorMap& c_map, int32_t T, int32_t* err, cudaStream_t stream) {
+  if (kind == HeadGemm::kAbsorbQ) return gemm::run<512, 128, 2, 2>(a_map, w_map, c_map, T, err, stream);
+  return gemm::run<128, 512, 4, 1>(a_map, w_map, c_map, T, err, stream);
 }
 
 }  // namespace mla

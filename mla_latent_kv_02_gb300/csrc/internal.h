@@ -122,7 +122,8 @@ cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int
 
 // Decompress-branch expansion: K_c and V_c in one pass (head-major outputs).
 cudaError_t launch_expand_kv(const CUtensorMap& a_map, const CUtensorMap& k_map, const CUtensorMap& v_map,
-                             uint16_t* k_c, uint16_t* v_c, int32_t n, int32_t* err, cudaStream_t stream);
+                             const CUtensorMap& kc_map, const CUtensorMap& vc_map, int32_t n, int32_t* err,
+                             cudaStream_t stream);
 int prefill_smem_bytes();
 cudaError_t launch_prefill_attn(const CUtensorMap& q_map, const CUtensorMap& r_map, const CUtensorMap& k_map,
                                 const CUtensorMap& kr_map, const CUtensorMap& v_map, const PrefillArgs& args,
@@ -130,7 +131,7 @@ cudaError_t launch_prefill_attn(const CUtensorMap& q_map, const CUtensorMap& r_m
 
 // Per-head GEMM C[t, h, :] = A[t, h, :] · W[h] (bf16 in, fp32 accumulate, bf16 out).
 enum class HeadGemm { kAbsorbQ, kUpV };
-cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map, uint16_t* c,
-                             int32_t T, int32_t* err, cudaStream_t stream);
+cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map,
+                             const CUtensorMap& c_map, int32_t T, int32_t* err, cudaStream_t stream);
 
 }  // namespace mla

@@ -626,11 +626,17 @@ static mla_status head_gemm(mla::HeadGemm kind, const void* a, const void* w, vo
   const uint64_t wdims[3] = {N, K, MLA_NUM_HEADS};
   const uint64_t wstr[2] = {N * 2, N * 2 * K};
   const uint32_t wbox[3] = {64, 64, 1};
+  // outputs [T, 128, N]; box = 64 of N x 1 head x 128 tokens (TMA store)
+  const uint64_t cdims[3] = {N, MLA_NUM_HEADS, (uint64_t)T};
+  const uint64_t cstr[2] = {N * 2, N * 2 * MLA_NUM_HEADS};
+  CUtensorMap cmap;
   mla_status s = make_map(&amap, a, 3, adims, astr, abox, "activations");
   if (s != MLA_OK) return s;
   s = make_map(&wmap, w, 3, wdims, wstr, wbox, "weights");
   if (s != MLA_OK) return s;
-  cudaError_t e = mla::launch_head_gemm(kind, amap, wmap, (uint16_t*)c, T, dev_err, (cudaStream_t)stream);
+  s = make_map(&cmap, c, 3, cdims, cstr, abox, "outputs");
+  if (s != MLA_OK) return s;
+  cudaError_t e = mla::launch_head_gemm(kind, amap, wmap, cmap, T, dev_err, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, absorb ? "absorb_q launch" : "up_v launch");
   return MLA_OK;
 }
@@ -676,8 +682,16 @@ mla_status mla_expand_kv(const void* rows, int32_t n, const void* w_uk, const vo
   const uint32_t vbox[3] = {64, 64, 1};
   s = make_map(&vmap, w_uv, 3, vdims, vstr, vbox, "W_UV");
   if (s != MLA_OK) return s;
-  cudaError_t e = mla::launch_expand_kv(amap, kmap, vmap, (uint16_t*)k_c, (uint16_t*)v_c, n, dev_err,
-                                        (cudaStream_t)stream);
+  // K_c, V_c [128 heads, n, 128] as {128, n, 128 heads}: box 64 x 128 tokens x 1 head (TMA stores)
+  const uint64_t odims[3] = {MLA_HEAD_DIM_C, (uint64_t)n, MLA_NUM_HEADS};
+  const uint64_t ostr[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)n * MLA_HEAD_DIM_C * 2};
+  const uint32_t obox[3] = {64, 128, 1};
+  CUtensorMap kcmap, vcmap;
+  s = make_map(&kcmap, k_c, 3, odims, ostr, obox, "K_c");
+  if (s != MLA_OK) return s;
+  s = make_map(&vcmap, v_c, 3, odims, ostr, obox, "V_c");
+  if (s != MLA_OK) return s;
+  cudaError_t e = mla::launch_expand_kv(amap, kmap, vmap, kcmap, vcmap, n, dev_err, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "expand_kv launch");
   return MLA_OK;
 }

@@ -70,11 +70,15 @@ def test_kv_append_slot_out_of_range_sets_error_word(api):
 def test_absorb_q(api, T):
     case = wl.make_case([T], [T], seed=2 + T)
     q_c, w_uk = to_bf16(case.q_c, "cuda"), to_bf16(case.w_uk, "cuda")
-    out = torch.full((T, 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    # rows past T (a guard band after the output) must stay untouched by the tile stores
+    buf = torch.full((T + 3, 128, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+    buf[T:] = 7.0
+    out = buf[:T]
     dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
     api.mla_absorb_q(q_c, w_uk, out, dev_err)
     assert api.mla_check(dev_err) == 0
     assert_close(to_np(out), oracle.absorb_q(case.q_c, case.w_uk), f"q_abs T={T}")
+    assert bool((buf[T:] == 7.0).all()), "a store wrote past the last row"
 
 
 @pytest.mark.parametrize("T", [1, 16, 130])
@@ -82,11 +86,14 @@ def test_up_v(api, T):
     rng = np.random.Generator(np.random.PCG64(T))
     o_lat = wl.bf16_round(rng.standard_normal((T, 128, 512), dtype=np.float32) * 0.1)
     case = wl.make_case([1], [1], seed=3)
-    out = torch.full((T, 128, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    buf = torch.full((T + 3, 128, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    buf[T:] = 7.0
+    out = buf[:T]
     dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
     api.mla_up_v(to_bf16(o_lat, "cuda"), to_bf16(case.w_uv, "cuda"), out, dev_err)
     assert api.mla_check(dev_err) == 0
     assert_close(to_np(out), oracle.up_v(o_lat, case.w_uv), f"out T={T}")
+    assert bool((buf[T:] == 7.0).all()), "a store wrote past the last row"
 
 
 # ------------------------------------------------------------------ A3 / A4

@@ -40,11 +40,16 @@ def test_branch_threshold(api):
 def test_expand_kv(api, n):
     case = wl.make_case([n], [1], seed=80 + n)
     rows = torch.cat([to_bf16(case.c_kv, "cuda"), to_bf16(case.k_r, "cuda")], dim=1).contiguous()
-    k_c = torch.empty((128, n, 128), dtype=torch.bfloat16, device="cuda")
-    v_c = torch.empty_like(k_c)
+    # one buffer [K_c | V_c | guard]: the stores of a ragged last tile must stay inside each head's n rows
+    buf = torch.full((2 * 128 * n * 128 + 4096,), 7.0, dtype=torch.bfloat16, device="cuda")
+    k_c = buf[:128 * n * 128].view(128, n, 128)
+    v_c = buf[128 * n * 128:2 * 128 * n * 128].view(128, n, 128)
+    k_c.fill_(float("nan"))
+    v_c.fill_(float("nan"))
     dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
     api.mla_expand_kv(rows, to_bf16(case.w_uk, "cuda"), to_bf16(case.w_uv, "cuda"), k_c, v_c, dev_err)
     assert api.mla_check(dev_err) == 0
+    assert bool((buf[2 * 128 * n * 128:] == 7.0).all()), "a store wrote past V_c"
     rk, rv = oracle.expand_kv(case.c_kv, case.w_uk, case.w_uv)
     assert_close(to_np(k_c), rk.transpose(1, 0, 2), f"K_c n={n}")   # head-major on the device
     assert_close(to_np(v_c), rv.transpose(1, 0, 2), f"V_c n={n}")
