@@ -79,6 +79,22 @@ def test_decompress_matches_the_absorbed_oracle(api, seq, q):
     assert_close(to_np(out), ref["out"], f"decompress out seq={seq} q={q}")
 
 
+@pytest.mark.parametrize("seq,q", [(600, 256), (900, 768), (1100, 1024)])
+def test_decompress_many_query_tiles(api, seq, q):
+    """2, 6 and 8 query tiles of 128 rows per head, each with its own causal
+    key range; the first and last row of every tile against the oracle."""
+    case = wl.make_case([seq], [q], seed=70 + q)
+    dc = DeviceCase(case)
+    got = to_np(_decompress(api, case, dc, 0))
+    assert np.all(np.isfinite(got))
+    rows = sorted({r for t in range(0, q, 128) for r in (t, min(t + 127, q - 1))} | {q - 1})
+    cache = oracle.append(np.zeros((case.num_pages, 64, 576), dtype=np.float32), case.c_kv, case.k_r,
+                          oracle.slot_mapping(case.block_table, *case.positions()))
+    ref = oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table, case.seq_lens,
+                          case.q_lens, SCALE, rows=rows)
+    assert_close(got[rows], ref["out"][rows], f"decompress out seq={seq} q={q}")
+
+
 def test_decompress_equals_path_a_rows(api):
     """A few rows against the oracle's own path A (decompress, then attend)."""
     case = wl.make_case([400], [270], seed=97)
