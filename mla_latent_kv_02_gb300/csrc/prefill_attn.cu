@@ -15,7 +15,9 @@
 //   O   += P(j)·V(j)  M = 128, N = 128, K = 128   (A = P from TMEM)
 //   l   += P(j)·1     M = 128, N = 16             (row sums of the bf16 P)
 // S is double-buffered in TMEM so that QK^T(j+1) runs while the softmax
-// works on tile j.  Warps: 0 TMA producer, 1 TMEM allocation + MMA issue,
+// works on tile j.  Warps: 0 TMA producer, 1 TMEM allocation + QK^T issue,
+// 10 P·V issue (an MMA issue blocks while the tensor pipe's queue is full, so
+// one thread issuing both would hold P·V(j) behind QK^T(j+1)),
 // 2-9 softmax and epilogue: two warps per query row (thread = TMEM lane),
 // each with 64 of a tile's 128 key columns; the two halves of a row swap
 // their maxima through shared memory once per tile.  The softmax
@@ -56,7 +58,8 @@ static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 constexpr uint32_t kColO = 0, kColS = 128, kColP = 384, kColSum = 448, kTmemCols = 512;
 constexpr int kSoftWarp0 = 2;
 constexpr int kSoftWarps = 8;                      // two warps per TMEM lane quarter, 64 key columns each
-constexpr int kThreads = 32 * (kSoftWarp0 + kSoftWarps);
+constexpr int kPvWarp = kSoftWarp0 + kSoftWarps;
+constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
 constexpr uint32_t kIdescSum = idesc_bf16_f32(128, 16, false, false);
@@ -72,6 +75,7 @@ enum : int {
   B_P_FULL = B_S_FREE + 2,          // one arrival per softmax warp
   B_O_DONE,
   B_DRAIN,
+  B_DRAIN_PV,
   B_XMAX,                           // 2 (tile parity), one arrival per softmax warp
   B_COUNT = B_XMAX + 2
 };
@@ -121,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_P_FULL), kSoftWarps);
     mbar_init(BAR(B_O_DONE), 1);
     mbar_init(BAR(B_DRAIN), 1);
+    mbar_init(BAR(B_DRAIN_PV), 1);
     mbar_init(BAR(B_XMAX), kSoftWarps);
     mbar_init(BAR(B_XMAX + 1), kSoftWarps);
     fence_mbar_init();
@@ -199,15 +204,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     __syncwarp();
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issue
+    // ---------------------------------------------------------------- QK^T issue
+    // S(j) = Q·K(j)^T once K(j) has landed and the softmax has read S(j-2)
+    // out of the same buffer.
     if (lane == 0) {
       const uint64_t qdesc = sdesc_sw128(base + kOffQ, 16, 1024);
       const uint64_t kdesc0 = sdesc_sw128(base + kOffK, 16, 1024);
-      const uint64_t vdesc0 = sdesc_sw128(base + kOffV, (uint32_t)kChunkBytes, 1024);
-      const uint64_t odesc = sdesc_sw128(base + kOffOnes, 16, 1024);
       bool ok = wait_phase<false, false>(BAR(B_Q_FULL), 0, err, abort_flag);
-      auto issue_qk = [&](int j) {
+      for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % kStages, sb = j & 1;
+        ok = wait_phase<false, false>(BAR(B_K_FULL + st), (j / kStages) & 1, err, abort_flag) &&
+             (j < 2 || wait_phase<false, false>(BAR(B_S_FREE + sb), ((j - 2) >> 1) & 1, err, abort_flag));
+        if (!ok) break;
         tc_fence_after();
         const uint64_t dk = kdesc0 + (uint64_t)((st * kKBytes) >> 4);
 #pragma unroll
@@ -218,8 +226,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                    dk + (uint64_t)((c * kChunkBytes + kk * 32) >> 4), kIdescQK, (c | kk) ? 1u : 0u);
         tc_commit(BAR(B_S_FULL + sb));
         tc_commit(BAR(B_K_EMPTY + st));
-      };
-      auto issue_pv = [&](int t) {
+      }
+      // every MMA of this thread has finished before TMEM is released
+      tc_commit(BAR(B_DRAIN));
+      wait_phase_drain(BAR(B_DRAIN), 0);
+    }
+    __syncwarp();
+  } else if (warp == kPvWarp) {
+    // ---------------------------------------------------------------- P·V issue
+    // O += P(j)·V(j) and l += P(j)·1 once the softmax has written P(j) and V(j)
+    // has landed.
+    if (lane == 0) {
+      const uint64_t vdesc0 = sdesc_sw128(base + kOffV, (uint32_t)kChunkBytes, 1024);
+      const uint64_t odesc = sdesc_sw128(base + kOffOnes, 16, 1024);
+      bool ok = true;
+      for (int t = 0; ok && t < n_tiles; ++t) {
+        ok = wait_phase<false, false>(BAR(B_P_FULL), t & 1, err, abort_flag) &&
+             wait_phase<false, false>(BAR(B_V_FULL + t % kStages), (t / kStages) & 1, err, abort_flag);
+        if (!ok) break;
         tc_fence_after();
         const uint64_t dv = vdesc0 + (uint64_t)(((t % kStages) * kVBytes) >> 4);
 #pragma unroll
@@ -230,41 +254,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_commit(BAR(B_V_EMPTY + t % kStages));
         tc_commit(BAR(B_O_DONE));
-      };
-      // Issue whichever is ready first: QK^T(nq) once its tile has landed and
-      // its S buffer is free, P·V(np) once the softmax has written P(np).  P·V
-      // never waits behind the next tile's load (which waits for that P·V to
-      // free its stage).
-      int nq = 0, np = 0;
-      uint64_t t0 = cycles();  // the time limit runs from the last progress
-      uint32_t spins = 0;
-      while (ok && np < n_tiles) {
-        bool progressed = false;
-        if (nq < n_tiles && mbar_test_wait(BAR(B_K_FULL + nq % kStages), (nq / kStages) & 1) &&
-            (nq < 2 || mbar_test_wait(BAR(B_S_FREE + (nq & 1)), ((nq - 2) >> 1) & 1))) {
-          issue_qk(nq++);
-          progressed = true;
-        }
-        if (np < nq && mbar_test_wait(BAR(B_P_FULL), np & 1) &&
-            mbar_test_wait(BAR(B_V_FULL + np % kStages), (np / kStages) & 1)) {
-          issue_pv(np++);
-          progressed = true;
-        }
-        if (progressed) {
-          spins = 0;
-          t0 = cycles();
-        } else if ((++spins & 255u) == 0u) {
-          if (*abort_flag) {
-            ok = false;
-          } else if (cycles() - t0 > kWaitLimitCycles) {
-            atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
-            *abort_flag = 1;
-            ok = false;
-          }
-        }
       }
-      tc_commit(BAR(B_DRAIN));
-      wait_phase_drain(BAR(B_DRAIN), 0);
+      tc_commit(BAR(B_DRAIN_PV));
+      wait_phase_drain(BAR(B_DRAIN_PV), 0);
     }
     __syncwarp();
   } else {

@@ -2,8 +2,8 @@
 (csrc/prefill_attn.cu), CPU only.
 
 The kernel's roles — a TMA producer that issues K and V loads into two
-2-deep rings as their stages free up, an MMA thread that issues QK^T(j)
-into one of two S buffers or P·V(j) whichever is ready, and softmax warps
+2-deep rings as their stages free up, one thread that issues QK^T(j) into
+one of two S buffers, another that issues P·V(j), and softmax warps
 in pairs that swap row maxima through a tile-parity buffer — are restated
 here with hardware parity semantics for every mbarrier wait and run under
 random interleavings of the roles and of every asynchronous completion
@@ -83,31 +83,30 @@ def run_model(n_tiles, seed, wait_o_done=True, s_buffers=2, xmax_slots=2, wait_v
             if not progressed:
                 yield
 
-    def mma():
-        nq = np_ = 0
-        while np_ < n_tiles:
-            progressed = False
-            if nq < n_tiles and B["k_full"][nq % STAGES].test(nq // STAGES) and \
-                    (nq < 2 or B["s_free"][s_idx(nq)].test((nq - 2) // 2 if s_buffers == 2 else nq - 1)):
-                if k_stage[nq % STAGES] != nq:
-                    raise ProtocolError(f"QK^T({nq}) reads a K stage holding {k_stage[nq % STAGES]}")
-                b = s_idx(nq)
-                if s_unread[b]:
-                    raise ProtocolError(f"QK^T({nq}) overwrites S({s_buf[b]}) before every warp read it")
-                k_reading[nq % STAGES] = nq
-                events.append(("qk", nq))
-                nq += 1
-                progressed = True
-            if np_ < nq and B["p_full"].test(np_) and B["v_full"][np_ % STAGES].test(np_ // STAGES):
-                if v_stage[np_ % STAGES] != np_ or p_buf["tile"] != np_:
-                    raise ProtocolError(f"P·V({np_}) reads V/P of another tile")
-                v_reading[np_ % STAGES] = np_
-                p_buf["reading"] = True
-                events.append(("pv", np_))
-                np_ += 1
-                progressed = True
-            if not progressed:
+    def qk():
+        for nq in range(n_tiles):
+            while not (B["k_full"][nq % STAGES].test(nq // STAGES) and
+                       (nq < 2 or B["s_free"][s_idx(nq)].test((nq - 2) // 2 if s_buffers == 2 else nq - 1))):
                 yield
+            if k_stage[nq % STAGES] != nq:
+                raise ProtocolError(f"QK^T({nq}) reads a K stage holding {k_stage[nq % STAGES]}")
+            b = s_idx(nq)
+            if s_unread[b]:
+                raise ProtocolError(f"QK^T({nq}) overwrites S({s_buf[b]}) before every warp read it")
+            k_reading[nq % STAGES] = nq
+            events.append(("qk", nq))
+            yield
+
+    def pv():
+        for np_ in range(n_tiles):
+            while not (B["p_full"].test(np_) and B["v_full"][np_ % STAGES].test(np_ // STAGES)):
+                yield
+            if v_stage[np_ % STAGES] != np_ or p_buf["tile"] != np_:
+                raise ProtocolError(f"P·V({np_}) reads V/P of another tile")
+            v_reading[np_ % STAGES] = np_
+            p_buf["reading"] = True
+            events.append(("pv", np_))
+            yield
 
     def softmax(w):
         for j in range(n_tiles):
@@ -139,7 +138,7 @@ def run_model(n_tiles, seed, wait_o_done=True, s_buffers=2, xmax_slots=2, wait_v
             p_buf["tile"] = j
             B["p_full"].arrive()
 
-    roles = {"prod": producer(), "mma": mma()}
+    roles = {"prod": producer(), "qk": qk(), "pv": pv()}
     for w in range(SOFT):
         roles[("sm", w)] = softmax(w)
     idle = 0
