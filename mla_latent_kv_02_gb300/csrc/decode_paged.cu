@@ -1,4 +1,4 @@
-// Steps A3 + A4: absorbed paged MLA attention (split-KV) and the combine.
+// Step A3: absorbed paged MLA attention (split-KV); the combine (A4) is in combine.cu.
 //
 // Method ([P1] "撕开 DeepSeek MLA 源码：C++ 与 TensorRT-LLM 算子设计优化全景与 TaoToken 实践",
 // §4 path B and §3 constants): per query row t and head h,
@@ -864,50 +864,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
 }
 
 // Merge split rows: lse = log2 Σ 2^{lse_s} (log2 domain), o = Σ 2^{lse_s - lse} o_s.
-// Step A4: merge the fp32 partials of each split row.  One CTA = one split
-// row and 16 heads; 16 threads per head, each with 8 of the head's 128
-// column quads, so a thread keeps 8 independent 16-byte loads of a piece in
-// flight and one wave of CTAs covers the whole merge.
-constexpr int kCombHeads = 16, kCombThreads = 256, kCombQuads = kDC / 4 / (kCombThreads / kCombHeads);
-__global__ void __launch_bounds__(kCombThreads) combine_kernel(const CombineArgs a) {
-  const int r = blockIdx.x, tid = threadIdx.x;
-  const int h = blockIdx.y * kCombHeads + (tid >> 4), q0 = tid & 15;
-  const int row = a.split_rows[4 * r], s0 = a.split_rows[4 * r + 1], n = a.split_rows[4 * r + 2];
-  if (row < 0 || row >= a.T || s0 < 0 || n < 1 || s0 + n > a.num_partials) {
-    if (tid == 0) atomicOr(a.dev_err, (int32_t)MLA_DEVERR_PLAN);
-    return;
-  }
-  float mx = -INFINITY;
-  for (int i = 0; i < n; ++i) mx = fmaxf(mx, __ldg(a.part_lse + (size_t)(s0 + i) * kH + h));
-  float wsum = 0.f;
-  float4 acc[kCombQuads];
-#pragma unroll
-  for (int k = 0; k < kCombQuads; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
-  const uint64_t last_use = l2_policy_evict_first();  // the partials' only read
-#pragma unroll 1
-  for (int i = 0; i < n; ++i) {
-    const float w = exp2f(__ldg(a.part_lse + (size_t)(s0 + i) * kH + h) - mx);
-    const float4* src = reinterpret_cast<const float4*>(a.part_o + ((size_t)(s0 + i) * kH + h) * kDC) + q0;
-    float4 v[kCombQuads];
-#pragma unroll
-    for (int k = 0; k < kCombQuads; ++k) v[k] = ld_global_v4_hint(src + 16 * k, last_use);
-    wsum += w;
-#pragma unroll
-    for (int k = 0; k < kCombQuads; ++k) {
-      acc[k].x += w * v[k].x;
-      acc[k].y += w * v[k].y;
-      acc[k].z += w * v[k].z;
-      acc[k].w += w * v[k].w;
-    }
-  }
-  const float inv = 1.f / wsum;
-  uint2* dst = reinterpret_cast<uint2*>(a.o_lat + ((size_t)row * kH + h) * kDC) + q0;
-#pragma unroll
-  for (int k = 0; k < kCombQuads; ++k)
-    dst[16 * k] = make_uint2(pack_bf16x2(acc[k].x * inv, acc[k].y * inv), pack_bf16x2(acc[k].z * inv, acc[k].w * inv));
-  if (q0 == 0 && a.lse) a.lse[(size_t)row * kH + h] = (mx + log2f(wsum)) * 0.6931471805599453f;
-}
-
 }  // namespace decode
 
 int decode_smem_bytes() { return decode::Layout<false>::kSmemBytes; }
@@ -946,13 +902,6 @@ cudaError_t launch_decode(const CUtensorMap& kv_map, const CUtensorMap& rope_map
   else
     decode::decode_kernel<false><<<2 * num_clusters, decode::Layout<false>::kThreads,
                                    decode::Layout<false>::kSmemBytes, stream>>>(kv_map, rope_map, args);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_combine(const CombineArgs& args, int num_split_rows, cudaStream_t stream) {
-  if (num_split_rows <= 0) return cudaSuccess;
-  decode::combine_kernel<<<dim3(num_split_rows, decode::kH / decode::kCombHeads), decode::kCombThreads, 0, stream>>>(
-      args);
   return cudaGetLastError();
 }
 
