@@ -281,8 +281,8 @@ def measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos_old
         del rows, scales
         # NVFP4 cache (E2M1 codes, E4M3 block scales, fp32 tensor scale):
         # quantising fill of the whole context, then the dequantising gather
-        # of every sequence (B launches queued back to back), 416 B read and
-        # 1152 B written per token.
+        # of every sequence, as B launches queued back to back and as one
+        # batched launch; 416 B read and 1152 B written per token.
         st_nv = 2.0 ** -8
         rows4 = torch.zeros((case.num_pages, 64, 416), dtype=torch.uint8, device=dev)
         us = _time_launches(torch, stream, lambda i: api.mla_kv_append_nvfp4(c_old, k_old, slots_old, rows4, st_nv,
@@ -297,9 +297,17 @@ def measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos_old
 
         us = _time_launches(torch, stream, gather_all, reps=3, warmup=2, per_rep=len(gl))
         tot = sum(gl)
-        entry("gather_nvfp4_all_sequences", us, tot * (416 + 1152) + sum((m + 63) // 64 * 4 for m in gl),
-              tokens=tot, launches=len(gl))
-        del rows4, outs
+        gbytes = tot * (416 + 1152) + sum((m + 63) // 64 * 4 for m in gl)
+        entry("gather_nvfp4_per_sequence", us, gbytes, tokens=tot, launches=len(gl))
+        # the same gather of every sequence as one batched launch into a packed output
+        del outs
+        offs = torch.from_numpy(np.concatenate([[0], np.cumsum(gl)]).astype(np.int64)).to(dev)
+        sids = torch.arange(len(gl), dtype=torch.int32, device=dev)
+        packed = torch.empty((tot, 576), dtype=torch.bfloat16, device=dev)
+        us = _time_launches(torch, stream, lambda i: api.mla_gather_paged_nvfp4_batch(rows4, st_nv, bt, sids, offs,
+                                                                                      packed, dev_err))
+        entry("gather_nvfp4_batch", us, gbytes + len(gl) * 12, tokens=tot, launches=1)
+        del rows4, packed
     if api.mla_check(dev_err) != 0:
         raise RuntimeError("device error word set while timing the cache-fill, RoPE and FP8 kernels")
     # put the unrotated keys back (the cache holds them for the step above)

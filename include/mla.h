@@ -73,6 +73,7 @@ typedef enum mla_status {
 #define MLA_DEVERR_PLAN 8u     /* the plan buffer is not a valid decode plan */
 #define MLA_DEVERR_POS_OOB 16u /* RoPE position outside [0, max_pos): that token / row skipped */
 #define MLA_DEVERR_FP8_RANGE 32u /* FP8 decode: a token scale outside [2^-15, 2^7]; that row was clamped */
+#define MLA_DEVERR_BATCH 64u   /* batched gather: a sequence id, offset or length out of range; those rows skipped */
 
 /* Thread-local message of the last failing call (never NULL). */
 const char* mla_last_error(void);
@@ -473,6 +474,26 @@ mla_status mla_kv_append_nvfp4(const void* c_kv_new, const void* k_r_new, const 
 mla_status mla_gather_paged_nvfp4(const void* rows, float tensor_scale, int64_t num_pages,
                                   const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
                                   void* out, int32_t* dev_err, void* stream);
+
+/*
+ * Batched dequantising gather, one launch for many sequences: for i < nb,
+ * the first n_i = out_offsets[i+1] - out_offsets[i] cached tokens of
+ * sequence seq_ids[i], in position order, go to rows [out_offsets[i],
+ * out_offsets[i+1]) of out bf16 [total_tokens, 576] (the values of
+ * mla_gather_paged_nvfp4).  seq_ids int32 [nb] and out_offsets int64 [nb+1]
+ * are device arrays (out_offsets[0] = 0, non-decreasing, out_offsets[nb] =
+ * total_tokens); block_table int32 [B, max_pages].  A row whose sequence id is
+ * outside [0, B), whose position needs more than max_pages pages, or whose
+ * offsets are inconsistent sets MLA_DEVERR_BATCH and is left unwritten; bad
+ * page ids set MLA_DEVERR_PAGE_OOB.  nb == 0 or total_tokens == 0 is a no-op.
+ * Host errors: MLA_ERR_INVALID_ARG (a null pointer, negative sizes, B or
+ * max_pages < 1, tensor_scale not finite and > 0), MLA_ERR_MISALIGNED (rows
+ * and out 16-byte, out_offsets 8-byte, the other pointers 4-byte aligned).
+ */
+mla_status mla_gather_paged_nvfp4_batch(const void* rows, float tensor_scale, int64_t num_pages,
+                                        const int32_t* block_table, int32_t B, int32_t max_pages,
+                                        const int32_t* seq_ids, const int64_t* out_offsets, int32_t nb,
+                                        int64_t total_tokens, void* out, int32_t* dev_err, void* stream);
 
 /*
  * Synchronise `stream`, read the device error word into *word_out (may be

@@ -52,6 +52,7 @@ SIGNATURES = {
     "mla_gather_paged_fp8": (C.c_int, [P, P, I64, P, I32, I32, I32, P, P, P]),
     "mla_kv_append_nvfp4": (C.c_int, [P, P, P, I32, C.c_float, P, I64, P, P]),
     "mla_gather_paged_nvfp4": (C.c_int, [P, C.c_float, I64, P, I32, I32, I32, P, P, P]),
+    "mla_gather_paged_nvfp4_batch": (C.c_int, [P, C.c_float, I64, P, I32, I32, P, P, I32, I64, P, P, P]),
     "mla_prefill_threshold": (I32, []),
     "mla_branch_for": (I32, [I32]),
     "mla_expand_kv": (C.c_int, [P, I32, P, P, P, P, P, P]),

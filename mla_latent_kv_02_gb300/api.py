@@ -22,6 +22,7 @@ D_QK = D_C + D_R
 STATUS = {0: "MLA_OK", 1: "MLA_ERR_INVALID_ARG", 2: "MLA_ERR_MISALIGNED", 3: "MLA_ERR_UNSUPPORTED",
           4: "MLA_ERR_CUDA", 5: "MLA_ERR_DEVICE", 6: "MLA_ERR_TIMEOUT", 7: "MLA_ERR_NO_SPACE"}
 DEVERR_PAGE_OOB, DEVERR_SLOT_OOB, DEVERR_TIMEOUT, DEVERR_PLAN, DEVERR_POS_OOB, DEVERR_FP8_RANGE = 1, 2, 4, 8, 16, 32
+DEVERR_BATCH = 64
 
 
 class MlaError(RuntimeError):
@@ -189,6 +190,28 @@ def mla_gather_paged_nvfp4(rows, tensor_scale: float, block_table, b: int, n_tok
     _check(lib().mla_gather_paged_nvfp4(_ptr(rows), float(tensor_scale), rows.shape[0], _ptr(block_table),
                                         block_table.shape[1], int(b), int(n_tokens), _ptr(out), _ptr(dev_err),
                                         _stream(stream)))
+
+
+def mla_gather_paged_nvfp4_batch(rows, tensor_scale: float, block_table, seq_ids, out_offsets, out, dev_err,
+                                 stream=None) -> None:
+    """Gather the sequences seq_ids (device int32 [nb]) into out bf16 [total, 576]:
+    sequence seq_ids[i] fills rows out_offsets[i] .. out_offsets[i+1] (device
+    int64 [nb + 1], out_offsets[0] = 0, out_offsets[nb] = total)."""
+    _need(rows, "rows", torch.uint8)
+    if rows.dim() != 3 or tuple(rows.shape[1:]) != (PAGE, NVFP4_ROW_BYTES):
+        raise ValueError(f"rows has shape {tuple(rows.shape)}, expected (pages, {PAGE}, {NVFP4_ROW_BYTES})")
+    _need(block_table, "block_table", torch.int32)
+    _need(seq_ids, "seq_ids", torch.int32)
+    nb = seq_ids.shape[0]
+    _need(out_offsets, "out_offsets", torch.int64, (nb + 1,))
+    _need(out, "out", torch.bfloat16)
+    if out.dim() != 2 or out.shape[1] != D_QK:
+        raise ValueError(f"out has shape {tuple(out.shape)}, expected (total, {D_QK})")
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    _check(lib().mla_gather_paged_nvfp4_batch(_ptr(rows), float(tensor_scale), rows.shape[0], _ptr(block_table),
+                                              block_table.shape[0], block_table.shape[1], _ptr(seq_ids),
+                                              _ptr(out_offsets), nb, out.shape[0], _ptr(out), _ptr(dev_err),
+                                              _stream(stream)))
 
 
 def mla_prefill_threshold() -> int:

@@ -13,9 +13,12 @@
 // * kv_append_nvfp4: one warp per token, lane l owns block l (16 values): its
 //   amax, s_b = E4M3(amax / (6 s_t)) and the 16 codes E2M1(x / (s_b s_t)),
 //   each division and product one correctly rounded fp32 operation.
-// * gather_nvfp4: one warp per token; lanes 0-15 load 32 codes each as one
-//   16-byte vector and write 64 bytes of bf16, lanes 16-23 copy the RoPE
-//   values.  Value = bf16(fp32(fp32(e2m1 * s_b) * s_t)).
+// * gather_nvfp4: one half-warp per token; in each of four steps lane l of
+//   the half dequantises code word 16 v + l (8 elements) and the 16 lanes
+//   write 256 contiguous bytes of bf16; lanes 0-7 copy the RoPE values.
+//   Value = bf16(fp32(fp32(e2m1 * s_b) * s_t)).
+// * gather_nvfp4_batch: many sequences into one packed output in one launch
+//   (the same values; one half-warp per token).
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -108,30 +111,77 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, float sb, float st) {
   return make_uint4(o[0], o[1], o[2], o[3]);
 }
 
+// One token's row, dequantised by the 16 lanes (hl) of a half-warp into dst
+// (72 uint4 = 576 bf16).  In step v lane hl takes code word 16 v + hl
+// (elements 8 (16 v + hl) .. + 7, block (16 v + hl) / 2), so each store
+// instruction writes 256 contiguous bytes; lanes 0-7 also copy the RoPE
+// values.  Every load is issued before the first store.
+__device__ __forceinline__ void gather_row_half(const uint8_t* __restrict__ row, uint4* __restrict__ dst, int hl,
+                                                float tensor_scale) {
+  uint32_t cw[4], sb[4];
+#pragma unroll
+  for (int v = 0; v < 4; ++v) {
+    cw[v] = __ldg(reinterpret_cast<const uint32_t*>(row) + 16 * v + hl);
+    sb[v] = __ldg(row + kScaleOff + ((16 * v + hl) >> 1));
+  }
+  uint4 rp = make_uint4(0u, 0u, 0u, 0u);
+  if (hl < 8) rp = __ldg(reinterpret_cast<const uint4*>(row + kRopeOff) + hl);
+#pragma unroll
+  for (int v = 0; v < 4; ++v) dst[16 * v + hl] = dequant_word(cw[v], e4m3_to_f32(sb[v]), tensor_scale);
+  if (hl < 8) dst[64 + hl] = rp;
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
     gather_nvfp4_kernel(const uint8_t* __restrict__ rows, float tensor_scale, int64_t num_pages,
                         const int32_t* __restrict__ block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
                         uint4* __restrict__ out, int32_t* err) {
-  const int lane = threadIdx.x & 31;
-  for (int64_t j = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); j < n_tokens; j += (int64_t)gridDim.x * kWarps) {
+  const int lane = threadIdx.x & 31, hl = lane & 15;
+  const int64_t stride = (int64_t)gridDim.x * kWarps * 2;
+  for (int64_t j0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * 2; j0 < n_tokens; j0 += stride) {
+    const int64_t j = j0 + (lane >> 4);  // one token per half-warp
+    if (j >= n_tokens) continue;
     const int32_t pid = __ldg(block_table + (int64_t)b * max_pages + j / 64);
     if (pid < 0 || (int64_t)pid >= num_pages) {
-      if (lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_PAGE_OOB);
+      if (hl == 0) atomicOr(err, (int32_t)MLA_DEVERR_PAGE_OOB);
       continue;
     }
-    const uint8_t* row = rows + ((int64_t)pid * 64 + j % 64) * kRow;
-    uint4* dst = out + j * 72;
-    if (lane < 16) {
-      const uint4 c = __ldg(reinterpret_cast<const uint4*>(row) + lane);   // codes of blocks 2l, 2l+1
-      const uint32_t s2 = __ldg(reinterpret_cast<const uint16_t*>(row + kScaleOff) + lane);
-      const float s0 = e4m3_to_f32(s2 & 0xFFu), s1 = e4m3_to_f32(s2 >> 8);
-      dst[4 * lane] = dequant_word(c.x, s0, tensor_scale);
-      dst[4 * lane + 1] = dequant_word(c.y, s0, tensor_scale);
-      dst[4 * lane + 2] = dequant_word(c.z, s1, tensor_scale);
-      dst[4 * lane + 3] = dequant_word(c.w, s1, tensor_scale);
-    } else if (lane < 24) {
-      dst[64 + (lane - 16)] = __ldg(reinterpret_cast<const uint4*>(row + kRopeOff) + (lane - 16));
+    gather_row_half(rows + ((int64_t)pid * 64 + j % 64) * kRow, out + j * 72, hl, tensor_scale);
+  }
+}
+
+// Batched gather: token g of the packed output belongs to the sequence i with
+// off[i] <= g < off[i + 1] (found by bisection of the small offsets array)
+// and sits at position g - off[i] of sequence seq_ids[i].  One half-warp per
+// token (gather_row_half), two tokens per warp.
+__global__ void __launch_bounds__(kWarps * 32)
+    gather_nvfp4_batch_kernel(const uint8_t* __restrict__ rows, float tensor_scale, int64_t num_pages,
+                              const int32_t* __restrict__ block_table, int32_t B, int32_t max_pages,
+                              const int32_t* __restrict__ seq_ids, const int64_t* __restrict__ off, int32_t nb,
+                              int64_t total, uint4* __restrict__ out, int32_t* err) {
+  const int lane = threadIdx.x & 31, hl = lane & 15;
+  const int64_t stride = (int64_t)gridDim.x * kWarps * 2;
+  for (int64_t g0 = ((int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5)) * 2; g0 < total; g0 += stride) {
+    const int64_t g = g0 + (lane >> 4);
+    if (g >= total) continue;
+    int lo = 0, hi = nb;  // off[lo] <= g < off[hi] when the offsets are consistent
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (__ldg(off + mid) <= g) lo = mid;
+      else hi = mid;
     }
+    const int64_t o0 = __ldg(off + lo), o1 = __ldg(off + lo + 1);
+    const int64_t j = g - o0;
+    const int32_t sid = __ldg(seq_ids + lo);
+    if (!(o0 <= g && g < o1) || sid < 0 || sid >= B || j / 64 >= max_pages) {
+      if (hl == 0) atomicOr(err, (int32_t)MLA_DEVERR_BATCH);
+      continue;
+    }
+    const int32_t pid = __ldg(block_table + (int64_t)sid * max_pages + j / 64);
+    if (pid < 0 || (int64_t)pid >= num_pages) {
+      if (hl == 0) atomicOr(err, (int32_t)MLA_DEVERR_PAGE_OOB);
+      continue;
+    }
+    gather_row_half(rows + ((int64_t)pid * 64 + j % 64) * kRow, out + g * 72, hl, tensor_scale);
   }
 }
 
@@ -157,8 +207,19 @@ cudaError_t launch_gather_nvfp4(const uint8_t* rows, float tensor_scale, int64_t
                                 const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
                                 uint16_t* out, int32_t* dev_err, cudaStream_t stream) {
   if (n_tokens <= 0) return cudaSuccess;
-  f4::gather_nvfp4_kernel<<<f4::blocks_for(n_tokens), f4::kWarps * 32, 0, stream>>>(
+  f4::gather_nvfp4_kernel<<<f4::blocks_for(((int64_t)n_tokens + 1) / 2), f4::kWarps * 32, 0, stream>>>(
       rows, tensor_scale, num_pages, block_table, max_pages, b, n_tokens, reinterpret_cast<uint4*>(out), dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_nvfp4_batch(const uint8_t* rows, float tensor_scale, int64_t num_pages,
+                                      const int32_t* block_table, int32_t B, int32_t max_pages, const int32_t* seq_ids,
+                                      const int64_t* out_offsets, int32_t nb, int64_t total_tokens, uint16_t* out,
+                                      int32_t* dev_err, cudaStream_t stream) {
+  if (total_tokens <= 0 || nb <= 0) return cudaSuccess;
+  f4::gather_nvfp4_batch_kernel<<<f4::blocks_for((total_tokens + 1) / 2), f4::kWarps * 32, 0, stream>>>(
+      rows, tensor_scale, num_pages, block_table, B, max_pages, seq_ids, out_offsets, nb, total_tokens,
+      reinterpret_cast<uint4*>(out), dev_err);
   return cudaGetLastError();
 }
 

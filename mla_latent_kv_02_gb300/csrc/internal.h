@@ -117,6 +117,10 @@ cudaError_t launch_kv_append_nvfp4(const uint16_t* c_kv_new, const uint16_t* k_r
 cudaError_t launch_gather_nvfp4(const uint8_t* rows, float tensor_scale, int64_t num_pages,
                                 const int32_t* block_table, int32_t max_pages, int32_t b, int32_t n_tokens,
                                 uint16_t* out, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_gather_nvfp4_batch(const uint8_t* rows, float tensor_scale, int64_t num_pages,
+                                      const int32_t* block_table, int32_t B, int32_t max_pages, const int32_t* seq_ids,
+                                      const int64_t* out_offsets, int32_t nb, int64_t total_tokens, uint16_t* out,
+                                      int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                           int32_t b, int32_t n_tokens, uint16_t* out, int32_t* dev_err, cudaStream_t stream);
 

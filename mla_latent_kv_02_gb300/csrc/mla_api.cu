@@ -595,6 +595,35 @@ mla_status mla_gather_paged_nvfp4(const void* rows, float tensor_scale, int64_t 
   return MLA_OK;
 }
 
+mla_status mla_gather_paged_nvfp4_batch(const void* rows, float tensor_scale, int64_t num_pages,
+                                        const int32_t* block_table, int32_t B, int32_t max_pages,
+                                        const int32_t* seq_ids, const int64_t* out_offsets, int32_t nb,
+                                        int64_t total_tokens, void* out, int32_t* dev_err, void* stream) {
+  if (nb < 0 || total_tokens < 0)
+    return fail(MLA_ERR_INVALID_ARG, "nb = %d, total_tokens = %lld: negative", nb, (long long)total_tokens);
+  if (nb == 0 || total_tokens == 0) return MLA_OK;
+  if (!(tensor_scale > 0.f) || !std::isfinite(tensor_scale))
+    return fail(MLA_ERR_INVALID_ARG, "tensor_scale must be finite and > 0");
+  CHECK_PTR(rows);
+  CHECK_PTR(block_table);
+  CHECK_PTR(seq_ids);
+  CHECK_PTR(out_offsets);
+  CHECK_PTR(out);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(rows);
+  CHECK_ALIGN16(out);
+  if (!aligned(out_offsets, 8)) return fail(MLA_ERR_MISALIGNED, "out_offsets is not 8-byte aligned");
+  if (!aligned(block_table, 4) || !aligned(seq_ids, 4) || !aligned(dev_err, 4))
+    return fail(MLA_ERR_MISALIGNED, "block_table, seq_ids and dev_err must be 4-byte aligned");
+  if (num_pages < 1 || B < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "bad pool/table sizes");
+  if (total_tokens > ((int64_t)1 << 40)) return fail(MLA_ERR_INVALID_ARG, "total_tokens too large");
+  cudaError_t e = mla::launch_gather_nvfp4_batch((const uint8_t*)rows, tensor_scale, num_pages, block_table, B,
+                                                 max_pages, seq_ids, out_offsets, nb, total_tokens, (uint16_t*)out,
+                                                 dev_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "gather_nvfp4_batch launch");
+  return MLA_OK;
+}
+
 // Decompress-branch workspace: gathered rows [N, 576] (rounded up to 16 B),
 // then K_c and V_c [N, 128, 128] bf16.
 static size_t prefill_rows_bytes(int64_t N) { return ((size_t)N * kRowBytes + 15) / 16 * 16; }

@@ -161,3 +161,67 @@ def test_nvfp4_errors(api):
     api.mla_gather_paged_nvfp4(rows, 0.01, torch.tensor([[0, 9]], dtype=torch.int32, device="cuda"), 0, 70, out,
                                dev_err)
     assert int(dev_err.item()) == api.DEVERR_PAGE_OOB
+
+
+def _batch_case(api, st):
+    case = wl.make_case([1, 64, 65, 300, 130], [1, 1, 1, 1, 1], seed=77)
+    seq, pos = case.positions()
+    slots = oracle.slot_mapping(case.block_table, seq, pos)
+    rows = torch.zeros((case.num_pages, 64, 416), dtype=torch.uint8, device="cuda")
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.mla_kv_append_nvfp4(to_bf16(case.c_kv, "cuda"), to_bf16(case.k_r, "cuda"), torch.from_numpy(slots).cuda(),
+                            rows, st, dev_err)
+    assert api.mla_check(dev_err) == 0
+    cache = n4.append(n4.empty_cache(case.num_pages), case.c_kv, case.k_r, slots, st)
+    return case, rows, cache
+
+
+@pytest.mark.parametrize("st", [2.0 ** -8, 0.0173])
+def test_gather_nvfp4_batch_bit_exact(api, st):
+    """Sequences in any order, prefixes of any length (an empty one
+    included), packed into one output by one launch: every bf16 bit equals
+    the oracle's per-sequence gather."""
+    case, rows, cache = _batch_case(api, st)
+    picks = [(3, 300), (0, 1), (1, 0), (2, 65), (4, 100), (3, 17)]
+    offs = np.concatenate([[0], np.cumsum([n for _, n in picks])]).astype(np.int64)
+    total = int(offs[-1])
+    out = torch.full((total, 576), float("nan"), dtype=torch.bfloat16, device="cuda")
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.mla_gather_paged_nvfp4_batch(rows, st, torch.from_numpy(case.block_table).cuda(),
+                                     torch.tensor([s for s, _ in picks], dtype=torch.int32, device="cuda"),
+                                     torch.from_numpy(offs).cuda(), out, dev_err)
+    assert api.mla_check(dev_err) == 0
+    got = _bits(out)
+    for i, (sid, n) in enumerate(picks):
+        if n == 0:
+            continue
+        lat, rope = n4.gather(cache, case.block_table, sid, n, st)
+        want = np.concatenate([lat, rope], axis=1).astype(np.float32)
+        assert np.array_equal(got[offs[i]:offs[i + 1]], _bf16_bits_of(want)), f"entry {i} (sequence {sid})"
+
+
+def test_gather_nvfp4_batch_bad_entries(api):
+    """A sequence id outside the block table and a prefix longer than the
+    table's pages set MLA_DEVERR_BATCH and leave their rows untouched; the
+    good entries are still gathered."""
+    st = 2.0 ** -8
+    case, rows, cache = _batch_case(api, st)
+    max_pages = case.block_table.shape[1]
+    assert int(case.seq_lens[3]) > 64 * (max_pages - 1)        # sequence 3 fills every table column
+    picks = [(0, 1), (99, 10), (2, 65), (3, 64 * max_pages + 5)]
+    offs = np.concatenate([[0], np.cumsum([n for _, n in picks])]).astype(np.int64)
+    out = torch.full((int(offs[-1]), 576), 7.0, dtype=torch.bfloat16, device="cuda")
+    dev_err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    api.mla_gather_paged_nvfp4_batch(rows, st, torch.from_numpy(case.block_table).cuda(),
+                                     torch.tensor([s for s, _ in picks], dtype=torch.int32, device="cuda"),
+                                     torch.from_numpy(offs).cuda(), out, dev_err)
+    assert int(dev_err.item()) == api.DEVERR_BATCH
+    o = out.float().cpu().numpy()
+    assert np.all(o[offs[1]:offs[2]] == 7.0)                       # bad sequence id: untouched
+    assert np.all(o[offs[3] + 64 * max_pages:offs[4]] == 7.0)      # positions past the table: untouched
+    got = _bits(out)
+    for i in (0, 2):
+        sid, n = picks[i]
+        lat, rope = n4.gather(cache, case.block_table, sid, n, st)
+        want = np.concatenate([lat, rope], axis=1).astype(np.float32)
+        assert np.array_equal(got[offs[i]:offs[i + 1]], _bf16_bits_of(want))

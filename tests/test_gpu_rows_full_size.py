@@ -6,7 +6,8 @@ sampled outputs are checked against the oracle one by one.
 * fp32 RoPE fill: latent bit-exact, the rotated key within the bf16 bound;
 * FP8 fill: codes and scales bit-exact;
 * NVFP4 fill: codes and block scales bit-exact; the gather of a whole
-  8 194-token sequence bit-exact.
+  8 194-token sequence bit-exact, and of all 64 sequences in one batched
+  launch on sampled rows.
 """
 import numpy as np
 import pytest
@@ -102,3 +103,20 @@ def test_nvfp4_fill_and_gather_full_size(api, full):
     want = np.concatenate([n4.dequantize_rows(c2, s2, st), case.k_r[off:off + n].astype(np.float64)], axis=1)
     want_bits = (np.ascontiguousarray(want, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
     assert np.array_equal(out.view(torch.int16).cpu().numpy().astype(np.uint16), want_bits)
+    del out
+    # every sequence whole in one batched launch (the bench's launch); sampled rows bit for bit
+    lens = case.seq_lens.astype(np.int64)
+    offs = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    allout = torch.empty((int(offs[-1]), 576), dtype=torch.bfloat16, device="cuda")
+    api.mla_gather_paged_nvfp4_batch(rows, st, torch.from_numpy(case.block_table).cuda(),
+                                     torch.arange(case.B, dtype=torch.int32, device="cuda"),
+                                     torch.from_numpy(offs).cuda(), allout, dev_err)
+    assert api.mla_check(dev_err) == 0
+    g = np.sort(np.random.default_rng(6).choice(int(offs[-1]), size=1500, replace=False))
+    seq_of = np.searchsorted(offs, g, side="right") - 1
+    tok = case.tok_off[seq_of] + (g - offs[seq_of])          # the token's row in the case's inputs
+    c3, s3 = n4.quantize_rows(case.c_kv[tok], st)
+    want = np.concatenate([n4.dequantize_rows(c3, s3, st), case.k_r[tok].astype(np.float64)], axis=1)
+    want_bits = (np.ascontiguousarray(want, dtype=np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    got = allout[torch.from_numpy(g).cuda()].view(torch.int16).cpu().numpy().astype(np.uint16)
+    assert np.array_equal(got, want_bits)

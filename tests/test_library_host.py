@@ -279,6 +279,17 @@ def test_nvfp4_calls_validate_before_any_launch(api):
     assert lib.mla_gather_paged_nvfp4(ok, f(0.01), 4, ok, 1, 0, 65, ok, err, None) == 1
     assert lib.mla_gather_paged_nvfp4(ok, f(-2.0), 4, ok, 2, 0, 10, ok, err, None) == 1
     assert lib.mla_gather_paged_nvfp4(None, f(0.01), 4, ok, 2, 0, 0, None, None, None) == 0
+    # batched gather: rows, B, max_pages, seq_ids, out_offsets, nb, total, out
+    g = lib.mla_gather_paged_nvfp4_batch
+    assert g(None, f(0.01), 4, None, 1, 1, None, None, 0, 0, None, None, None) == 0
+    assert g(ok, f(0.01), 4, ok, 2, 2, ok, ok, -1, 10, ok, err, None) == 1
+    assert g(ok, f(0.01), 4, ok, 2, 2, ok, ok, 1, -10, ok, err, None) == 1
+    assert g(ok, f(0.0), 4, ok, 2, 2, ok, ok, 1, 10, ok, err, None) == 1
+    assert g(ok, f(0.01), 4, ok, 0, 2, ok, ok, 1, 10, ok, err, None) == 1
+    assert g(ok, f(0.01), 4, ok, 2, 2, None, ok, 1, 10, ok, err, None) == 1
+    assert g(odd, f(0.01), 4, ok, 2, 2, ok, ok, 1, 10, ok, err, None) == 2
+    assert g(ok, f(0.01), 4, ok, 2, 2, ok, P(0x10004), 1, 10, ok, err, None) == 2
+    assert g(ok, f(0.01), 4, ok, 2, 2, ok, ok, 1, 10, odd, err, None) == 2
 
 
 def test_fp8_and_decompress_calls_validate_before_any_launch(api):
