@@ -1,6 +1,6 @@
 // Inline-PTX building blocks for sm_103a: mbarriers with bounded waits, TMA
 // tensor loads, tcgen05 (TMEM allocation, MMA, loads/stores), cluster
-// addressing and st.async.  Written from the PTX ISA's public description of
+// addressing and bulk copies.  Written from the PTX ISA's public description of
 // these instructions.
 #pragma once
 
@@ -56,7 +56,7 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Acquire at cluster scope: pairs with data written into this CTA's shared
-// memory by the peer CTA (st.async completing on this barrier).
+// memory by the peer CTA (a bulk copy completing on this barrier).
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -149,15 +149,6 @@ __device__ __forceinline__ uint32_t mapa(uint32_t addr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
 }
-// 16-byte store into a peer CTA's shared memory, completing `bytes` of the
-// transaction count of the peer's mbarrier.
-__device__ __forceinline__ void st_async_v4(uint32_t raddr, float a, float b, float c, float d,
-                                            uint32_t rbar) {
-  asm volatile(
-      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(raddr),
-      "f"(a), "f"(b), "f"(c), "f"(d), "r"(rbar)
-      : "memory");
-}
 __device__ __forceinline__ float4 ld_shared_v4(uint32_t addr) {
   float4 v;
   asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
@@ -202,19 +193,9 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t rdst, uint32_t src, u
                "r"(src), "r"(bytes), "r"(rbar)
                : "memory");
 }
-// Arrive on a peer CTA's mbarrier, releasing this thread's prior accesses at cluster scope.
-__device__ __forceinline__ void mbar_arrive_remote(uint32_t rbar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(rbar) : "memory");
-}
 // Named barrier over `count` threads (whole warps).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-// 2^x with the hardware approximation (flush-to-zero); 2^-inf = +0.
-__device__ __forceinline__ float ex2_approx(float x) {
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
 }
 
 // ------------------------------------------------------------------ TMA
@@ -427,20 +408,6 @@ __device__ __forceinline__ void tmem_ld32_sync(uint32_t taddr, uint32_t (&r)[32]
                :
                : "memory");
 }
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&r)[8]) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
-               MLA_W8(r, 0)
-               : "memory");
-}
-// Load 16 columns and wait for completion (registers tied to the wait).
-__device__ __forceinline__ void tmem_ld16_sync(uint32_t taddr, uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-      : MLA_R8(r, 0), MLA_R8(r, 8)
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" : MLA_RW8(r, 0), MLA_RW8(r, 8) : : "memory");
-}
 // Load 64 columns (one row's whole tile slice) and wait; registers tied to the wait.
 __device__ __forceinline__ void tmem_ld64_sync(uint32_t taddr, uint32_t (&r)[64]) {
   asm volatile(
@@ -468,16 +435,6 @@ __device__ __forceinline__ uint32_t ex2_f16x2(uint32_t x) {
   uint32_t y;
   asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
   return y;
-}
-// fp16x2 of two values clamped to the finite fp16 range (no infinities).
-__device__ __forceinline__ uint32_t pack_f16x2_sat(float lo, float hi) {
-  lo = fminf(fmaxf(lo, -65504.f), 65504.f);
-  hi = fminf(fmaxf(hi, -65504.f), 65504.f);
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
-__device__ __forceinline__ float2 unpack_f16x2(uint32_t u) {
-  return __half22float2(*reinterpret_cast<const __half2*>(&u));
 }
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x (low half) = lo
