@@ -452,7 +452,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     // half): 8 codes in, one 16-byte f16 chunk out, written in the 128-byte
     // swizzled layout the tensor core reads.  The f16 rows overwrite the
     // codes, so every converter thread reads all of its codes first and the
-    // four warps meet at a named barrier before the first store.
+    // four warps meet at a named barrier before the first store.  A warp that
+    // leaves the loop (a wait gave up, or the CTA's abort flag is up) first
+    // arrives at that tile's barrier without waiting, so every warp counts
+    // exactly once for every tile any warp syncs on: the barrier always
+    // completes.  A warp leaves at its wait only after the abort flag was
+    // raised (by its own timeout or another's), and a warp that passed an
+    // earlier tile's barrier sees the flag at the next check.
     const int cw = warp - kConvWarp0;
     uint32_t G = 0;
     for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
@@ -462,9 +468,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     for (uint32_t t = 0; t < G; ++t) {
       const uint32_t st = t % kStages;
       const bool w = wait_phase<false, true>(BAR(B_F8_FULL + st), (t / kStages) & 1u, err, abort_flag);
-      // every converter warp takes this decision alike: all of them pass the
-      // barrier below or none does
-      if (!__all_sync(0xffffffffu, w)) break;
+      if (!__all_sync(0xffffffffu, w)) {
+        named_bar_arrive(kConvBarrier, kConvWarps * 32);
+        break;
+      }
       const uint32_t stage = base + kOffKV + st * kStageBytes;
       // All loads first (codes and row scales into registers), so that the
       // store loop holds no shared-memory load behind a store and its rows'
@@ -489,6 +496,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
         in_range = in_range && ok_j;
       }
       if (!in_range && lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_FP8_RANGE);  // warp-uniform
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) {
+        named_bar_arrive(kConvBarrier, kConvWarps * 32);
+        break;
+      }
       named_bar_sync(kConvBarrier, kConvWarps * 32);
 #pragma unroll
       for (int j0 = 0; j0 < kRows; j0 += kBatch) {

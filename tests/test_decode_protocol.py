@@ -91,7 +91,7 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             f8_full=[Barrier(1) for _ in range(n_stages)],
             stage=[None] * n_stages,        # (tile, "codes" | "bf16") held by a stage
             codes_read=[set() for _ in range(n_stages)],   # converter warps that have read this tile's codes
-            conv_bar=[0] * n_stages,        # converter warps arrived at the named barrier, per tile
+            conv=Barrier(WARPS),            # converters' mbarrier: phase t = every warp holds tile t's codes
             s_full=[Barrier(1), Barrier(1)], s_free=Barrier(WG_THREADS), p_full=Barrier(WG_THREADS),
             o_done=[Barrier(1), Barrier(1)], q_ready=Barrier(WG_THREADS), o_free=Barrier(WG_THREADS),
             x_full=[Barrier(1) for _ in range(XBUFS)],
@@ -127,8 +127,8 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             c["codes_read"][st].add(w)
             yield
             if not conv_no_barrier:
-                c["conv_bar"][st] += 1
-                while c["conv_bar"][st] < WARPS * (t // n_stages + 1):
+                c["conv"].arrive()
+                while not c["conv"].test(t):
                     yield
             if c["codes_read"][st] != set(range(WARPS)):
                 raise ProtocolError(f"converter {w} overwrites tile {t}'s codes before every warp read them")
@@ -330,6 +330,75 @@ def test_planted_fp8_protocol_mistakes_are_caught(mistake):
     for i, segs in enumerate(_layouts(60, 22)):
         try:
             run_model(segs + [1, 1, 3], seed=i, fp8=True, **mistake)
+        except ProtocolError:
+            caught += 1
+    assert caught > 0, f"the model did not catch {mistake}"
+
+
+def run_converter_abort_model(seed, tiles=6, warps=4, arrive_on_leave=True, check_flag=True):
+    """The FP8 converters' exit protocol around their named barrier.  Each tile
+    a warp passes its stage wait, or gives up (a timeout raises the CTA's abort
+    flag; a wait that finds the flag up gives up too); it then checks the
+    flag and syncs on the hardware barrier (which completes when `warps`
+    arrivals are in, then starts its next generation).  A warp that leaves
+    arrives first without waiting.  Returns once every warp has left or
+    finished; a warp blocked for good in the barrier is a deadlock."""
+    rnd = random.Random(seed)
+    st = {"flag": False, "count": 0, "gen": 0}
+    timeout_at = (rnd.randrange(warps), rnd.randrange(tiles))   # the warp and tile whose wait times out
+
+    def arrive():
+        st["count"] += 1
+        if st["count"] == warps:
+            st["count"] = 0
+            st["gen"] += 1
+
+    def warp(w):
+        for t in range(tiles):
+            yield
+            gave_up = st["flag"] and rnd.random() < 0.5        # a wait that finds the flag up may give up
+            if (w, t) == timeout_at:
+                st["flag"] = True
+                gave_up = True
+            if gave_up:
+                if arrive_on_leave:
+                    arrive()
+                return
+            yield
+            if check_flag and st["flag"]:
+                if arrive_on_leave:
+                    arrive()
+                return
+            g = st["gen"]
+            arrive()
+            while st["gen"] == g:
+                yield
+
+    roles = {w: warp(w) for w in range(warps)}
+    idle = 0
+    while roles:
+        key = rnd.choice(list(roles))
+        try:
+            next(roles[key])
+            idle += 1
+        except StopIteration:
+            del roles[key]
+            idle = 0
+        if idle > 5000:
+            raise ProtocolError(f"converter warps {sorted(roles)} blocked in the barrier")
+
+
+def test_converter_exit_never_blocks_a_warp():
+    for seed in range(400):
+        run_converter_abort_model(seed)
+
+
+@pytest.mark.parametrize("mistake", [dict(arrive_on_leave=False), dict(check_flag=False)])
+def test_converter_exit_mistakes_are_caught(mistake):
+    caught = 0
+    for seed in range(400):
+        try:
+            run_converter_abort_model(seed, **mistake)
         except ProtocolError:
             caught += 1
     assert caught > 0, f"the model did not catch {mistake}"
