@@ -7,7 +7,7 @@
 // and m = max_i lse_i.
 //
 // One CTA = one split row and HPC heads; TPH threads per head, each with QPT
-// of the head's 128 column quads (float4), loaded for a piece all at once.
+// of the head's 128 column quads (float4), loaded for two pieces at once.
 // Many split rows: 16 heads x 16 threads x 8 quads (one wave covers the
 // merge); few (one or sixteen query rows cut into many pieces): one head x
 // 128 threads x 1 quad, so that the few rows spread over many SMs.
@@ -36,27 +36,41 @@ __global__ void __launch_bounds__(HPC * 128 / QPT) combine_kernel(const CombineA
     if (tid == 0) atomicOr(a.dev_err, (int32_t)MLA_DEVERR_PLAN);
     return;
   }
-  float mx = -INFINITY;
-  for (int i = 0; i < n; ++i) mx = fmaxf(mx, __ldg(a.part_lse + (size_t)(s0 + i) * kH + h));
-  float wsum = 0.f;
+  // One pass over the pieces, two at a time, with a running maximum: both
+  // pieces' outputs and log-sum-exps are loaded together, so a row of two
+  // pieces costs one round of loads.
+  float mx = -INFINITY, wsum = 0.f;
   float4 acc[QPT];
 #pragma unroll
   for (int k = 0; k < QPT; ++k) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   const uint64_t last_use = l2_policy_evict_first();  // the partials' only read
-#pragma unroll(QPT == 1 ? 4 : 1)
-  for (int i = 0; i < n; ++i) {
-    const float w = exp2f(__ldg(a.part_lse + (size_t)(s0 + i) * kH + h) - mx);
-    const float4* src = reinterpret_cast<const float4*>(a.part_o + ((size_t)(s0 + i) * kH + h) * kDC) + q0;
-    float4 v[QPT];
+#pragma unroll 1
+  for (int i = 0; i < n; i += 2) {
+    const bool two = i + 1 < n;
+    const float la = __ldg(a.part_lse + (size_t)(s0 + i) * kH + h);
+    const float lb = two ? __ldg(a.part_lse + (size_t)(s0 + i + 1) * kH + h) : -INFINITY;
+    const float4* pa = reinterpret_cast<const float4*>(a.part_o + ((size_t)(s0 + i) * kH + h) * kDC) + q0;
+    float4 va[QPT], vb[QPT];
 #pragma unroll
-    for (int k = 0; k < QPT; ++k) v[k] = ld_global_v4_hint(src + kTPH * k, last_use);
-    wsum += w;
+    for (int k = 0; k < QPT; ++k) va[k] = ld_global_v4_hint(pa + kTPH * k, last_use);
+    if (two) {
+      const float4* pb = pa + (size_t)kH * kDC / 4;
+#pragma unroll
+      for (int k = 0; k < QPT; ++k) vb[k] = ld_global_v4_hint(pb + kTPH * k, last_use);
+    } else {
+#pragma unroll
+      for (int k = 0; k < QPT; ++k) vb[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    const float mn = fmaxf(mx, fmaxf(la, lb));
+    const float sc = exp2f(mx - mn), wa = exp2f(la - mn), wb = two ? exp2f(lb - mn) : 0.f;
+    mx = mn;
+    wsum = wsum * sc + wa + wb;
 #pragma unroll
     for (int k = 0; k < QPT; ++k) {
-      acc[k].x += w * v[k].x;
-      acc[k].y += w * v[k].y;
-      acc[k].z += w * v[k].z;
-      acc[k].w += w * v[k].w;
+      acc[k].x = acc[k].x * sc + wa * va[k].x + wb * vb[k].x;
+      acc[k].y = acc[k].y * sc + wa * va[k].y + wb * vb[k].y;
+      acc[k].z = acc[k].z * sc + wa * va[k].z + wb * vb[k].z;
+      acc[k].w = acc[k].w * sc + wa * va[k].w + wb * vb[k].w;
     }
   }
   const float inv = 1.f / wsum;
