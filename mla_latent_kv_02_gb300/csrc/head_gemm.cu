@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(128, 2)
         bulk_commit_group();
       }
     }
-    if (threadIdx.x == 0) bulk_wait_all();
+    if (threadIdx.x == 0) bulk_wait_all_read();  // the staging ring is released at exit
   }
   tc_fence_before();
   __syncthreads();

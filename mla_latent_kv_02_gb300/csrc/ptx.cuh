@@ -280,8 +280,12 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// Every bulk store this thread committed has completed (its writes are done).
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+// Every bulk store this thread committed has read its shared-memory source
+// (the source may be reused or released; the global writes complete before
+// the grid does).
+__device__ __forceinline__ void bulk_wait_all_read() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
 
 // ------------------------------------------------------------------ tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
