@@ -502,6 +502,20 @@ mla_status mla_gather_paged_nvfp4_batch(const void* rows, float tensor_scale, in
  */
 mla_status mla_check(void* stream, const int32_t* dev_err, int32_t* word_out);
 
+/*
+ * Test hook for the decode kernel's failure path (no counterpart on the
+ * source pages; they describe no failure handling).  Every wait inside the
+ * decode loop (mla_decode_paged, mla_decode_paged_fp8 and the entry points
+ * built on them) gives up after `cycles` SM clock cycles, sets
+ * MLA_DEVERR_TIMEOUT in the call's dev_err, and the kernel stops: it waits
+ * for its own loads, MMAs and the score copies already in flight, frees its
+ * tensor memory and returns, so the context stays usable.  0 restores the
+ * default, 2^31 cycles (about a second at the maximum SM clock).  The
+ * setting is process-wide and applies to launches made after the call.
+ * Errors: MLA_ERR_INVALID_ARG if cycles exceeds the default.
+ */
+mla_status mla_debug_set_decode_wait_limit(uint64_t cycles);
+
 #ifdef __cplusplus
 }
 #endif

@@ -73,6 +73,7 @@ SIGNATURES = {
     "mla_decode_paged_fp8": (C.c_int, [P, P, P, P, I64, P, I32, P, C.POINTER(mla_plan_info), C.c_float, P, SZ, P, P,
                                        P, P]),
     "mla_check": (C.c_int, [P, P, PI32]),
+    "mla_debug_set_decode_wait_limit": (C.c_int, [C.c_uint64]),
     "mla_decode_paged_noalloc": (C.c_int, [P, P, P, I64, P, I32, PI32, PI32, I32, C.c_float, P, P, P, P]),
 }
 

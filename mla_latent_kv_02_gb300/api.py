@@ -464,6 +464,12 @@ def mla_check(dev_err, stream=None) -> int:
     return int(word.value)
 
 
+def mla_debug_set_decode_wait_limit(cycles: int) -> None:
+    """Test hook: every wait of the decode loop gives up after `cycles` SM
+    cycles (0 restores the default of 2^31); process-wide."""
+    _check(lib().mla_debug_set_decode_wait_limit(int(cycles)))
+
+
 def mla_decode_paged_noalloc(q_abs, q_r, kv_cache, block_table, seq_lens, q_lens, o_lat, dev_err, lse=None,
                              scale: float = 1.0 / (192 ** 0.5), stream=None) -> None:
     """mla_decode_paged without caller-provided plan or workspace: for callers

@@ -45,6 +45,10 @@
 //  * Work: the plan cuts all rows' 64-token tiles into equal contiguous ranges,
 //    one per cluster; a row cut by a boundary is written as fp32 partials
 //    (normalised O and log2-sum-exp) and merged by the combine kernel.
+//  * Every wait in the loop is bounded (DecodeArgs::wait_limit); on expiry the
+//    kernel raises an abort flag that every role polls, drains its own TMA
+//    loads and MMAs, waits until the score copies the peer already issued
+//    into this CTA have landed, frees TMEM and returns.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -96,7 +100,12 @@ constexpr int kNumBars = 32;
 constexpr int kSmallBar = 0;
 constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [4][128]: {reference max bits, tile}
 constexpr int kSmallMisc = kSmallPair + 4 * kH * 8;
-constexpr int kSmallBytes = kSmallMisc + 64;
+// misc: +0 abort flag, +8 TMEM address, +16 segment range [2], +32 copies
+// issued per softmax warp [8], +64 the peer's copies [8] (written by the
+// peer), +96 the abort flags of this CTA and the peer [2], +104 the last tile
+// armed on each exchange buffer [4].
+constexpr int kMiscPush = 32, kMiscPeerPush = 64, kMiscAborts = 96, kMiscArmed = 104;
+constexpr int kSmallBytes = kSmallMisc + 128;
 
 // The two cache formats.  bf16: the producer's TMA fills a 4-deep ring of
 // [latent half | RoPE half] stages.  FP8: the TMA fills the same 4-deep ring
@@ -231,6 +240,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem_raw + kSmallMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + kSmallMisc + 8);
   int32_t* seg_range = reinterpret_cast<int32_t*>(smem_raw + kSmallMisc + 16);
+  uint32_t* push_cnt = reinterpret_cast<uint32_t*>(smem_raw + kSmallMisc + kMiscPush);
+  volatile uint32_t* peer_push = reinterpret_cast<volatile uint32_t*>(smem_raw + kSmallMisc + kMiscPeerPush);
+  volatile int32_t* aborts = reinterpret_cast<volatile int32_t*>(smem_raw + kSmallMisc + kMiscAborts);
+  int32_t* armed = reinterpret_cast<int32_t*>(smem_raw + kSmallMisc + kMiscArmed);
   const uint32_t base = (raw + kSmallBytes + 1023u) & ~1023u;
   const bool layout_fits = base + kAlignedBytes <= raw + kSmemBytes;
 #define BAR(i) (bars + 8u * (uint32_t)(i))
@@ -256,7 +269,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     mbar_init(BAR(B_O_DONE1), 1);
     mbar_init(BAR(B_Q_READY), kTileThreads);
     mbar_init(BAR(B_O_FREE), kTileThreads);
-    for (int i = 0; i < kXBufs; ++i) mbar_init(BAR(B_X_FULL0 + i), 1);
+    for (int i = 0; i < kXBufs; ++i) {
+      mbar_init(BAR(B_X_FULL0 + i), 1);
+      armed[i] = -1;
+    }
+    for (int i = 0; i < kSWarps; ++i) {
+      push_cnt[i] = 0u;
+      peer_push[i] = 0u;
+    }
+    aborts[0] = aborts[1] = 0;
     mbar_init(BAR(B_DRAIN), 1);
     mbar_init(BAR(B_DRAIN_PV), 1);
     fence_mbar_init();
@@ -330,7 +351,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
             prefetch_l2_bulk(qa + rank * (kH * kDC), kH * kDC);
             if (rank == 0) prefetch_l2_bulk(reinterpret_cast<const uint8_t*>(a.q_r) + qrow * (kH * kDR * 2), kH * kDR * 2);
           }
-          if (use > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_KV_EMPTY + st), (use - 1) & 1u, err, abort_flag)) {
+          if (use > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_KV_EMPTY + st), (use - 1) & 1u, err, abort_flag, a.wait_limit, a.wait_every)) {
             ok = false;
             break;
           }
@@ -378,13 +399,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       const uint64_t rdesc0 = sdesc_sw64(base + kOffKV + 4 * kChunkBytes, 16, 512);
       for (uint32_t tq = 0; cq.valid(); ++tq) {
         const uint32_t st = tq % kStages;
-        if (!wait_phase<false, kIssueSuspend>(BAR(B_KV_FULL + st), (tq / kStages) & 1u, err, abort_flag)) break;
+        if (!wait_phase<false, kIssueSuspend>(BAR(B_KV_FULL + st), (tq / kStages) & 1u, err, abort_flag, a.wait_limit, a.wait_every)) break;
         // FP8: the RoPE half came with the codes (already complete; waited for its TMA visibility)
-        if (kF8 && !wait_phase<false, kIssueSuspend>(BAR(B_F8_FULL + st), (tq / kStages) & 1u, err, abort_flag))
+        if (kF8 && !wait_phase<false, kIssueSuspend>(BAR(B_F8_FULL + st), (tq / kStages) & 1u, err, abort_flag, a.wait_limit, a.wait_every))
           break;
-        if (tq > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_S_FREE), (tq - 1) & 1u, err, abort_flag)) break;
+        if (tq > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_S_FREE), (tq - 1) & 1u, err, abort_flag, a.wait_limit, a.wait_every)) break;
         if (cq.first() &&
-            !wait_phase<false, kIssueSuspend>(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u, err, abort_flag))
+            !wait_phase<false, kIssueSuspend>(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u, err, abort_flag, a.wait_limit, a.wait_every))
           break;
         tc_fence_after();
         // [128 x 64] += Q_r[128 x 288] · K_r^T, K-major, 16 per step: 4 latent
@@ -419,8 +440,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       const uint64_t odesc0 = sdesc_sw128(base + kOffOnes, 16, 1024);
       for (uint32_t tp = 0; cp.valid(); ++tp) {
         const bool first = cp.first();
-        if (!wait_phase<false, kIssueSuspend>(BAR(B_P_FULL), tp & 1u, err, abort_flag)) break;
-        if (first && !wait_phase<false, kIssueSuspend>(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u, err, abort_flag))
+        if (!wait_phase<false, kIssueSuspend>(BAR(B_P_FULL), tp & 1u, err, abort_flag, a.wait_limit, a.wait_every)) break;
+        if (first && !wait_phase<false, kIssueSuspend>(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u, err, abort_flag, a.wait_limit, a.wait_every))
           break;
         tc_fence_after();
         // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
@@ -467,7 +488,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     constexpr int kBatch = 4;
     for (uint32_t t = 0; t < G; ++t) {
       const uint32_t st = t % kStages;
-      const bool w = wait_phase<false, true>(BAR(B_F8_FULL + st), (t / kStages) & 1u, err, abort_flag);
+      const bool w = wait_phase<false, true>(BAR(B_F8_FULL + st), (t / kStages) & 1u, err, abort_flag, a.wait_limit, a.wait_every);
       if (!__all_sync(0xffffffffu, w)) {
         named_bar_arrive(kConvBarrier, kConvWarps * 32);
         break;
@@ -615,7 +636,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     // t ends a segment (its QK^T was the segment's last).  `own` keeps the
     // rounded values.
     auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[kWords]) -> bool {
-      bool w = wait_phase<false, true>(BAR(B_S_FULL0 + (t & 1u)), (t >> 1) & 1u, err, abort_flag);
+      bool w = wait_phase<false, true>(BAR(B_S_FULL0 + (t & 1u)), (t >> 1) & 1u, err, abort_flag, a.wait_limit, a.wait_every);
       if (!__all_sync(0xffffffffu, w)) return false;
       tc_fence_after();
       {
@@ -641,9 +662,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
                      own[4 * k + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      if (lane == 0)
+      if (lane == 0) {
         bulk_copy_to_peer(mapa(base + kOffX + (t % kXBufs) * kXBytes + warp_off, peer), stage + warp_off,
                           (uint32_t)kXWarp, mapa(BAR(B_X_FULL0 + t % kXBufs), peer));
+        push_cnt[sw] += 1u;  // copies this warp issued into the peer
+      }
       if (c.last() && c.s + 1 < c.s_end) load_q(c.s + 1);
       return true;
     };
@@ -654,8 +677,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
 
     if (wg == 0) mbar_arrive(BAR(B_O_FREE));  // O is free for the first segment
     if (sw == 0 && lane == 0)                  // arm the ring: the first kXBufs tiles each expect one peer push
-      for (uint32_t t = 0; t < G && t < (uint32_t)kXBufs; ++t)
+      for (uint32_t t = 0; t < G && t < (uint32_t)kXBufs; ++t) {
         mbar_arrive_expect_tx(BAR(B_X_FULL0 + t), (uint32_t)kXBytes);
+        armed[t] = (int32_t)t;
+      }
     TileCursor cf;  // this warpgroup's tile
     cf.init(a.segs, s_begin, s_end);
     if (wg == 1 && cf.valid()) cf.next();
@@ -669,7 +694,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       }
       // ---- add the peer's half (fp16, unscaled)
       const uint32_t xb = g % kXBufs;
-      bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag);
+      bool w = wait_phase<true, true>(BAR(B_X_FULL0 + xb), (g / kXBufs) & 1u, err, abort_flag, a.wait_limit, a.wait_every);
       if (!__all_sync(0xffffffffu, w)) {
         ok = false;
         break;
@@ -677,7 +702,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       // Re-arm this buffer's barrier for tile g + kXBufs (this warpgroup's
       // again).  That push cannot land before this warpgroup has pushed tile
       // g + kXBufs - kXLead, which it does only after finishing tile g.
-      if (wg_leader && g + kXBufs < G) mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
+      if (wg_leader && g + kXBufs < G) {
+        mbar_arrive_expect_tx(BAR(B_X_FULL0 + xb), (uint32_t)kXBytes);
+        armed[xb] = (int32_t)(g + kXBufs);
+      }
       const uint32_t recv = base + kOffX + xb * kXBytes + row_off;
 #pragma unroll
       for (int k = 0; k < 8; ++k) {
@@ -716,7 +744,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
         if (v.y != g - 1) {
           const uint64_t t0 = cycles();
           for (uint32_t it = 1; (v = ld_shared_v2_volatile(slot)).y != g - 1; ++it) {
-            if ((it & 255u) == 0u && (*abort_flag || cycles() - t0 > kWaitLimitCycles)) {
+            if ((it & a.wait_every) == 0u && (*abort_flag || cycles() - t0 > a.wait_limit)) {
               if (!*abort_flag) atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
               *abort_flag = 1;
               break;
@@ -758,7 +786,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       }
       // Writing P (single TMEM buffer) and a rescale both need P·V of tile g-1 done.
       if (g > 0) {
-        w = od_ready || wait_phase<false, true>(BAR(B_O_DONE0 + (gp & 1u)), (gp >> 1) & 1u, err, abort_flag);
+        w = od_ready || wait_phase<false, true>(BAR(B_O_DONE0 + (gp & 1u)), (gp >> 1) & 1u, err, abort_flag, a.wait_limit, a.wait_every);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
@@ -785,7 +813,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       if (cf.last()) {
         // ---- epilogue of this segment: wait for its last P·V, normalise, store
         const int row = cf.row, slot = cf.slot;
-        w = wait_phase(BAR(B_O_DONE0 + (g & 1u)), (g >> 1) & 1u, err, abort_flag);
+        w = wait_phase(BAR(B_O_DONE0 + (g & 1u)), (g >> 1) & 1u, err, abort_flag, a.wait_limit, a.wait_every);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
@@ -870,7 +898,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+  // Every role is done, so every score copy either CTA will ever issue has
+  // been issued.  On the normal path each one was awaited by its receiver.
+  // After an abort some may still be in flight: tell the peer how many copies
+  // each softmax warp issued, and whether this CTA aborted.
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < kSWarps; ++i)
+      st_cluster_u32(mapa(raw + kSmallMisc + kMiscPeerPush + 4u * i, peer), push_cnt[i]);
+    const int32_t mine = *abort_flag;
+    aborts[0] = mine;
+    st_cluster_u32(mapa(raw + kSmallMisc + kMiscAborts + 4u, peer), (uint32_t)mine);
+  }
   cluster_sync();  // neither CTA leaves while its peer may still address its shared memory
+  if (aborts[0] != 0 || aborts[1] != 0) {
+    // Drain: each exchange buffer has at most one armed phase this CTA did not
+    // see complete.  The peer's counts say how many of that tile's four
+    // per-warp copies it issued; the bytes of the copies never issued are
+    // retired by hand, and the phase then completes once the issued ones land.
+    if (threadIdx.x == 0) {
+      for (int b = 0; b < kXBufs; ++b) {
+        const int32_t t = armed[b];
+        if (t < 0) continue;
+        const uint32_t par = ((uint32_t)t / kXBufs) & 1u;
+        if (mbar_test_wait_cluster(BAR(B_X_FULL0 + b), par)) continue;
+        const uint32_t idx = (uint32_t)t >> 1, pg = (uint32_t)t & 1u;
+        uint32_t issued = 0;
+        for (int q = 0; q < 4; ++q) issued += peer_push[pg * 4 + q] > idx ? 1u : 0u;
+        if (issued < 4) mbar_complete_tx(BAR(B_X_FULL0 + b), (4u - issued) * (uint32_t)kXWarp);
+        const uint64_t t0 = cycles();
+        while (!mbar_test_wait_cluster(BAR(B_X_FULL0 + b), par) && cycles() - t0 < kWaitLimitCycles) {
+        }
+      }
+    }
+    // and neither CTA leaves while a copy out of its shared memory may still be reading it
+    cluster_sync();
+  }
 #undef BAR
 }
 

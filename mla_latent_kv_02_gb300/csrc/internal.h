@@ -63,6 +63,13 @@ struct DecodeArgs {
   int32_t num_segments;
   int32_t num_partials;
   const float* kv_scales;  // FP8 cache: fp32 [num_pages * 64] token scales (null for bf16)
+  // Bound, in SM cycles, of every wait in the decode loop (the drains before
+  // exit keep the full default bound).
+  uint64_t wait_limit;
+  // The deadline is checked when a wait's probe count & wait_every is 0
+  // (255 for the default bound; 0, every probe, for a short test bound).
+  uint32_t wait_every;
+  int32_t pad3_;
 };
 
 // Decompress branch: one sequence, M query rows at positions N - M .. N - 1.

@@ -6,6 +6,7 @@
 #include <cudaTypedefs.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -21,6 +22,11 @@
 namespace {
 
 thread_local std::string g_last_error = "no error";
+
+// Bound of the decode kernel's waits, in SM cycles (about a second at the
+// maximum clock); mla_debug_set_decode_wait_limit changes it for tests.
+constexpr uint64_t kDefaultDecodeWaitLimit = 1ull << 31;
+std::atomic<uint64_t> g_decode_wait_limit{kDefaultDecodeWaitLimit};
 
 mla_status fail(mla_status s, const char* fmt, ...) {
   char buf[512];
@@ -958,6 +964,8 @@ static mla_status decode_common(const void* q_abs, const void* q_r, const void* 
   a.num_segments = info->num_segments;
   a.num_partials = info->num_partials;
   a.kv_scales = fp8 ? kv_scales : nullptr;
+  a.wait_limit = g_decode_wait_limit.load(std::memory_order_relaxed);
+  a.wait_every = a.wait_limit < (1ull << 20) ? 0u : 255u;
   cudaError_t e = mla::launch_decode(kv_map, rope_map, a, info->num_clusters, fp8, (cudaStream_t)stream);
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   if (info->num_split_rows > 0) {
@@ -990,6 +998,14 @@ mla_status mla_decode_paged_fp8(const void* q_abs, const void* q_r, const void* 
                                 size_t ws_bytes, void* o_lat, float* lse, int32_t* dev_err, void* stream) {
   return decode_common(q_abs, q_r, rows, scales, num_pages, block_table, max_pages, plan_dev, info, scale,
                        workspace, ws_bytes, o_lat, lse, dev_err, stream, true);
+}
+
+mla_status mla_debug_set_decode_wait_limit(uint64_t cycles) {
+  if (cycles > kDefaultDecodeWaitLimit)
+    return fail(MLA_ERR_INVALID_ARG, "wait limit %llu above the default %llu", (unsigned long long)cycles,
+                (unsigned long long)kDefaultDecodeWaitLimit);
+  g_decode_wait_limit.store(cycles == 0 ? kDefaultDecodeWaitLimit : cycles, std::memory_order_relaxed);
+  return MLA_OK;
 }
 
 mla_status mla_check(void* stream, const int32_t* dev_err, int32_t* word_out) {

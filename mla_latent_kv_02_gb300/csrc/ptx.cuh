@@ -100,9 +100,13 @@ __device__ __forceinline__ bool mbar_test_wait_cluster(uint32_t bar, uint32_t pa
 // kSuspend: the thread may be suspended inside the probe (mbarrier.try_wait),
 // which frees issue slots for other warps at the cost of a later wake-up; for
 // roles that run ahead of the critical path.
+// limit: the bound in SM cycles; every: the deadline is checked when the
+// probe count & every is 0 (255 for the default bound, 0 — at every probe —
+// for a short one, a test of the failure path).
 template <bool kCluster = false, bool kSuspend = false>
 __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_t* err,
-                                           volatile int32_t* abort_flag) {
+                                           volatile int32_t* abort_flag, uint64_t limit = kWaitLimitCycles,
+                                           uint32_t every = 255u) {
   auto probe = [&]() -> bool {
     if (kSuspend) return kCluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity);
     return kCluster ? mbar_test_wait_cluster(bar, parity) : mbar_test_wait(bar, parity);
@@ -111,9 +115,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, int32_
   const uint64_t t0 = cycles();
   for (uint32_t i = 1;; ++i) {
     if (probe()) return true;
-    if ((i & 255u) == 0u) {
+    if ((i & every) == 0u) {
       if (*abort_flag) return false;
-      if (cycles() - t0 > kWaitLimitCycles) {
+      if (cycles() - t0 > limit) {
         atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
         *abort_flag = 1;
         return false;
@@ -129,6 +133,12 @@ __device__ __forceinline__ void wait_phase_drain(uint32_t bar, uint32_t parity) 
   while (!mbar_test_wait(bar, parity)) {
     if (cycles() - t0 > kWaitLimitCycles) return;
   }
+}
+
+// Count `tx` bytes as arrived on this CTA's mbarrier without any copy (used to
+// retire the part of an armed phase whose copies were never issued).
+__device__ __forceinline__ void mbar_complete_tx(uint32_t bar, uint32_t tx) {
+  asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(tx) : "memory");
 }
 
 // ------------------------------------------------------------------ cluster
@@ -169,6 +179,10 @@ __device__ __forceinline__ uint2 ld_shared_v2_volatile(uint32_t addr) {
   uint2 v;
   asm volatile("ld.volatile.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(addr) : "memory");
   return v;
+}
+// Plain 32-bit store into a peer CTA's shared memory (address from mapa).
+__device__ __forceinline__ void st_cluster_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 __device__ __forceinline__ uint2 ld_shared_v2(uint32_t addr) {
   uint2 v;

@@ -67,13 +67,20 @@ class Barrier:
 
 
 def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv_no_barrier=False,
-              conv_skips_f8_full=False):
+              conv_skips_f8_full=False, abort_at=None, drain=True):
     """fp8: the FP8 layout — the producer's TMA fills stage t mod STAGES with
     codes, the converter warps read all of their codes, meet at a barrier and
     write the bf16 rows over them, and QK^T waits for all converter warps.
     Planted mistakes: converters without the barrier (a warp overwrites codes
     another warp has not read yet) and converters that do not wait for the
-    codes to land."""
+    codes to land.
+    abort_at: (cta, step) — that CTA's abort flag goes up after `step` model
+    steps (a wait that timed out); every role then leaves at its next wait.
+    After the roles, each CTA tells the peer how many score copies each warp
+    issued, both meet at the cluster barrier, a CTA that or whose peer aborted
+    drains the copies still in flight into it (retiring by hand the bytes of
+    copies never issued), and both meet again before they exit.  drain=False
+    plants the mistake of exiting without the drain."""
     rnd = random.Random(seed)
     n_stages = STAGES
     tiles = []
@@ -98,8 +105,25 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             xbuf=[[None] * WARPS for _ in range(XBUFS)],   # region state per (buffer, row block)
             reading=[[False] * WARPS for _ in range(XBUFS)],  # a copy out of this region is in flight
             slot=[[None] * WARPS for _ in range(slots)], slot_unread=[[False] * WARPS for _ in range(slots)],
+            abort=False, pushes=[0] * (2 * WARPS), peer_pushes=None, peer_abort=None,
+            armed=[-1] * XBUFS, exited=False,
         ))
     events = []
+
+    def wait(c, cond):
+        """Yield until cond() holds; False if the CTA's abort flag went up
+        first.  Once either CTA has aborted, a wait also gives up (and raises
+        its own CTA's flag) after a while: the kernel's waits are bounded."""
+        n = 0
+        while not cond():
+            if c["abort"]:
+                return False
+            n += 1
+            if n > 200 and any(x["abort"] for x in ctas):
+                c["abort"] = True
+                return False
+            yield
+        return True
 
     def s_full_bar(c, t):
         return (c["s_full"][0], t) if shared_s_full else (c["s_full"][t & 1], t >> 1)
@@ -111,8 +135,8 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
         c = ctas[ci]
         for t in range(G):
             if t >= STAGES:
-                while not c["kv_empty"][t % STAGES].test(t // STAGES - 1):
-                    yield
+                if not (yield from wait(c, lambda: c["kv_empty"][t % STAGES].test(t // STAGES - 1))):
+                    return
             events.append(("f8" if fp8 else "kv", ci, t))
 
     def converter(ci, w):
@@ -120,8 +144,8 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
         for t in range(G):
             st = t % n_stages
             if not conv_skips_f8_full:
-                while not c["f8_full"][st].test(t // n_stages):
-                    yield
+                if not (yield from wait(c, lambda: c["f8_full"][st].test(t // n_stages))):
+                    return
             if c["stage"][st] != (t, "codes"):
                 raise ProtocolError(f"converter {w} reads tile {t}'s codes from a stage holding {c['stage'][st]}")
             c["codes_read"][st].add(w)
@@ -141,31 +165,31 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
     def qk(ci):
         c = ctas[ci]
         for t in range(G):
-            while not c["kv_full"][t % n_stages].test(t // n_stages):
-                yield
+            if not (yield from wait(c, lambda: c["kv_full"][t % n_stages].test(t // n_stages))):
+                return
             if fp8:
-                while not c["f8_full"][t % n_stages].test(t // n_stages):
-                    yield
+                if not (yield from wait(c, lambda: c["f8_full"][t % n_stages].test(t // n_stages))):
+                    return
                 if c["stage"][t % n_stages] != (t, "bf16"):
                     raise ProtocolError(f"QK^T of tile {t} reads a stage holding {c['stage'][t % n_stages]}")
             if t > 0:
-                while not c["s_free"].test(t - 1):
-                    yield
+                if not (yield from wait(c, lambda: c["s_free"].test(t - 1))):
+                    return
             seg, first, _ = tiles[t]
             if first:
-                while not c["q_ready"].test(seg):
-                    yield
+                if not (yield from wait(c, lambda: c["q_ready"].test(seg))):
+                    return
             events.append(("s", ci, t))
 
     def pv(ci):
         c = ctas[ci]
         for t in range(G):
-            while not c["p_full"].test(t):
-                yield
+            if not (yield from wait(c, lambda: c["p_full"].test(t))):
+                return
             seg, first, _ = tiles[t]
             if first:
-                while not c["o_free"].test(seg):
-                    yield
+                if not (yield from wait(c, lambda: c["o_free"].test(seg))):
+                    return
             if fp8 and c["stage"][t % n_stages] != (t, "bf16"):
                 raise ProtocolError(f"P·V of tile {t} reads a stage holding {c['stage'][t % n_stages]}")
             events.append(("o", ci, t))
@@ -178,11 +202,12 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             if w == 0:
                 for t in range(min(G, XBUFS)):
                     c["x_full"][t].arrive(1, expect_tx=WARPS)
+                    c["armed"][t] = t
         for t in range(wg, G, 2):
             seg, first, last = tiles[t]
             bar, k = s_full_bar(c, t)
-            while not bar.test(k):
-                yield
+            if not (yield from wait(c, lambda: bar.test(k))):
+                return
             c["s_free"].arrive(per_warp)
             # stage this row block's scores and push them to the peer
             sb = (t + xlead) % XBUFS
@@ -194,23 +219,25 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             c["xbuf"][sb][w] = ("stage", t)
             c["reading"][sb][w] = True
             events.append(("x", ci, (t, w, sb)))
+            c["pushes"][wg * WARPS + w] += 1
             if last and seg + 1 < len(segs):
                 c["q_ready"].arrive(per_warp)
             yield
             # the peer's half of tile t
             b = t % XBUFS
-            while not c["x_full"][b].test(t // XBUFS):
-                yield
+            if not (yield from wait(c, lambda: c["x_full"][b].test(t // XBUFS))):
+                return
             if c["xbuf"][b][w] != ("data", t):
                 raise ProtocolError(f"tile {t} reads {c['xbuf'][b][w]}")
             c["xbuf"][b][w] = None
             if w == 0 and t + XBUFS < G:
                 c["x_full"][b].arrive(1, expect_tx=WARPS)
+                c["armed"][b] = t + XBUFS
             # reference max from tile t-1
             if not first:
                 sl = (t - 1) % slots
-                while c["slot"][sl][w] != t - 1:
-                    yield
+                if not (yield from wait(c, lambda: c["slot"][sl][w] == t - 1)):
+                    return
                 c["slot_unread"][sl][w] = False
             sl = t % slots
             if c["slot_unread"][sl][w]:
@@ -220,14 +247,45 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             yield
             if t > 0:
                 bar, k = o_done_bar(c, t - 1)
-                while not bar.test(k):
-                    yield
+                if not (yield from wait(c, lambda: bar.test(k))):
+                    return
             c["p_full"].arrive(per_warp)
             if last:
                 bar, k = o_done_bar(c, t)
-                while not bar.test(k):
-                    yield
+                if not (yield from wait(c, lambda: bar.test(k))):
+                    return
                 c["o_free"].arrive(per_warp)
+
+    def exit_sequence(ci):
+        """After the roles: counts to the peer, cluster barrier, drain, barrier."""
+        c, p = ctas[ci], ctas[1 - ci]
+        p["peer_pushes"] = list(c["pushes"])
+        p["peer_abort"] = c["abort"]
+        c["at_barrier"] = 1
+        while p.get("at_barrier", 0) < 1:
+            yield
+        if drain and (c["abort"] or c["peer_abort"]):
+            for b in range(XBUFS):
+                t = c["armed"][b]
+                if t < 0:
+                    continue
+                k = t // XBUFS
+                xb = c["x_full"][b]
+                if xb.phase >= k + 1:
+                    continue
+                idx, pg = t >> 1, t & 1
+                issued = sum(1 for q in range(WARPS) if c["peer_pushes"][pg * WARPS + q] > idx)
+                if issued < WARPS:
+                    xb.complete_tx(WARPS - issued)
+                while xb.phase < k + 1:
+                    yield
+            c["at_barrier"] = 2
+            while p.get("at_barrier", 0) < 2 and not p["exited"]:
+                yield
+        c["exited"] = True
+        for kind, cj, payload in events:
+            if kind == "x":
+                raise ProtocolError(f"CTA {ci} exits with a score copy of CTA {cj} in flight")
 
     roles = {}
     for ci in range(2):
@@ -241,8 +299,20 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             for w in range(WARPS):
                 roles[("sm", ci, wg, w)] = softmax_warp(ci, wg, w)
     idle = 0
+    pending_exit = {0, 1}
+    steps = 0
     while roles or events:
+        steps += 1
+        if abort_at is not None and steps == abort_at[1]:
+            ctas[abort_at[0]]["abort"] = True
+        for ci in list(pending_exit):
+            if not any(key[1] == ci for key in roles):
+                pending_exit.discard(ci)
+                roles[("exit", ci)] = exit_sequence(ci)
         pick = rnd.randrange(len(roles) + len(events))
+        if pick >= len(roles) and abort_at is not None and events[pick - len(roles)][0] == "x" \
+                and rnd.random() < 0.95:
+            pick = rnd.randrange(len(roles)) if roles else pick  # copies in flight linger after an abort
         if pick >= len(roles):
             kind, ci, t = events.pop(pick - len(roles))
             c = ctas[ci]
@@ -267,6 +337,8 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             else:  # a row block's copy lands in the peer's buffer t mod XBUFS
                 tile, w, sb = t
                 p = ctas[1 - ci]
+                if p["exited"] or c["exited"]:
+                    raise ProtocolError(f"a copy of tile {tile} lands after a CTA exited")
                 b = tile % XBUFS
                 state = p["xbuf"][b][w]
                 if state is not None and state[0] == "data":
@@ -287,6 +359,10 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             idle = 0
         if idle > 50000:
             raise ProtocolError(f"deadlock; roles still running: {sorted(map(str, roles))}")
+    if abort_at is None:
+        for c in ctas:
+            if not c["exited"]:
+                raise ProtocolError("a CTA never reached its exit")
 
 
 def _layouts(n, seed):
@@ -315,6 +391,27 @@ def test_planted_protocol_mistakes_are_caught(mistake):
         except ProtocolError:
             caught += 1
     assert caught > 0, f"the model did not catch {mistake}"
+
+
+def test_abort_drains_every_copy_before_exit():
+    # either CTA's abort flag goes up at a random point; neither may exit
+    # while a score copy into or out of its shared memory is in flight
+    rng = random.Random(31)
+    for i, segs in enumerate(_layouts(200, 32)):
+        run_model(segs, seed=i, abort_at=(rng.randrange(2), rng.randrange(1, 3000)))
+    for i, segs in enumerate(_layouts(60, 35)):
+        run_model(segs, seed=i, fp8=True, abort_at=(rng.randrange(2), rng.randrange(1, 3000)))
+
+
+def test_exit_without_drain_is_caught():
+    rng = random.Random(33)
+    caught = 0
+    for i, segs in enumerate(_layouts(200, 34)):
+        try:
+            run_model(segs + [3, 5], seed=i, abort_at=(rng.randrange(2), rng.randrange(1, 3000)), drain=False)
+        except ProtocolError:
+            caught += 1
+    assert caught > 0, "the model did not catch an exit with copies in flight"
 
 
 def test_fp8_protocol_holds_on_random_interleavings():
