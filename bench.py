@@ -153,24 +153,31 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ CPU oracle baseline
-def cpu_baseline(case, budget_s: float, max_rows: int = 128):
-    """The oracle as it stands on a bounded sample of rows of the same workload."""
+def cpu_baseline(case, budget_s: float, max_rows: int = 128, check=None):
+    """The oracle as it stands on a bounded sample of rows of the same workload.
+
+    check: the timed GPU step's outputs on some rows ({rows, split, o_lat,
+    out, lse}); those rows are computed first and compared with it (the
+    parity of the timed run, with the tolerances of the parity tests)."""
     import oracle  # test infrastructure: only the CPU-baseline leg imports it
     t0 = time.perf_counter()
-    cache = None
     seq, pos = case.positions()
     slots = oracle.slot_mapping(case.block_table, seq, pos)
     cache = oracle.append(np.zeros((case.num_pages, 64, 576), dtype=np.float32), case.c_kv, case.k_r, slots)
     setup = time.perf_counter() - t0
+    first = list(check["rows"]) if check else []
+    order = first + [r for r in range(case.T) if r not in set(first)]
+    ref = {}
     rows_done = 0
     t1 = time.perf_counter()
-    order = list(range(case.T))
-    while rows_done < min(max_rows, case.T):
+    while rows_done < min(max(max_rows, len(first)), case.T):
         r = order[rows_done]
-        oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table,
-                        case.seq_lens, case.q_lens, SCALE, rows=[r])
+        res = oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table,
+                              case.seq_lens, case.q_lens, SCALE, rows=[r])
+        if r in first:
+            ref[r] = (res["o_lat"][r], res["out"][r], res["lse"][r])
         rows_done += 1
-        if time.perf_counter() - t1 > budget_s:
+        if time.perf_counter() - t1 > budget_s and rows_done >= len(first):
             break
     el = time.perf_counter() - t1
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
@@ -180,9 +187,26 @@ def cpu_baseline(case, budget_s: float, max_rows: int = 128):
         blas = sum(int(x.get("num_threads", 0)) for x in threadpool_info() if x.get("user_api") == "blas") or None
     except Exception:
         pass
-    return dict(value=rows_done / el, unit="tokens/s", cores=int(blas or cores), kind="oracle",
-                sample=f"{rows_done} of {case.T} query rows (A2+A3+A5 in float64 NumPy, all 128 heads); "
-                       f"cache placement {setup:.1f}s untimed", seconds=el)
+    out = dict(value=rows_done / el, unit="tokens/s", cores=int(blas or cores), kind="oracle",
+               sample=f"{rows_done} of {case.T} query rows (A2+A3+A5 in float64 NumPy, all 128 heads); "
+                      f"cache placement {setup:.1f}s untimed", seconds=el)
+    if check:
+        def stats(gpu, want):
+            d = np.abs(np.asarray(gpu, dtype=np.float64) - want)
+            return dict(max_err_frac=float(d.max() / max(np.abs(want).max(), 1e-300)),
+                        mean_rel=float(d.sum() / max(np.abs(want).sum(), 1e-300)))
+        rows = list(check["rows"])
+        par = dict(rows=rows, split_rows_checked=sorted(set(rows) & set(check["split"])),
+                   o_lat=stats(check["o_lat"], np.stack([ref[r][0] for r in rows])),
+                   out=stats(check["out"], np.stack([ref[r][1] for r in rows])),
+                   lse=stats(check["lse"], np.stack([ref[r][2] for r in rows])),
+                   tolerance="max|err| <= 2e-2 max|ref| and sum|err|/sum|ref| <= 5e-3 (o_lat, out); "
+                             "2e-3 and 5e-4 (lse)")
+        par["passed"] = bool(all(par[x]["max_err_frac"] <= 2e-2 and par[x]["mean_rel"] <= 5e-3
+                                 for x in ("o_lat", "out"))
+                             and par["lse"]["max_err_frac"] <= 2e-3 and par["lse"]["mean_rel"] <= 5e-4)
+        out["parity"] = par
+    return out
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -380,6 +404,105 @@ def measure_decompress(api, torch, dev, stream, peaks):
     }
 
 
+def parity_rows(api, plan, T, k=8):
+    """Rows checked against the oracle: the first and last row, then rows the
+    combine merges from split pieces, then rows at cluster-range boundaries."""
+    r = api.plan_rows(plan)
+    pick = [0, T - 1]
+    for x in r["split"][::max(1, len(r["split"]) // max(1, k // 2))] + r["boundary"]:
+        if len(pick) >= k:
+            break
+        if x not in pick:
+            pick.append(int(x))
+    return sorted(set(pick)), r["split"]
+
+
+def measure_configs(api, torch, dev, stream, peaks, main_w, main_st, main_dec_us, main_step_us, num_clusters,
+                    reps=6):
+    """Every workload of the scope table, each in the bench's launch
+    configuration (all clusters, inputs resident): the decode (decode +
+    combine launches) and the whole step A1 -> A5, each launch timed alone
+    with CUDA events after a write of 256 MB that flushes L2 (workloads 0, 1
+    and 4 would otherwise find their cache in L2); the roofline of the
+    decode.  The main workload's entry repeats the timed run's figures.
+    (Every workload's rows are checked against the oracle at full size by
+    the GPU parity tests; the main workload's timed step also by the CPU
+    baseline leg here.)"""
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    table = {}
+    for w in sorted(wl.WORKLOADS):
+        case = wl.workload(w, seed=0)
+        st = workload_stats(case)
+        t_f = st["flops"] / (peaks["bf16_tflops"] * 1e12)
+        t_b = st["bytes"] / (peaks["hbm_gbs"] * 1e9)
+        bound = "tensor" if t_f >= t_b else "hbm"
+        t_roof_us = max(t_f, t_b) * 1e6
+        if w == main_w:
+            dec_us, step_us = main_dec_us, main_step_us
+        else:
+            def bf(x):
+                return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(device=dev, dtype=torch.bfloat16)
+            err = torch.zeros(1, dtype=torch.int32, device=dev)
+            kv = torch.empty((case.num_pages, 64, 576), dtype=torch.bfloat16, device=dev)
+            api.mla_cache_init(kv)
+            seq, pos = case.positions()
+            slots = api.mla_slot_mapping(case.block_table, seq, pos)
+            new_idx = case.new_token_index()
+            old = np.ones(slots.shape[0], dtype=bool)
+            old[new_idx] = False
+            if old.any():
+                api.mla_kv_append(bf(case.c_kv[old]), bf(case.k_r[old]), torch.from_numpy(slots[old]).to(dev), kv,
+                                  err)
+            c_new, k_new = bf(case.c_kv[new_idx]), bf(case.k_r[new_idx])
+            s_new = torch.from_numpy(slots[new_idx]).to(dev)
+            bt = torch.from_numpy(case.block_table).to(dev)
+            q_c, q_r, w_uk, w_uv = bf(case.q_c), bf(case.q_r), bf(case.w_uk), bf(case.w_uv)
+            T = case.T
+            q_abs = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
+            o_lat = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
+            lse = torch.empty((T, 128), dtype=torch.float32, device=dev)
+            out = torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev)
+            plan = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, num_clusters=num_clusters)
+
+            def decode():
+                api.mla_decode_paged(q_abs, q_r, kv, bt, plan, o_lat, err, lse=lse, scale=SCALE)
+
+            def whole():
+                api.mla_kv_append(c_new, k_new, s_new, kv, err)
+                api.mla_absorb_q(q_c, w_uk, q_abs, err)
+                decode()
+                api.mla_up_v(o_lat, w_uv, out, err)
+
+            def timed(fn):
+                for _ in range(3):
+                    fn()
+                ts = []
+                for _ in range(reps):
+                    flush.zero_()
+                    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                    a.record(stream)
+                    fn()
+                    b.record(stream)
+                    torch.cuda.synchronize(dev)
+                    ts.append(a.elapsed_time(b) * 1e3)
+                return statistics.median(ts)
+
+            step_us = timed(whole)
+            dec_us = timed(decode)
+            if api.mla_check(err) != 0:
+                raise RuntimeError(f"device error word set while timing workload {w}")
+            del kv, q_abs, o_lat, out
+            torch.cuda.empty_cache()
+        table[case.name] = dict(
+            rows=case.T, bound=bound, t_roof_us=round(t_roof_us, 2), decode_us=round(dec_us, 2),
+            frac=round(t_roof_us / dec_us, 4), kv_tb_per_s=round(st["kv_bytes"] / (dec_us * 1e-6) / 1e12, 4),
+            tflops=round(st["flops"] / (dec_us * 1e-6) / 1e12, 1), step_us=round(step_us, 2),
+            step_tokens_per_s=round(case.T / (step_us * 1e-6), 1),
+            timing="main timed run" if w == main_w else "median of %d launches, L2 flushed before each" % reps)
+    del flush
+    return table
+
+
 def run_mla(args):
     import torch
     from mla_latent_kv_02_gb300 import api
@@ -442,8 +565,8 @@ def run_mla(args):
     K = args.steps
     dec_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    clocks = ClockSampler(local, os.path.join(ROOT, "gpurun_out", f"bench_clocks_r{rank}.csv")) \
-        if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else ClockSampler(local, "/tmp/mla_bench_clocks.csv")
+    import tempfile
+    clocks = ClockSampler(local, os.path.join(tempfile.gettempdir(), f"mla_bench_clocks_{os.getpid()}_r{rank}.csv"))
     barrier(ws)
     torch.cuda.synchronize(dev)
     torch.cuda._sleep(2_000_000)   # untimed: lets the first launches queue up behind it
@@ -535,6 +658,10 @@ def run_mla(args):
         raise RuntimeError("device error word set during the end-to-end steps")
 
     peaks = load_peaks()
+    # the timed step's outputs on the rows the CPU baseline will check (split and boundary rows first)
+    check_rows, check_split = parity_rows(api, plan, T)
+    gpu_rows = dict(rows=check_rows, split=check_split, o_lat=o_lat.float().cpu().numpy()[check_rows],
+                    out=out.float().cpu().numpy()[check_rows], lse=lse.cpu().numpy()[check_rows])
     rows = measure_rows(api, torch, dev, stream, case, c_old, k_old, slots_old, pos[old_idx], q_r, kv, dev_err,
                         peaks["hbm_gbs"], plan=plan, q_abs=q_abs, st=st, peaks=peaks) if old_idx.size else {}
     step_s = ms_total / 1e3 / K
@@ -586,13 +713,21 @@ def run_mla(args):
                 "d2h_bytes_per_step": int(d2h), "steps_in_flight": 2},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
+        "parity": None,
         "rows": rows,
     }
+    if not args.no_configs:
+        # free this workload's device buffers before the others are built
+        del kv, c_old, k_old, q_abs, o_lat, out, d_in, d_out
+        torch.cuda.empty_cache()
+        line["configs"] = measure_configs(api, torch, dev, stream, peaks, args.workload, st, dec_avg * 1e3,
+                                          ms_total / K * 1e3, plan.num_clusters)
     if not args.no_decompress:
         line["decompress_branch"] = measure_decompress(api, torch, dev, stream, peaks)
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(case, args.cpu_budget)
+        line["cpu_baseline"] = cpu_baseline(case, args.cpu_budget, check=gpu_rows)
         line["cpu_baseline"].pop("seconds", None)
+        line["parity"] = line["cpu_baseline"].pop("parity", None)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if ws > 1:
@@ -649,6 +784,7 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decompress", action="store_true", help="skip the decompress-branch measurement")
+    ap.add_argument("--no-configs", action="store_true", help="skip the per-workload table")
     ap.add_argument("--ref-rows", type=int, default=2, help="query rows per reference-arm step")
     args = ap.parse_args(argv)
     if args.warmup < 3 and args.impl == "mla":

@@ -283,18 +283,36 @@ mla_status mla_decode_paged(const void* q_abs, const void* q_r, const void* kv_c
  * given on the host (seq_lens_host / q_lens_host, int32 [B]) and the plan is
  * built internally.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress) and the cluster count; make that first call
- * before capturing any stream.  When the plan for all clusters needs more
- * workspace than the array holds, fewer clusters are used; a batch whose plan
- * exceeds MLA_NOALLOC_PLAN_BYTES (about 16 000 query rows) is rejected with
- * MLA_ERR_INVALID_ARG.  Nothing in the array needs to start at zero: every
- * call writes the plan and every workspace slot before reading them.  All
- * calls share the one array, so calls that may overlap on the GPU (different
- * streams, or host threads racing on one device) race on it: serialise them.
+ * before capturing any stream.  The plan reaches the array inside the launch
+ * parameters of a small copy kernel on `stream` (one launch per 7 936 plan
+ * words, one for every usual batch), so the call reads no host memory after
+ * it returns and never waits for the stream.
+ *
+ * When the plan for every cluster needs more split-KV workspace than the
+ * array holds (MLA_NOALLOC_WORKSPACE_BYTES fits 63 split pieces; long
+ * contexts split every row), the largest cluster count whose plan fits is
+ * used, found by planning on the host from the most clusters down.  Fewer
+ * clusters mean fewer SMs at work: on a GB300 (76 two-CTA clusters) a batch
+ * of 16 sequences of 64K tokens runs on 48 clusters in about 1.6x the time of
+ * mla_decode_paged, and a batch of 64 two-token MTP rows over 8K tokens on
+ * 64 clusters (no split rows) in about 1.2x.  A batch whose plan exceeds
+ * MLA_NOALLOC_PLAN_BYTES even on one cluster (about 16 000 query rows) is
+ * rejected with MLA_ERR_INVALID_ARG.  Nothing in the array needs to start at
+ * zero: every call writes the plan and every workspace slot before reading
+ * them.  All calls share the one array, so calls that may overlap on the GPU
+ * (different streams, or host threads racing on one device) race on it:
+ * serialise them.
  */
 mla_status mla_decode_paged_noalloc(const void* q_abs, const void* q_r, const void* kv_cache,
                                     int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                                     const int32_t* seq_lens_host, const int32_t* q_lens_host, int32_t B,
                                     float scale, void* o_lat, float* lse, int32_t* dev_err, void* stream);
+
+/* Test hook of mla_decode_paged_noalloc (no counterpart in the source pages):
+ * the summary of the plan the last successful call on the current device
+ * ran (its cluster count and split pieces).  MLA_ERR_INVALID_ARG before the
+ * first call on this device or when out is NULL. */
+mla_status mla_debug_noalloc_last_plan(mla_plan_info* out);
 
 /* ---------------------------------------------------------------------------
  * Decoupled RoPE in fp32 ([P1] §1: the 64-d RoPE key carries the position

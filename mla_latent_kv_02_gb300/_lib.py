@@ -75,6 +75,7 @@ SIGNATURES = {
     "mla_check": (C.c_int, [P, P, PI32]),
     "mla_debug_set_decode_wait_limit": (C.c_int, [C.c_uint64]),
     "mla_decode_paged_noalloc": (C.c_int, [P, P, P, I64, P, I32, PI32, PI32, I32, C.c_float, P, P, P, P]),
+    "mla_debug_noalloc_last_plan": (C.c_int, [C.POINTER(mla_plan_info)]),
 }
 
 

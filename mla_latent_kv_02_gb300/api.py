@@ -415,6 +415,28 @@ def mla_decode_plan(seq_lens: Sequence[int], q_lens: Sequence[int], device=None,
     return DecodePlan(plan=plan, info=info, workspace=ws, host=host)
 
 
+def plan_rows(plan: DecodePlan) -> dict:
+    """The query rows a plan treats specially, read from its host copy (the
+    plan layout of csrc/internal.h): rows cut into several pieces (merged by
+    the combine) and rows whose segment starts or ends a cluster's range.
+    For choosing parity samples; no device work."""
+    w = plan.host.numpy() if plan.host is not None else None
+    if w is None:
+        raise ValueError("the plan has no host copy")
+    nc, ns, nsplit = int(w[3]), int(w[4]), int(w[6])
+    seg_off = 16
+    seg_base = (seg_off + nc + 1 + 7) // 8 * 8
+    split_base = seg_base + 8 * ns
+    split = sorted(int(w[split_base + 4 * i]) for i in range(nsplit))
+    boundary = set()
+    for c in range(nc):
+        a, b = int(w[seg_off + c]), int(w[seg_off + c + 1])
+        if b > a:
+            boundary.add(int(w[seg_base + 8 * a]))
+            boundary.add(int(w[seg_base + 8 * (b - 1)]))
+    return {"split": split, "boundary": sorted(boundary)}
+
+
 def mla_decode_paged(q_abs, q_r, kv_cache, block_table, plan: DecodePlan, o_lat, dev_err, lse=None,
                      scale: float = 1.0 / (192 ** 0.5), stream=None) -> None:
     T = q_abs.shape[0]

@@ -18,7 +18,7 @@ Sources:
   holds the subnormals m·2^-9; S.1111.111 is NaN; there are no infinities;
   the largest finite magnitude is 448.
 
-Reading (the pages give no FP8 layout; listed in the design notes): each
+Reading (the pages give no FP8 layout): each
 token's 512 latent values share one power-of-two scale 2^k, k the smallest
 integer with max|c| <= 448·2^k (k = 0 for an all-zero row); the codes are
 c·2^-k rounded to the nearest E4M3 value, ties to the even code.  Because the

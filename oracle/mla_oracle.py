@@ -25,8 +25,7 @@ Sources (cited by page title and section):
 * [P3] bjbfmj.com/news/60700 — the KV-byte formula
   L × (d_c + d_r) × b × tokens × sequences and its calculator's checks.
 
-Readings where the pages are silent (each listed in the design notes):
-softmax is the exact softmax over the visible tokens (the pages print none;
+Readings where the pages are silent: softmax is the exact softmax over the visible tokens (the pages print none;
 online softmax and split-KV are implementations of it); a query at sequence
 position p sees positions [0, p]; V is the latent itself in the absorbed path
 (o_lat = P·c_KV, then out = o_lat·W_UV), which equals softmax·(c_KV·W_UV) by
@@ -117,23 +116,26 @@ def gather(kv_cache: np.ndarray, block_table: np.ndarray, b: int, n: int,
 # Steps A2, A3, A5
 # --------------------------------------------------------------------------
 def absorb_q(q_c: np.ndarray, w_uk: np.ndarray) -> np.ndarray:
-    """[P1] §4 path B: q_abs[t, h, c] = Σ_d q_c[t, h, d] · W_UK[h, d, c]."""
+    """[P1] §4 path B: q_abs[t, h, c] = Σ_d q_c[t, h, d] · W_UK[h, d, c].
+
+    One query row at a time (per head, a vector times W_UK[h]), so a row's
+    value does not depend on which other rows are computed with it."""
     q = np.asarray(q_c, dtype=np.float64)
     w = np.asarray(w_uk, dtype=np.float64)
     out = np.empty((q.shape[0], q.shape[1], w.shape[2]), dtype=np.float64)
-    for h in range(q.shape[1]):
-        out[:, h, :] = q[:, h, :] @ w[h]
+    for t in range(q.shape[0]):
+        out[t] = np.matmul(q[t][:, None, :], w)[:, 0, :]
     return out
 
 
 def up_v(o_lat: np.ndarray, w_uv: np.ndarray) -> np.ndarray:
     """out[t, h, d] = Σ_c o_lat[t, h, c] · W_UV[h, c, d] ([P2] V = c·W_UV, absorbed
-    into the output by associativity)."""
+    into the output by associativity).  One query row at a time, like absorb_q."""
     o = np.asarray(o_lat, dtype=np.float64)
     w = np.asarray(w_uv, dtype=np.float64)
     out = np.empty((o.shape[0], o.shape[1], w.shape[2]), dtype=np.float64)
-    for h in range(o.shape[1]):
-        out[:, h, :] = o[:, h, :] @ w[h]
+    for t in range(o.shape[0]):
+        out[t] = np.matmul(o[t][:, None, :], w)[:, 0, :]
     return out
 
 
@@ -217,10 +219,12 @@ def mla_step(q_c, q_r, w_uk, w_uv, kv_cache, block_table, seq_lens, q_lens, scal
         idx = sorted(int(r) for r in rows)
         qa[idx] = absorb_q(q_c[idx], w_uk)
     o, lse = decode(qa, q_r, kv_cache, block_table, seq_lens, q_lens, scale, rows, dc)
-    out = up_v(np.nan_to_num(o), w_uv)
-    if rows is not None:
-        mask = np.isnan(o[:, 0, 0])
-        out[mask] = np.nan
+    if rows is None:
+        out = up_v(o, w_uv)
+    else:
+        # only the requested rows are up-projected; the others stay NaN
+        out = np.full((o.shape[0], o.shape[1], w_uv.shape[2]), np.nan)
+        out[idx] = up_v(o[idx], w_uv)
     return dict(q_abs=qa, o_lat=o, lse=lse, out=out)
 
 
@@ -306,7 +310,7 @@ def absorbed_scores(q_c_row, q_r_row, c_kv, k_r, w_uk, scale):
 # and [P1] §4 traces a failed equivalence check to RoPE computed in fp16
 # (phase error), fixed by generating the precomputed RoPE table in fp32 and
 # multiply-adding in fp32.  The pages print no rotation formula; the reading
-# used here (listed in the design notes) is the standard rotary embedding:
+# used here is the standard rotary embedding:
 # consecutive pairs (x[2i], x[2i+1]), i < d/2, rotated by the angle
 # p * base^(-2i/d) with base 10000.
 ROPE_BASE = 10000.0

@@ -17,7 +17,7 @@ Sources:
   3, 4, 6), one E4M3 scale per block of 16 elements, and one fp32 scale per
   tensor; an element's value is e2m1 * block_scale * tensor_scale.
 
-Readings (the pages give no layout; listed in the design notes):
+Readings (the pages give no layout):
 * the tensor scale s_t is a caller-supplied fp32 constant (an append-only
   cache cannot rescale what it already holds);
 * block scale: the E4M3 rounding (nearest, ties to even, saturating at 448)

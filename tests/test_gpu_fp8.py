@@ -264,16 +264,21 @@ def _fp8_row_reference(case, q_abs, t, b, i):
     return oracle.attention_row(q_abs[t], case.q_r[t], lat, case.k_r[off:off + n].astype(np.float64), SCALE)
 
 
-@pytest.mark.parametrize("cfg,k", [(2, 4), (3, 3)])
+@pytest.mark.parametrize("cfg,k", [(2, 6), (3, 4)])
 def test_decode_fp8_full_size_sampled_rows(api, cfg, k):
     """The MTP B64 x 8K and B16 x 64K workloads at full size, FP8 cache,
-    in the bench's launch configuration; the oracle computes sampled rows."""
+    in the bench's launch configuration; the oracle computes sampled rows,
+    half of them rows that the combine merges from split pieces."""
     case = wl.workload(cfg, with_q_abs=True, with_weights=False)
     dc = DeviceCase(case, with_weights=False, fp8=True)
     o, lse, plan = dc.decode()
     index = oracle.row_index(case.seq_lens, case.q_lens)
+    split = api.plan_rows(plan)["split"]
+    assert split, "the full-size workloads split rows across clusters"
     rng = np.random.Generator(np.random.PCG64(99))
-    pick = sorted({0, case.T - 1} | set(int(x) for x in rng.choice(case.T, size=k - 2, replace=False)))
+    pick = {0, case.T - 1} | set(int(x) for x in rng.choice(split, size=min(len(split), k // 2), replace=False))
+    pick |= set(int(x) for x in rng.choice(case.T, size=k - len(pick), replace=False)) if k > len(pick) else set()
+    pick = sorted(pick)
     got_o, got_l = to_np(o), lse.cpu().numpy()
     for t in pick:
         _, b, i = index[t]

@@ -196,19 +196,30 @@ def test_full_step_small(api):
 
 
 # ------------------------------------------------------------------ the five workloads at full size
-def _sample_rows(case, k):
-    T = case.T
-    if T <= k:
-        return list(range(T))
-    rng = np.random.Generator(np.random.PCG64(1234))
-    pick = {0, T - 1} | set(int(x) for x in rng.choice(T, size=k - 2, replace=False))
+def _check_rows(case, plan):
+    """Rows checked against the oracle at full size: every row of workloads
+    0-3; for the 2048-row chunked prefill, every split row, every row whose
+    segment starts or ends a cluster's range, and the first and last row of
+    each block of 128 rows."""
+    if case.T <= 128:
+        return list(range(case.T))
+    r = api_mod().plan_rows(plan)
+    pick = set(r["split"]) | set(r["boundary"])
+    for b0 in range(0, case.T, 128):
+        pick |= {b0, min(case.T, b0 + 128) - 1}
     return sorted(pick)
 
 
-@pytest.mark.parametrize("cfg,k", [(0, 1), (1, 16), (2, 6), (3, 3), (4, 5)])
-def test_workload_full_size_sampled_rows(api, cfg, k):
+def api_mod():
+    from mla_latent_kv_02_gb300 import api as a
+    return a
+
+
+@pytest.mark.parametrize("cfg", [0, 1, 2, 3, 4])
+def test_workload_full_size_rows(api, cfg):
     """Full-size workload in the bench's launch configuration; the oracle
-    computes a sample of rows (all rows for the small workloads)."""
+    computes every row (workloads 0-3) or every split, boundary and block-end
+    row (workload 4)."""
     case = wl.workload(cfg)
     dc = DeviceCase(case)
     T = case.T
@@ -218,11 +229,18 @@ def test_workload_full_size_sampled_rows(api, cfg, k):
     out = torch.empty((T, 128, 128), dtype=torch.bfloat16, device="cuda")
     api.mla_up_v(o, dc.w_uv, out, dc.dev_err)
     assert api.mla_check(dc.dev_err) == 0
-    rows = _sample_rows(case, k)
+    rows = _check_rows(case, plan)
+    split = api.plan_rows(plan)["split"]
+    assert set(split) <= set(rows)
+    if cfg in (2, 3, 4):
+        assert split, "the full-size workloads split rows across clusters"
     ref = oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, oracle_cache(case), case.block_table,
                           case.seq_lens, case.q_lens, SCALE, rows=rows)
     assert_close(to_np(o)[rows], ref["o_lat"][rows], f"cfg{cfg} o_lat")
     assert_close(to_np(out)[rows], ref["out"][rows], f"cfg{cfg} out")
     assert_close(lse.cpu().numpy()[rows], ref["lse"][rows], f"cfg{cfg} lse", max_frac=2e-3, mean_rel=5e-4)
-    # property over every row: finite outputs, lse >= max-free lower bound ln(1)
+    if split:
+        # the rows merged by the combine, on their own
+        assert_close(to_np(o)[split], ref["o_lat"][split], f"cfg{cfg} o_lat split rows")
+    # property over every row: finite outputs
     assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()

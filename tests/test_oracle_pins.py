@@ -367,3 +367,21 @@ def test_expand_kv_closed_forms_and_absorption():
     # the plausible mistake, contracting over W_UK's other axis (square block), changes the result
     sq = w_uk[:, :, :d]
     assert not np.allclose(np.einsum("tc,hcd->thd", c[:, :d], sq), np.einsum("tc,hdc->thd", c[:, :d], sq))
+
+
+def test_row_subset_equals_full_run_bit_for_bit():
+    """Every oracle step is computed one query row at a time, so asking for a
+    subset of rows (as the GPU parity tests at full size and the timed CPU
+    baseline do) gives the same bits as the full run, and leaves the other
+    rows NaN."""
+    case = wl.make_case([70, 130, 65], [1, 2, 3], seed=23)
+    cache = _cache_for(case)
+    args = (case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table, case.seq_lens, case.q_lens,
+            1.0 / math.sqrt(192))
+    full = oracle.mla_step(*args)
+    for rows in ([0], [2, 4], [5]):
+        sub = oracle.mla_step(*args, rows=rows)
+        for key in ("q_abs", "o_lat", "lse", "out"):
+            assert np.array_equal(sub[key][rows], full[key][rows]), key
+            others = [r for r in range(case.T) if r not in rows]
+            assert np.isnan(sub[key][others]).all(), key

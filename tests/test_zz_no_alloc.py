@@ -66,6 +66,25 @@ def test_noalloc_matches_regular_entry_point_on_two_calls(lib):
                      max_frac=1e-3, mean_rel=1e-4)
 
 
+def test_noalloc_uses_fewer_clusters_when_the_split_pieces_exceed_its_scratch(lib):
+    # Sixteen sequences of 64K tokens (the long-context workload): with every
+    # cluster, each row is cut into pieces that need more workspace than the
+    # array holds, so the call plans with fewer clusters, still splitting rows
+    # (the workspace in use), and must match the regular entry point.
+    from mla_latent_kv_02_gb300 import _lib
+    case = wl.workload(3, with_q_abs=True, with_weights=False)
+    dc = DeviceCase(case, with_weights=False)
+    o_ref, lse_ref, plan = dc.decode()
+    o, lse = _call_noalloc(lib, dc, case)
+    info = _lib.mla_plan_info()
+    assert lib.mla_debug_noalloc_last_plan(C.byref(info)) == 0, lib.mla_last_error().decode()
+    assert 0 < info.num_partials and info.num_clusters < plan.info.num_clusters
+    assert info.num_partials * (128 * 512 * 4 + 128 * 4) <= 16 * 1024 * 1024
+    assert_close(to_np(o), to_np(o_ref), "o_lat no-alloc (fewer clusters) vs regular")
+    assert_close(lse.cpu().numpy(), lse_ref.cpu().numpy(), "lse no-alloc (fewer clusters) vs regular",
+                 max_frac=1e-3, mean_rel=1e-4)
+
+
 def test_noalloc_rejects_batches_beyond_its_scratch(lib):
     # A plan for this many query rows exceeds the fixed plan area: the call must
     # fail on the host with a clear message and enqueue nothing.
