@@ -497,23 +497,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       // All loads first (codes and row scales into registers), so that the
       // store loop holds no shared-memory load behind a store and its rows'
       // arithmetic overlaps.
-      uint2 code[kRows];
-      float scale[kRows];
-#pragma unroll
-      for (int j = 0; j < kRows; ++j) {
-        const uint32_t r = (uint32_t)(kConvWarps * j + cw);
-        code[j] = ld_shared_v2(stage + r * 256u + (uint32_t)lane * 8u);
-        scale[j] = ld_shared_f32(stage + kF8ScaleOff + 4u * r);
-      }
       // f16 operands: one conversion (exact) and one multiply by the row's
       // 2^k per pair, issued kBatch rows at a time so that one warp keeps
       // many in flight.  A scale outside [2^-15, 2^7] is clamped and flagged.
+      // A row's factor is formed as soon as its scale is read, so the scales
+      // themselves are never all live at once.
+      uint2 code[kRows];
       uint32_t fac[kRows];
       bool in_range = true;
 #pragma unroll
       for (int j = 0; j < kRows; ++j) {
+        const uint32_t r = (uint32_t)(kConvWarps * j + cw);
+        code[j] = ld_shared_v2(stage + r * 256u + (uint32_t)lane * 8u);
         bool ok_j;
-        fac[j] = fp8_f16_factor(scale[j], ok_j);
+        fac[j] = fp8_f16_factor(ld_shared_f32(stage + kF8ScaleOff + 4u * r), ok_j);
         in_range = in_range && ok_j;
       }
       if (!in_range && lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_FP8_RANGE);  // warp-uniform
@@ -870,18 +867,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
   if constexpr (kF8) {
     // 512 threads x 128 registers at launch: warpgroup 0 (producer, MMA
     // issue, an idle warp) drops to 64, warpgroup 3 (converters, which hold
-    // a tile's codes in registers) to 96, the softmax warpgroups 1-2 rise
-    // to 176; 128*64 + 128*96 + 256*176 = 65536, the launch's total.
+    // a tile's codes and row factors in registers) to 112, the softmax
+    // warpgroups 1-2 rise to 168; 128*64 + 128*112 + 256*168 = 65536, the
+    // launch's total.  (96 for the converters spilled their codes.)
     if (warp < 4) {
       regs_dec<64>();
       if (warp == 0) role_producer();
       else if (warp == 1) role_qk();
       else if (warp == kPvWarp) role_pv();
     } else if (warp >= kConvWarp0) {
-      regs_dec<96>();
+      regs_dec<112>();
       role_convert();
     } else {
-      regs_inc<176>();
+      regs_inc<168>();
       role_softmax();
     }
   } else {
