@@ -343,7 +343,8 @@ def measure_decompress(api, torch, dev, stream, peaks):
     """The decompress branch on its own workload (B4 x 16384 cached + a
     512-token chunk, q_len >= the 256-token threshold): per-kernel times of
     one sequence (gather, K/V expansion, attention), the whole branch for the
-    batch, and steps A2-A5 of the absorbed path on the same inputs."""
+    batch in one batched call, and steps A2-A5 of the absorbed path on the
+    same inputs."""
     case = wl.workload(4, seed=0)
 
     def bf(x):
@@ -367,13 +368,18 @@ def measure_decompress(api, torch, dev, stream, peaks):
     a_us = _time_launches(torch, stream, lambda i: api.mla_prefill_attention(q_c[:M], q_r[:M], rows, k_c, v_c, out[:M],
                                                                                err))
 
-    def branch(i):
-        for b in range(case.B):
-            r0 = int(case.q_start[b])
-            api.mla_prefill_decompress(q_c[r0:r0 + M], q_r[r0:r0 + M], kv, bt, b, N, w_uk, w_uv, ws, out[r0:r0 + M],
-                                       err)
+    # the whole branch for the batch: one gather, one expansion and one
+    # attention launch over every sequence's packed cache
+    n_all = [int(x) for x in case.seq_lens]
+    ws_all = torch.empty(api.mla_prefill_batch_workspace_size(n_all), dtype=torch.uint8, device=dev)
+    seqs = list(range(case.B))
+    starts = [int(x) for x in case.q_start[:case.B]]
+    qls = [int(x) for x in case.q_lens]
 
-    d_us = _time_launches(torch, stream, branch, reps=3, warmup=2, per_rep=3 * case.B)
+    def branch(i):
+        api.mla_prefill_decompress_batch(q_c, q_r, kv, bt, seqs, starts, qls, n_all, w_uk, w_uv, ws_all, out, err)
+
+    d_us = _time_launches(torch, stream, branch, reps=3, warmup=2, per_rep=3)
     q_abs = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
     o_lat = torch.empty((T, 128, 512), dtype=torch.bfloat16, device=dev)
     out2 = torch.empty_like(out)

@@ -403,8 +403,9 @@ mla_status mla_prefill_workspace_size(int32_t N, size_t* bytes);
 
 /*
  * The whole branch for sequence b of a paged cache: gather its N cached
- * tokens (mla_gather_paged), expand them (mla_expand_kv) and attend
- * (mla_prefill_attention) into out bf16 [M, 128, 128].  workspace is
+ * tokens, expand them (mla_expand_kv) and attend into out bf16
+ * [M, 128, 128] (mla_prefill_decompress_batch with one sequence whose rows
+ * start at row 0).  workspace is
  * device memory of at least mla_prefill_workspace_size(N) bytes, 16-byte
  * aligned; the same validation and device error bits as the three calls.
  */
@@ -412,6 +413,36 @@ mla_status mla_prefill_decompress(const void* q_c, const void* q_r, int32_t M, c
                                   const int32_t* block_table, int32_t max_pages, int32_t b, int32_t N,
                                   const void* w_uk, const void* w_uv, float scale, void* workspace, size_t ws_bytes,
                                   void* out, int32_t* dev_err, void* stream);
+
+/* Workspace bytes mla_prefill_decompress_batch needs for nb sequences of
+ * n_tokens[i] cached tokens (host int32 [nb], nb <= 64): the packed rows
+ * [Σ n, 576] (16-byte rounded) + K_c + V_c (2 * Σ n * 32 KiB).
+ * MLA_ERR_INVALID_ARG for nb outside [0, 64] or a negative length. */
+mla_status mla_prefill_batch_workspace_size(const int32_t* n_tokens, int32_t nb, size_t* bytes);
+
+/*
+ * The decompress branch for every qualifying sequence of a batch in three
+ * launches: one gather of all nb sequences' cached rows into one packed
+ * array, one expansion of all of them (mla_expand_kv over Σ n_tokens rows)
+ * and one attention launch over every (sequence, head, 128-row query tile).
+ * Host int32 arrays of nb entries (nb <= 64): seq_ids (block-table rows,
+ * each in [0, batch)), q_starts (first row of the sequence's chunk in q_c,
+ * q_r and out), q_lens (1 <= q_len <= n_tokens) and n_tokens (cached tokens
+ * of the sequence, its chunk included).  q_c bf16 [rows, 128, 128], q_r
+ * bf16 [rows, 128, 64], out bf16 [rows, 128, 128] on the device, rows the
+ * largest q_starts[i] + q_lens[i]; only the chunks' rows of out are
+ * written.  block_table int32 [batch, max_pages].  workspace: device, at
+ * least mla_prefill_batch_workspace_size bytes, 16-byte aligned.  The same
+ * validation and device error bits as the single-sequence calls (a
+ * block-table entry outside the pool sets MLA_DEVERR_PAGE_OOB); nothing is
+ * launched when validation fails.  nb == 0 is a no-op.
+ */
+mla_status mla_prefill_decompress_batch(const void* q_c, const void* q_r, const int32_t* seq_ids,
+                                        const int32_t* q_starts, const int32_t* q_lens, const int32_t* n_tokens,
+                                        int32_t nb, const void* kv_cache, int64_t num_pages,
+                                        const int32_t* block_table, int32_t batch, int32_t max_pages,
+                                        const void* w_uk, const void* w_uv, float scale, void* workspace,
+                                        size_t ws_bytes, void* out, int32_t* dev_err, void* stream);
 
 /* ---------------------------------------------------------------------------
  * FP8 (E4M3) latent cache ([P3] bjbfmj.com/news/60700: quantisation scale

@@ -58,6 +58,9 @@ SIGNATURES = {
     "mla_expand_kv": (C.c_int, [P, I32, P, P, P, P, P, P]),
     "mla_prefill_attention": (C.c_int, [P, P, I32, P, P, P, I32, C.c_float, P, P, P]),
     "mla_prefill_workspace_size": (C.c_int, [I32, C.POINTER(SZ)]),
+    "mla_prefill_batch_workspace_size": (C.c_int, [PI32, I32, C.POINTER(SZ)]),
+    "mla_prefill_decompress_batch": (C.c_int, [P, P, PI32, PI32, PI32, PI32, I32, P, I64, P, I32, I32, P, P, C.c_float,
+                                               P, SZ, P, P, P]),
     "mla_prefill_decompress": (C.c_int, [P, P, I32, P, I64, P, I32, I32, I32, P, P, C.c_float, P, SZ, P, P, P]),
     "mla_rope_table": (C.c_int, [I32, C.c_float, P, P]),
     "mla_kv_append_rope": (C.c_int, [P, P, P, P, I32, P, I32, P, I64, P, P]),

@@ -274,6 +274,42 @@ def mla_prefill_decompress(q_c, q_r, kv_cache, block_table, b: int, n_tokens: in
                                         _ptr(dev_err), _stream(stream)))
 
 
+def mla_prefill_batch_workspace_size(n_tokens: Sequence[int]) -> int:
+    n = np.ascontiguousarray(n_tokens, dtype=np.int32)
+    out = C.c_size_t()
+    _check(lib().mla_prefill_batch_workspace_size(n.ctypes.data_as(C.POINTER(C.c_int32)), int(n.size),
+                                                  C.byref(out)))
+    return int(out.value)
+
+
+def mla_prefill_decompress_batch(q_c, q_r, kv_cache, block_table, seq_ids, q_starts, q_lens, n_tokens, w_uk, w_uv,
+                                 workspace, out, dev_err, scale: float = 1.0 / (192 ** 0.5), stream=None) -> None:
+    """The decompress branch for several sequences at once: sequence seq_ids[i]
+    (n_tokens[i] cached) with its chunk's q_lens[i] query rows at rows
+    q_starts[i].. of q_c, q_r and out."""
+    rows = q_c.shape[0]
+    _need(q_c, "q_c", torch.bfloat16, (rows, H, D_HC))
+    _need(q_r, "q_r", torch.bfloat16, (rows, H, D_R))
+    _need(kv_cache, "kv_cache", torch.bfloat16)
+    _need(block_table, "block_table", torch.int32)
+    _need(w_uk, "w_uk", torch.bfloat16, (H, D_HC, D_C))
+    _need(w_uv, "w_uv", torch.bfloat16, (H, D_C, D_HC))
+    _need(workspace, "workspace", torch.uint8)
+    _need(out, "out", torch.bfloat16, (rows, H, D_HC))
+    _need(dev_err, "dev_err", torch.int32, (1,))
+    arrs = [np.ascontiguousarray(x, dtype=np.int32) for x in (seq_ids, q_starts, q_lens, n_tokens)]
+    nb = int(arrs[0].size)
+    if any(a.size != nb for a in arrs):
+        raise ValueError("seq_ids, q_starts, q_lens and n_tokens must have the same length")
+    if any(int(s0) + int(m) > rows for s0, m in zip(arrs[1], arrs[2])):
+        raise ValueError("a chunk's rows run past q_c")
+    P32 = C.POINTER(C.c_int32)
+    _check(lib().mla_prefill_decompress_batch(
+        _ptr(q_c), _ptr(q_r), *[a.ctypes.data_as(P32) for a in arrs], nb, _ptr(kv_cache), kv_cache.shape[0],
+        _ptr(block_table), block_table.shape[0], block_table.shape[1], _ptr(w_uk), _ptr(w_uv), float(scale),
+        _ptr(workspace), workspace.numel(), _ptr(out), _ptr(dev_err), _stream(stream)))
+
+
 def mla_rope_table(max_pos: int, table, base: float = 10000.0, stream=None) -> None:
     _need(table, "table", torch.float32, (max_pos, D_R // 2, 2))
     _check(lib().mla_rope_table(int(max_pos), float(base), _ptr(table), _stream(stream)))

@@ -72,14 +72,34 @@ struct DecodeArgs {
   int32_t pad3_;
 };
 
-// Decompress branch: one sequence, M query rows at positions N - M .. N - 1.
-struct PrefillArgs {
+// Decompress branch over a batch of sequences: sequence i has M query rows
+// at positions N - M .. N - 1; its query rows (q_c, q_r, out) start at row
+// q_off, its cache rows (gathered rows, K_c, V_c) at token kv_off of the
+// packed arrays.  The table rides in the launch parameters.
+constexpr int kPrefillMaxSeqs = 64;
+struct PrefillSeq {
   int32_t M;
   int32_t N;
+  int32_t q_off;
+  int32_t kv_off;
+};
+struct PrefillArgs {
+  int32_t nb;           // sequences in seq[]
   float scale_log2;     // scale * log2(e)
-  int32_t pad_;
-  uint16_t* out;        // bf16 [M, 128, 128]
+  uint16_t* out;        // bf16 [rows, 128, 128]
   int32_t* dev_err;
+  PrefillSeq seq[kPrefillMaxSeqs];
+};
+
+// Gather of the first n[i] cached tokens of sequence b[i] of the block
+// table, for i < nb, to rows [off[i], off[i] + n[i]) of one packed output.
+struct GatherBatch {
+  int32_t nb;
+  int32_t pad_;
+  int64_t total;        // Σ n[i]
+  int32_t b[kPrefillMaxSeqs];
+  int32_t n[kPrefillMaxSeqs];
+  int64_t off[kPrefillMaxSeqs];
 };
 
 struct CombineArgs {
@@ -130,6 +150,9 @@ cudaError_t launch_gather_nvfp4_batch(const uint8_t* rows, float tensor_scale, i
                                       int32_t* dev_err, cudaStream_t stream);
 cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table, int32_t max_pages,
                           int32_t b, int32_t n_tokens, uint16_t* out, int32_t* dev_err, cudaStream_t stream);
+cudaError_t launch_gather_batch(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table,
+                                int32_t max_pages, const GatherBatch& g, uint16_t* out, int32_t* dev_err,
+                                cudaStream_t stream);
 
 // Decompress-branch expansion: K_c and V_c in one pass (head-major outputs).
 cudaError_t launch_expand_kv(const CUtensorMap& a_map, const CUtensorMap& k_map, const CUtensorMap& v_map,

@@ -731,6 +731,34 @@ mla_status mla_expand_kv(const void* rows, int32_t n, const void* w_uk, const vo
   return MLA_OK;
 }
 
+// Tensor maps over the packed arrays of a batch (T rows of queries, N cached
+// tokens in all) and the attention launch.
+static mla_status prefill_attention_launch(const void* q_c, const void* q_r, int64_t T, const void* rows,
+                                           const void* k_c, const void* v_c, int64_t N, const mla::PrefillArgs& a,
+                                           void* stream) {
+  CUtensorMap qm, rm, km, krm, vm;
+  const uint32_t box3[3] = {64, 1, 128};
+  const uint64_t qd[3] = {MLA_HEAD_DIM_C, MLA_NUM_HEADS, (uint64_t)T};
+  const uint64_t qs[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)MLA_HEAD_DIM_C * 2 * MLA_NUM_HEADS};
+  const uint64_t rd[3] = {MLA_ROPE_DIM, MLA_NUM_HEADS, (uint64_t)T};
+  const uint64_t rs[2] = {MLA_ROPE_DIM * 2, (uint64_t)MLA_ROPE_DIM * 2 * MLA_NUM_HEADS};
+  const uint64_t kd[3] = {MLA_HEAD_DIM_C, (uint64_t)N, MLA_NUM_HEADS};   // head-major K_c / V_c
+  const uint64_t ks[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)MLA_HEAD_DIM_C * 2 * (uint64_t)N};
+  const uint32_t kbox[3] = {64, 128, 1};
+  const uint64_t krd[2] = {MLA_TOKEN_ELEMS, (uint64_t)N};
+  const uint64_t krs[1] = {(uint64_t)kRowBytes};
+  const uint32_t box2[2] = {64, 128};
+  mla_status s = make_map(&qm, q_c, 3, qd, qs, box3, "q_c");
+  if (s == MLA_OK) s = make_map(&rm, q_r, 3, rd, rs, box3, "q_r");
+  if (s == MLA_OK) s = make_map(&km, k_c, 3, kd, ks, kbox, "K_c");
+  if (s == MLA_OK) s = make_map(&vm, v_c, 3, kd, ks, kbox, "V_c");
+  if (s == MLA_OK) s = make_map(&krm, rows, 2, krd, krs, box2, "k_R rows");
+  if (s != MLA_OK) return s;
+  cudaError_t e = mla::launch_prefill_attn(qm, rm, km, krm, vm, a, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+  return MLA_OK;
+}
+
 mla_status mla_prefill_attention(const void* q_c, const void* q_r, int32_t M, const void* rows, const void* k_c,
                                  const void* v_c, int32_t N, float scale, void* out, int32_t* dev_err,
                                  void* stream) {
@@ -753,33 +781,13 @@ mla_status mla_prefill_attention(const void* q_c, const void* q_r, int32_t M, co
   CHECK_ALIGN16(v_c);
   CHECK_ALIGN16(out);
   if (!aligned(dev_err, 4)) return fail(MLA_ERR_MISALIGNED, "dev_err is not 4-byte aligned");
-  CUtensorMap qm, rm, km, krm, vm;
-  const uint32_t box3[3] = {64, 1, 128};
-  const uint64_t qd[3] = {MLA_HEAD_DIM_C, MLA_NUM_HEADS, (uint64_t)M};
-  const uint64_t qs[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)MLA_HEAD_DIM_C * 2 * MLA_NUM_HEADS};
-  const uint64_t rd[3] = {MLA_ROPE_DIM, MLA_NUM_HEADS, (uint64_t)M};
-  const uint64_t rs[2] = {MLA_ROPE_DIM * 2, (uint64_t)MLA_ROPE_DIM * 2 * MLA_NUM_HEADS};
-  const uint64_t kd[3] = {MLA_HEAD_DIM_C, (uint64_t)N, MLA_NUM_HEADS};   // head-major K_c / V_c
-  const uint64_t ks[2] = {MLA_HEAD_DIM_C * 2, (uint64_t)MLA_HEAD_DIM_C * 2 * (uint64_t)N};
-  const uint32_t kbox[3] = {64, 128, 1};
-  const uint64_t krd[2] = {MLA_TOKEN_ELEMS, (uint64_t)N};
-  const uint64_t krs[1] = {(uint64_t)kRowBytes};
-  const uint32_t box2[2] = {64, 128};
-  mla_status s = make_map(&qm, q_c, 3, qd, qs, box3, "q_c");
-  if (s == MLA_OK) s = make_map(&rm, q_r, 3, rd, rs, box3, "q_r");
-  if (s == MLA_OK) s = make_map(&km, k_c, 3, kd, ks, kbox, "K_c");
-  if (s == MLA_OK) s = make_map(&vm, v_c, 3, kd, ks, kbox, "V_c");
-  if (s == MLA_OK) s = make_map(&krm, rows, 2, krd, krs, box2, "k_R rows");
-  if (s != MLA_OK) return s;
   mla::PrefillArgs a = {};
-  a.M = M;
-  a.N = N;
+  a.nb = 1;
+  a.seq[0] = {M, N, 0, 0};
   a.scale_log2 = (float)((double)scale * 1.4426950408889634);
   a.out = (uint16_t*)out;
   a.dev_err = dev_err;
-  cudaError_t e = mla::launch_prefill_attn(qm, rm, km, krm, vm, a, (cudaStream_t)stream);
-  if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
-  return MLA_OK;
+  return prefill_attention_launch(q_c, q_r, M, rows, k_c, v_c, N, a, stream);
 }
 
 mla_status mla_prefill_workspace_size(int32_t N, size_t* bytes) {
@@ -789,6 +797,95 @@ mla_status mla_prefill_workspace_size(int32_t N, size_t* bytes) {
   return MLA_OK;
 }
 
+mla_status mla_prefill_batch_workspace_size(const int32_t* n_tokens, int32_t nb, size_t* bytes) {
+  CHECK_PTR(bytes);
+  if (nb < 0 || nb > mla::kPrefillMaxSeqs)
+    return fail(MLA_ERR_INVALID_ARG, "nb = %d outside [0, %d]", nb, mla::kPrefillMaxSeqs);
+  if (nb > 0) CHECK_PTR(n_tokens);
+  int64_t total = 0;
+  for (int32_t i = 0; i < nb; ++i) {
+    if (n_tokens[i] < 0) return fail(MLA_ERR_INVALID_ARG, "n_tokens[%d] = %d < 0", i, n_tokens[i]);
+    total += n_tokens[i];
+  }
+  if (total > (1 << 24)) return fail(MLA_ERR_INVALID_ARG, "%lld cached tokens in all: too many", (long long)total);
+  *bytes = prefill_ws_bytes(total);
+  return MLA_OK;
+}
+
+mla_status mla_prefill_decompress_batch(const void* q_c, const void* q_r, const int32_t* seq_ids,
+                                        const int32_t* q_starts, const int32_t* q_lens, const int32_t* n_tokens,
+                                        int32_t nb, const void* kv_cache, int64_t num_pages,
+                                        const int32_t* block_table, int32_t batch, int32_t max_pages,
+                                        const void* w_uk, const void* w_uv, float scale, void* workspace,
+                                        size_t ws_bytes, void* out, int32_t* dev_err, void* stream) {
+  if (nb < 0 || nb > mla::kPrefillMaxSeqs)
+    return fail(MLA_ERR_INVALID_ARG, "nb = %d outside [0, %d]", nb, mla::kPrefillMaxSeqs);
+  if (nb == 0) return MLA_OK;
+  CHECK_PTR(seq_ids);
+  CHECK_PTR(q_starts);
+  CHECK_PTR(q_lens);
+  CHECK_PTR(n_tokens);
+  CHECK_PTR(q_c);
+  CHECK_PTR(q_r);
+  CHECK_PTR(kv_cache);
+  CHECK_PTR(block_table);
+  CHECK_PTR(w_uk);
+  CHECK_PTR(w_uv);
+  CHECK_PTR(workspace);
+  CHECK_PTR(out);
+  CHECK_PTR(dev_err);
+  CHECK_ALIGN16(q_c);
+  CHECK_ALIGN16(q_r);
+  CHECK_ALIGN16(kv_cache);
+  CHECK_ALIGN16(w_uk);
+  CHECK_ALIGN16(w_uv);
+  CHECK_ALIGN16(workspace);
+  CHECK_ALIGN16(out);
+  if (!aligned(block_table, 4) || !aligned(dev_err, 4))
+    return fail(MLA_ERR_MISALIGNED, "block_table and dev_err must be 4-byte aligned");
+  if (!(scale > 0.f) || !std::isfinite(scale)) return fail(MLA_ERR_INVALID_ARG, "scale must be finite and positive");
+  if (num_pages < 1 || batch < 1 || max_pages < 1) return fail(MLA_ERR_INVALID_ARG, "bad pool/table sizes");
+  mla::GatherBatch g = {};
+  mla::PrefillArgs a = {};
+  int64_t total = 0, rows_end = 0;
+  for (int32_t i = 0; i < nb; ++i) {
+    const int32_t b = seq_ids[i], M = q_lens[i], N = n_tokens[i], q0 = q_starts[i];
+    if (b < 0 || b >= batch) return fail(MLA_ERR_INVALID_ARG, "seq_ids[%d] = %d outside [0, %d)", i, b, batch);
+    if (M < 1 || N < M)
+      return fail(MLA_ERR_INVALID_ARG, "sequence %d: q_len %d must be in [1, n_tokens = %d]", i, M, N);
+    if ((N + MLA_PAGE_SIZE - 1) / MLA_PAGE_SIZE > max_pages)
+      return fail(MLA_ERR_INVALID_ARG, "sequence %d: %d tokens need more than max_pages = %d pages", i, N, max_pages);
+    if (q0 < 0) return fail(MLA_ERR_INVALID_ARG, "q_starts[%d] = %d < 0", i, q0);
+    g.b[i] = b;
+    g.n[i] = N;
+    g.off[i] = total;
+    a.seq[i] = {M, N, q0, (int32_t)total};
+    total += N;
+    rows_end = std::max<int64_t>(rows_end, (int64_t)q0 + M);
+  }
+  if (total > (1 << 24)) return fail(MLA_ERR_INVALID_ARG, "%lld cached tokens in all: too many", (long long)total);
+  if (rows_end > (1 << 24)) return fail(MLA_ERR_INVALID_ARG, "query rows past 2^24");
+  if (ws_bytes < prefill_ws_bytes(total))
+    return fail(MLA_ERR_INVALID_ARG, "workspace holds %zu bytes, %lld cached tokens need %zu", ws_bytes,
+                (long long)total, prefill_ws_bytes(total));
+  g.nb = nb;
+  g.total = total;
+  a.nb = nb;
+  a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+  a.out = (uint16_t*)out;
+  a.dev_err = dev_err;
+  uint8_t* ws = (uint8_t*)workspace;
+  void* rows = ws;
+  void* k_c = ws + prefill_rows_bytes(total);
+  void* v_c = (uint8_t*)k_c + (size_t)total * MLA_NUM_HEADS * MLA_HEAD_DIM_C * 2;
+  cudaError_t e = mla::launch_gather_batch((const uint16_t*)kv_cache, num_pages, block_table, max_pages, g,
+                                           (uint16_t*)rows, dev_err, (cudaStream_t)stream);
+  if (e != cudaSuccess) return cuda_fail(e, "batched gather launch");
+  mla_status s = mla_expand_kv(rows, (int32_t)total, w_uk, w_uv, k_c, v_c, dev_err, stream);
+  if (s != MLA_OK) return s;
+  return prefill_attention_launch(q_c, q_r, rows_end, rows, k_c, v_c, total, a, stream);
+}
+
 mla_status mla_prefill_decompress(const void* q_c, const void* q_r, int32_t M, const void* kv_cache, int64_t num_pages,
                                   const int32_t* block_table, int32_t max_pages, int32_t b, int32_t N,
                                   const void* w_uk, const void* w_uv, float scale, void* workspace, size_t ws_bytes,
@@ -796,19 +893,11 @@ mla_status mla_prefill_decompress(const void* q_c, const void* q_r, int32_t M, c
   if (M < 0 || N < 0) return fail(MLA_ERR_INVALID_ARG, "M = %d, N = %d: negative", M, N);
   if (M == 0) return MLA_OK;
   if (M > N) return fail(MLA_ERR_INVALID_ARG, "M = %d query rows exceed the N = %d cached tokens", M, N);
-  CHECK_PTR(workspace);
-  CHECK_ALIGN16(workspace);
-  if (N < 0 || ws_bytes < prefill_ws_bytes(N))
-    return fail(MLA_ERR_INVALID_ARG, "workspace holds %zu bytes, N = %d needs %zu", ws_bytes, N,
-                prefill_ws_bytes(N < 0 ? 0 : N));
-  uint8_t* ws = (uint8_t*)workspace;
-  void* rows = ws;
-  void* k_c = ws + prefill_rows_bytes(N);
-  void* v_c = (uint8_t*)k_c + (size_t)N * MLA_NUM_HEADS * MLA_HEAD_DIM_C * 2;
-  mla_status s = mla_gather_paged(kv_cache, num_pages, block_table, max_pages, b, N, rows, dev_err, stream);
-  if (s == MLA_OK) s = mla_expand_kv(rows, N, w_uk, w_uv, k_c, v_c, dev_err, stream);
-  if (s == MLA_OK) s = mla_prefill_attention(q_c, q_r, M, rows, k_c, v_c, N, scale, out, dev_err, stream);
-  return s;
+  if (b < 0) return fail(MLA_ERR_INVALID_ARG, "b = %d < 0", b);
+  const int32_t zero = 0;
+  // one sequence: its block-table row b, its query rows at the start of q_c / q_r / out
+  return mla_prefill_decompress_batch(q_c, q_r, &b, &zero, &M, &N, 1, kv_cache, num_pages, block_table, b + 1,
+                                      max_pages, w_uk, w_uv, scale, workspace, ws_bytes, out, dev_err, stream);
 }
 
 mla_status mla_absorb_q(const void* q_c, const void* w_uk, void* q_abs, int32_t T, int32_t* dev_err, void* stream) {

@@ -6,8 +6,12 @@
 // path A: K = c_KV·W_UK per head, s = (q_c·K + q_R·k_R)·(d_hc + d_r)^-1/2;
 // [P2] MLA section: V = c_KV·W_UV; out = softmax(s)·V per head.
 //
-// One CTA = one head h and 128 query rows of one sequence; query row i sits
-// at position N - M + i and sees keys [0, N - M + i].  Key tiles of 128
+// One CTA = one head h and 128 query rows of one sequence of the batch
+// (blockIdx.z; its rows and cache tokens sit at offsets of the packed
+// arrays); query row i sits at position N - M + i and sees keys
+// [0, N - M + i].  Keys of a sequence's last tile that belong to the next
+// sequence are past N - 1 and always masked; query rows past M compute as
+// the last row and are not stored.  Key tiles of 128
 // tokens stream by TMA through two 2-deep rings, K = [K_c[h, ., 0:128] | k_R]
 // (192 columns, K-major) and V = V_c[h, ., :] (MN-major); K_c and V_c are
 // head-major, so a head's tile is 32 contiguous KB.  tcgen05:
@@ -103,7 +107,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qt = blockIdx.x, h = blockIdx.y;
   const int i0 = qt * kBM;
-  const int M = a.M, N = a.N;
+  const PrefillSeq sq = a.seq[blockIdx.z];
+  if (i0 >= sq.M) return;                             // this sequence has fewer query tiles
+  const int M = sq.M, N = sq.N;
   const int kv_base = N - M;                          // position of query row 0
   const int last_row = min(i0 + kBM, M) - 1;
   const int n_tiles = (kv_base + last_row) / kBN + 1;  // tiles any row of this CTA sees
@@ -152,9 +158,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&k_map);
       prefetch_tmap(&v_map);
       mbar_arrive_expect_tx(BAR(B_Q_FULL), (uint32_t)kQBytes);
-      tma_load_3d(base + kOffQ, &q_map, 0, h, i0, BAR(B_Q_FULL));
-      tma_load_3d(base + kOffQ + kChunkBytes, &q_map, 64, h, i0, BAR(B_Q_FULL));
-      tma_load_3d(base + kOffQ + 2 * kChunkBytes, &r_map, 0, h, i0, BAR(B_Q_FULL));
+      tma_load_3d(base + kOffQ, &q_map, 0, h, sq.q_off + i0, BAR(B_Q_FULL));
+      tma_load_3d(base + kOffQ + kChunkBytes, &q_map, 64, h, sq.q_off + i0, BAR(B_Q_FULL));
+      tma_load_3d(base + kOffQ + 2 * kChunkBytes, &r_map, 0, h, sq.q_off + i0, BAR(B_Q_FULL));
       // K(nk) as soon as its stage is free (QK^T(nk-2) done), V(nv) as soon as
       // its stage is free (P·V(nv-2) done); a tile's K goes before its V.
       int nk = 0, nv = 0;
@@ -164,7 +170,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       while (ok && nv < n_tiles) {
         bool progressed = false;
         if (nk < n_tiles && (nk < kStages || mbar_test_wait(BAR(B_K_EMPTY + nk % kStages), ((nk - kStages) / kStages) & 1))) {
-          const int st = nk % kStages, t0 = nk * kBN;
+          const int st = nk % kStages, t0 = sq.kv_off + nk * kBN;
           const uint32_t dst = base + kOffK + st * kKBytes;
           mbar_arrive_expect_tx(BAR(B_K_FULL + st), (uint32_t)kKBytes);
           tma_load_3d(dst, &k_map, 0, t0, h, BAR(B_K_FULL + st));
@@ -174,7 +180,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           progressed = true;
         }
         if (nv < nk && (nv < kStages || mbar_test_wait(BAR(B_V_EMPTY + nv % kStages), ((nv - kStages) / kStages) & 1))) {
-          const int st = nv % kStages, t0 = nv * kBN;
+          const int st = nv % kStages, t0 = sq.kv_off + nv * kBN;
           const uint32_t dst = base + kOffV + st * kVBytes;
           mbar_arrive_expect_tx(BAR(B_V_FULL + st), (uint32_t)kVBytes);
           tma_load_3d(dst, &v_map, 0, t0, h, BAR(B_V_FULL + st));
@@ -369,7 +375,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
         const float inv = 1.f / __uint_as_float(tmem_ld1_sync(tl + kColSum));
-        uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)min(i, M - 1) * 128 + h) * 128);
+        uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)(sq.q_off + min(i, M - 1)) * 128 + h) * 128);
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
           uint32_t o[32];
@@ -408,11 +414,13 @@ int prefill_smem_bytes() { return prefill::kSmemBytes; }
 cudaError_t launch_prefill_attn(const CUtensorMap& q_map, const CUtensorMap& r_map, const CUtensorMap& k_map,
                                 const CUtensorMap& kr_map, const CUtensorMap& v_map, const PrefillArgs& args,
                                 cudaStream_t stream) {
-  if (args.M <= 0) return cudaSuccess;
+  int max_m = 0;
+  for (int i = 0; i < args.nb; ++i) max_m = args.seq[i].M > max_m ? args.seq[i].M : max_m;
+  if (args.nb <= 0 || max_m <= 0) return cudaSuccess;
   cudaError_t e = cudaFuncSetAttribute(prefill::prefill_attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        prefill::kSmemBytes);
   if (e != cudaSuccess) return e;
-  dim3 grid((args.M + prefill::kBM - 1) / prefill::kBM, 128);
+  dim3 grid((max_m + prefill::kBM - 1) / prefill::kBM, 128, args.nb);
   prefill::prefill_attn_kernel<<<grid, prefill::kThreads, prefill::kSmemBytes, stream>>>(q_map, r_map, k_map,
                                                                                         kr_map, v_map, args);
   return cudaGetLastError();

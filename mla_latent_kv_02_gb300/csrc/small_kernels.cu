@@ -54,6 +54,36 @@ __global__ void __launch_bounds__(kWarps * 32)
   }
 }
 
+// The packed gather of several sequences (the decompress branch of a
+// batch): a warp finds its token's sequence by bisection of the offsets.
+__global__ void __launch_bounds__(kWarps * 32)
+    gather_batch_kernel(const uint4* __restrict__ cache, int64_t num_pages, const int32_t* __restrict__ block_table,
+                        int32_t max_pages, const __grid_constant__ GatherBatch g, uint4* __restrict__ out,
+                        int32_t* err) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t t = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); t < g.total;
+       t += (int64_t)gridDim.x * kWarps) {
+    int lo = 0, hi = g.nb - 1;  // the last sequence whose offset is <= t
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (g.off[mid] <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    const int64_t j = t - g.off[lo];
+    if (j < 0 || j >= g.n[lo]) {  // offsets inconsistent with the lengths
+      if (lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_BATCH);
+      continue;
+    }
+    const int32_t pid = __ldg(block_table + (int64_t)g.b[lo] * max_pages + j / 64);
+    if (pid < 0 || (int64_t)pid >= num_pages) {
+      if (lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_PAGE_OOB);
+      continue;
+    }
+    const uint4* src = cache + ((int64_t)pid * 64 + j % 64) * kRowVec;
+    for (int k = lane; k < kRowVec; k += 32) out[t * kRowVec + k] = __ldg(src + k);
+  }
+}
+
 inline int blocks_for(int64_t items) {
   int64_t b = (items + kWarps - 1) / kWarps;
   if (b > 152 * 16) b = 152 * 16;
@@ -77,6 +107,16 @@ cudaError_t launch_gather(const uint16_t* kv_cache, int64_t num_pages, const int
   small::gather_kernel<<<small::blocks_for(n_tokens), small::kWarps * 32, 0, stream>>>(
       reinterpret_cast<const uint4*>(kv_cache), num_pages, block_table, max_pages, b, n_tokens,
       reinterpret_cast<uint4*>(out), dev_err);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_batch(const uint16_t* kv_cache, int64_t num_pages, const int32_t* block_table,
+                                int32_t max_pages, const GatherBatch& g, uint16_t* out, int32_t* dev_err,
+                                cudaStream_t stream) {
+  if (g.total <= 0 || g.nb <= 0) return cudaSuccess;
+  small::gather_batch_kernel<<<small::blocks_for(g.total), small::kWarps * 32, 0, stream>>>(
+      reinterpret_cast<const uint4*>(kv_cache), num_pages, block_table, max_pages, g, reinterpret_cast<uint4*>(out),
+      dev_err);
   return cudaGetLastError();
 }
 

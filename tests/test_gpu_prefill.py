@@ -165,3 +165,82 @@ def test_decompress_rejects_bad_arguments(api):
                                    out, dc.dev_err)
     torch.cuda.synchronize()
     assert int(dc.dev_err.item()) == 0
+
+
+def _decompress_batch(api, case, dc, seqs):
+    """The branch for the sequences `seqs` of a device case in one batched call;
+    returns out [T, 128, 128] with the chunks' rows written (others NaN)."""
+    n = [int(case.seq_lens[b]) for b in seqs]
+    ws = torch.empty(api.mla_prefill_batch_workspace_size(n), dtype=torch.uint8, device="cuda")
+    out = torch.full((case.T, 128, 128), float("nan"), dtype=torch.bfloat16, device="cuda")
+    api.mla_prefill_decompress_batch(dc.q_c, dc.q_r, dc.kv_cache, dc.block_table, seqs,
+                                     [int(case.q_start[b]) for b in seqs], [int(case.q_lens[b]) for b in seqs], n,
+                                     dc.w_uk, dc.w_uv, ws, out, dc.dev_err)
+    assert api.mla_check(dc.dev_err) == 0
+    return out
+
+
+def test_decompress_batch_equals_per_sequence_calls(api):
+    """Three qualifying sequences of different lengths (several query tiles,
+    ragged tiles, a chunk that fills its cache) around an absorbed one: the
+    batched call (one gather, one expansion, one attention launch over the
+    packed arrays) gives, row for row, the bits of one call per sequence,
+    writes nothing else, and matches the oracle on sampled rows."""
+    case = wl.make_case([700, 200, 300, 1000], [300, 1, 300, 512], seed=101)
+    dc = DeviceCase(case)
+    seqs = [b for b in range(case.B) if api.mla_branch_for(int(case.q_lens[b])) == 1]
+    assert seqs == [0, 2, 3]
+    got = _decompress_batch(api, case, dc, seqs)
+    for b in seqs:
+        r0, q = int(case.q_start[b]), int(case.q_lens[b])
+        one = _decompress(api, case, dc, b)
+        assert torch.equal(got[r0:r0 + q], one), f"sequence {b}"
+    absorbed_rows = int(case.q_start[1])
+    assert torch.isnan(got[absorbed_rows].float()).all(), "the batched call wrote an absorbed sequence's row"
+    rows = sorted({0, 299, 300 + 1, 301 + 150, 601, 601 + 255, 601 + 256, case.T - 1})
+    cache = oracle.append(np.zeros((case.num_pages, 64, 576), dtype=np.float32), case.c_kv, case.k_r,
+                          oracle.slot_mapping(case.block_table, *case.positions()))
+    ref = oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table, case.seq_lens,
+                          case.q_lens, SCALE, rows=rows)
+    assert_close(to_np(got)[rows], ref["out"][rows], "batched decompress out")
+
+
+def test_decompress_batch_full_size_chunked_prefill(api):
+    """The chunked-prefill workload (B4 x (16384 + 512)) through one batched
+    call: the same bits as the per-sequence calls, and sampled rows against
+    the oracle."""
+    case = wl.workload(4)
+    dc = DeviceCase(case)
+    got = _decompress_batch(api, case, dc, list(range(case.B)))
+    for b in (0, case.B - 1):
+        r0 = int(case.q_start[b])
+        assert torch.equal(got[r0:r0 + 512], _decompress(api, case, dc, b)), f"sequence {b}"
+    rows = [3, 700, 1300, case.T - 2]
+    cache = oracle.append(np.zeros((case.num_pages, 64, 576), dtype=np.float32), case.c_kv, case.k_r,
+                          oracle.slot_mapping(case.block_table, *case.positions()))
+    ref = oracle.mla_step(case.q_c, case.q_r, case.w_uk, case.w_uv, cache, case.block_table, case.seq_lens,
+                          case.q_lens, SCALE, rows=rows)
+    assert_close(to_np(got)[rows], ref["out"][rows], "batched chunked prefill out")
+
+
+def test_decompress_batch_rejects_bad_arguments(api):
+    case = wl.make_case([300, 300], [260, 260], seed=102)
+    dc = DeviceCase(case)
+    ws = torch.empty(api.mla_prefill_batch_workspace_size([300, 300]), dtype=torch.uint8, device="cuda")
+    out = torch.empty((case.T, 128, 128), dtype=torch.bfloat16, device="cuda")
+    ok = dict(seq_ids=[0, 1], q_starts=[0, 260], q_lens=[260, 260], n_tokens=[300, 300])
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        api.mla_prefill_decompress_batch(dc.q_c, dc.q_r, dc.kv_cache, dc.block_table, a["seq_ids"], a["q_starts"],
+                                         a["q_lens"], a["n_tokens"], dc.w_uk, dc.w_uv, a.get("ws", ws), out,
+                                         dc.dev_err)
+
+    for bad in (dict(seq_ids=[0, 2]), dict(q_lens=[301, 260]), dict(q_lens=[0, 260]), dict(n_tokens=[300, 5000]),
+                dict(q_starts=[-1, 260]), dict(ws=ws[:1024])):
+        with pytest.raises(api.MlaError):
+            call(**bad)
+    with pytest.raises(api.MlaError):
+        api.mla_prefill_batch_workspace_size([10] * 65)
+    torch.cuda.synchronize()
+    assert int(dc.dev_err.item()) == 0
