@@ -13,21 +13,18 @@
 //  * The score contraction (576) is split evenly: CTA r takes latent chunks
 //    4r..4r+3 (64 columns each, 128-byte swizzle) and RoPE dims [32r, 32r+32)
 //    (64-byte swizzle).  Each CTA computes a partial S = Q_r·K_r^T (tcgen05,
-//    M = 128 heads, N = 64 tokens, A = Q's latent half from TMEM and its RoPE
-//    half from shared memory, B = the page tile in shared memory) into one of
-//    two TMEM score buffers, so QK^T of tile t+1 runs while the softmax of
-//    tile t works.  The partials are exchanged unscaled as fp16 (the scale times
+//    M = 128 heads, N = 64 tokens, A = Q from TMEM, B = the page tile in shared
+//    memory).  The partials are exchanged unscaled as fp16 (the scale times
 //    log2 e enters once, in the exponent of P): each
 //    warp stages its rows and one bulk copy per warp pushes them into the peer
 //    CTA, completing on the peer's mbarrier.  Both CTAs add the same two
 //    rounded halves, so they hold bit-identical S and take identical softmax
 //    decisions.
 //  * Softmax in packed fp16 (add, max, subtract, 2^x with one MUFU issue per
-//    pair), P converted to bf16 and written over the scores it came from in
-//    TMEM; O_r += P·V_r (tcgen05, N = 256, A = P from TMEM, B = the same page
-//    tile read as an MN-major operand).  The row sum l is kept by the
-//    softmax threads, summing the rounded P the tensor core accumulates, and
-//    passed from tile to tile like the reference max.
+//    pair), P converted to bf16 and written to TMEM; O_r += P·V_r (tcgen05,
+//    N = 256, B = the same page tile read as an MN-major operand) and the row
+//    sums l += P·1 (N = 16 against a tile of ones), so l matches exactly the
+//    bf16 P the tensor core accumulated.
 //  * Exchange ring: kXBufs receive buffers per CTA; tile t lands in buffer
 //    t mod kXBufs, and the rows this CTA sends for tile t are staged in its own
 //    buffer (t + kXLead) mod kXBufs.  Pushing tile t needs only the peer's tile
@@ -35,15 +32,14 @@
 //    the buffer tile t goes to has finished, and that the peer had consumed
 //    what it held.  No release message crosses the cluster.
 //  * Two softmax warpgroups take alternate tiles, each tile whole (thread =
-//    head row = TMEM lane, all 64 tokens), warpgroup w with score buffer w:
-//    while one waits for the peer's half of its tile, the other computes.
-//    The only hand-offs between them are the row's reference max and row
-//    sum, passed from tile g-1 to tile g through tagged shared-memory slots.
-//    QK^T and P·V are issued by two warps, each as soon as its own inputs are
-//    ready; QK^T of tile t+2 waits for P·V of tile t, which read its buffer.
+//    head row = TMEM lane, all 64 tokens): while one waits for the peer's half
+//    of its tile, the other computes.  The only hand-off between them is the
+//    row's reference max, passed from tile g-1 to tile g through a tagged
+//    shared-memory slot.  QK^T and P·V are issued by two warps, each as soon
+//    as its own inputs are ready.
 //  * Online softmax with lazy rescaling: the running reference max only moves
 //    when a tile's max exceeds it by more than 8 (log2 units), so P stays
-//    below 256 and O (TMEM) and l are rescaled only on those rare tiles.
+//    below 256 and O and l in TMEM are rescaled only on those rare tiles.
 //  * Warp roles: warp 0 TMA producer, warp 1 TMEM allocation + QK^T issue,
 //    warps 2-9 softmax/epilogue (two warpgroups), warp 10 P·V issue.
 //  * Work: the plan cuts all rows' 64-token tiles into equal contiguous ranges,
@@ -82,29 +78,28 @@ constexpr int kXWarp = 32 * kXRow;                        // one warp's 32 rows 
 constexpr int kXBufs = 4;                                 // exchange ring depth
 constexpr int kXLead = kXBufs - 2;                        // staging buffer offset
 static_assert(kXLead >= 1 && kXLead <= kXBufs - 2, "the exchange ring needs two tiles between staging and reuse");
-constexpr int kQRBytes = kH * kRopeHalf * 2;             // Q's RoPE half [128 x 32], 64-byte swizzle (8 KB)
+constexpr int kOnesBytes = 16 * kChunk * 2;               // [16 x 64] bf16 ones for the row sums
 
 // FP8 stage (one page, this CTA's half): the 32 KB latent area, whose first
 // 16 KB first receive the 64 token rows of 256 E4M3 codes and are then
-// overwritten by their bf16 values, and the RoPE half (64-byte swizzle); the
-// page's 64 token scales go to a small ring of their own.
+// overwritten by their bf16 values; the RoPE half (64-byte swizzle); the 64
+// token scales.
 constexpr int kF8Codes = kPage * 256;                     // 16 KB
 constexpr int kF8RopeOff = 4 * kChunkBytes;               // 32 KB
-constexpr int kF8ScaleBytes = kPage * 4;
-constexpr int kF8Payload = kF8Codes + kRopeBytes + kF8ScaleBytes;  // bytes the copies deliver per stage
-constexpr int kF8StageBytes = 36 * 1024;
+constexpr int kF8ScaleOff = kF8RopeOff + kRopeBytes;
+constexpr int kF8Payload = kF8Codes + kRopeBytes + kPage * 4;  // bytes the TMA delivers per stage
+constexpr int kF8StageBytes = 37 * 1024;                  // keeps every stage 1024-byte aligned
 constexpr int kConvWarps = 4;
 constexpr uint32_t kConvBarrier = 1;                      // named barrier of the converter warps
-static_assert(kF8RopeOff + kRopeBytes <= kF8StageBytes, "FP8 stage too small");
+static_assert(kF8ScaleOff + kPage * 4 <= kF8StageBytes, "FP8 stage too small");
 
-// Shared memory: a small region (barriers, row-max and row-sum slots,
-// flags) at the start, then the 1024-byte aligned region (page ring,
-// exchange ring, Q's RoPE half, FP8 scale ring).
+// Shared memory: a small region (barriers, row-max slots, flags) at the
+// start, then the 1024-byte aligned region (page ring, FP8 staging ring,
+// exchange ring, the ones tile).
 constexpr int kNumBars = 32;
 constexpr int kSmallBar = 0;
 constexpr int kSmallPair = kSmallBar + 8 * kNumBars;      // uint2 [4][128]: {reference max bits, tile}
-constexpr int kSmallSum = kSmallPair + 4 * kH * 8;        // uint2 [4][128]: {row sum bits, tile}
-constexpr int kSmallMisc = kSmallSum + 4 * kH * 8;
+constexpr int kSmallMisc = kSmallPair + 4 * kH * 8;
 // misc: +0 abort flag, +8 TMEM address, +16 segment range [2], +32 copies
 // issued per softmax warp [8], +64 the peer's copies [8] (written by the
 // peer), +96 the abort flags of this CTA and the peer [2], +104 the last tile
@@ -114,7 +109,7 @@ constexpr int kSmallBytes = kSmallMisc + 128;
 
 // The two cache formats.  bf16: the producer's TMA fills a 4-deep ring of
 // [latent half | RoPE half] stages.  FP8: the TMA fills the same 4-deep ring
-// with [codes | RoPE half] and the scale ring, and a converter warpgroup dequantises
+// with [codes | RoPE half | scales], and a converter warpgroup dequantises
 // the codes in place (all codes read into registers, a barrier, then the
 // bf16 rows written over them).  Warp roles:
 //   bf16: 0 producer, 1 QK^T, 2-9 softmax, 10 P·V                (352 threads)
@@ -132,7 +127,7 @@ struct Cfg<false> {
 template <>
 struct Cfg<true> {
   static constexpr int kStages = 4;
-  static constexpr int kStageBytes = kF8StageBytes;                 // 36 KB
+  static constexpr int kStageBytes = kF8StageBytes;                 // 37 KB
   static constexpr int kSoftWarp0 = 4, kPvWarp = 2, kConvWarp0 = 12;
   static constexpr int kThreads = 512;
 };
@@ -142,23 +137,20 @@ struct Layout : Cfg<kF8> {
   using C = Cfg<kF8>;
   static constexpr int kOffKV = 0;
   static constexpr int kOffX = C::kStages * C::kStageBytes;
-  static constexpr int kOffQR = kOffX + kXBufs * kXBytes;
-  static constexpr int kOffScale = kOffQR + kQRBytes;            // FP8 only: [kStages][64] fp32
-  static constexpr int kAlignedBytes = kOffScale + (kF8 ? C::kStages * kF8ScaleBytes : 0);
+  static constexpr int kOffOnes = kOffX + kXBufs * kXBytes;
+  static constexpr int kAlignedBytes = kOffOnes + kOnesBytes;
   static constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
   static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
   enum : int {
     B_KV_FULL = 0,
     B_KV_EMPTY = C::kStages,
-    // S_FULL, P_FULL and O_DONE come in pairs by tile parity (the S/P
-    // buffer of tile t is t mod 2): each waiter waits on a pair's phases in
-    // order (a parity test cannot tell a phase from the one two before it, and
-    // the warpgroups run apart).  O_DONE(t) (P·V of tile t complete) also
-    // frees S buffer t mod 2 for QK^T of tile t+2.
+    // S_FULL and O_DONE come in pairs by tile parity: each softmax warpgroup
+    // waits only on its own tiles' phases, in order (a parity test cannot tell
+    // a phase from the one two before it, and the warpgroups run apart).
     B_S_FULL0 = 2 * C::kStages,
     B_S_FULL1,
-    B_P_FULL0,
-    B_P_FULL1,
+    B_S_FREE,
+    B_P_FULL,
     B_O_DONE0,
     B_O_DONE1,
     B_Q_READY,
@@ -172,15 +164,11 @@ struct Layout : Cfg<kF8> {
   static_assert(B_COUNT <= kNumBars, "barrier area too small");
 };
 
-// TMEM: O (this CTA's 256 latent columns), Q's latent half (bf16 pairs), two
-// 64-column score buffers; P of tile t (bf16 pairs) is written over the
-// first 32 columns of S buffer t mod 2 once its scores have been read.
-constexpr uint32_t kColO = 0, kColQ = 256, kColS = 384, kSBufCols = 64, kTmemCols = 512;
+constexpr uint32_t kColO = 0, kColS = 256, kColSum = 320, kColQ = 336, kColP = 480, kTmemCols = 512;
 // The producer and the two MMA-issuing threads poll (mbarrier.test_wait)
 // rather than sleep: their wake-up sits on the score chain.
 constexpr bool kIssueSuspend = false;
 constexpr uint32_t kTileThreads = 128;                    // the warpgroup that handles one tile
-
 
 // bf16 operands for the bf16 cache; f16 for the FP8 cache (an E4M3 value is
 // an exact f16, and P is computed in f16 in both).
@@ -188,6 +176,7 @@ template <bool kF8>
 struct Idesc {
   static constexpr uint32_t kQK = kF8 ? idesc_f16_f32(128, 64, false, false) : idesc_bf16_f32(128, 64, false, false);
   static constexpr uint32_t kPV = kF8 ? idesc_f16_f32(128, 256, false, true) : idesc_bf16_f32(128, 256, false, true);
+  static constexpr uint32_t kSum = kF8 ? idesc_f16_f32(128, 16, false, false) : idesc_bf16_f32(128, 16, false, false);
 };
 
 // Walks the 64-token tiles of a cluster's segments in order; a segment's
@@ -236,19 +225,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
   using L = Layout<kF8>;
   constexpr int kStages = L::kStages, kStageBytes = L::kStageBytes, kThreads = L::kThreads;
   constexpr int kPvWarp = L::kPvWarp, kSoftWarp0 = L::kSoftWarp0, kConvWarp0 = L::kConvWarp0;
-  constexpr int kOffKV = L::kOffKV, kOffX = L::kOffX, kOffQR = L::kOffQR, kOffScale = L::kOffScale;
+  constexpr int kOffKV = L::kOffKV, kOffX = L::kOffX, kOffOnes = L::kOffOnes;
   constexpr int kAlignedBytes = L::kAlignedBytes, kSmemBytes = L::kSmemBytes;
   constexpr int B_KV_FULL = L::B_KV_FULL, B_KV_EMPTY = L::B_KV_EMPTY, B_S_FULL0 = L::B_S_FULL0,
-                B_S_FULL1 = L::B_S_FULL1, B_P_FULL0 = L::B_P_FULL0, B_P_FULL1 = L::B_P_FULL1,
+                B_S_FULL1 = L::B_S_FULL1, B_S_FREE = L::B_S_FREE, B_P_FULL = L::B_P_FULL,
                 B_O_DONE0 = L::B_O_DONE0, B_O_DONE1 = L::B_O_DONE1, B_Q_READY = L::B_Q_READY,
                 B_O_FREE = L::B_O_FREE, B_X_FULL0 = L::B_X_FULL0, B_DRAIN = L::B_DRAIN, B_DRAIN_PV = L::B_DRAIN_PV,
                 B_F8_FULL = L::B_F8_FULL;
-  constexpr uint32_t kIdescQK = Idesc<kF8>::kQK, kIdescPV = Idesc<kF8>::kPV;
+  constexpr uint32_t kIdescQK = Idesc<kF8>::kQK, kIdescPV = Idesc<kF8>::kPV, kIdescSum = Idesc<kF8>::kSum;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t bars = raw + kSmallBar;
   const uint32_t pair = raw + kSmallPair;  // uint2 slots, accessed with volatile ld/st
-  const uint32_t sums = raw + kSmallSum;   // likewise
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem_raw + kSmallMisc);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + kSmallMisc + 8);
   int32_t* seg_range = reinterpret_cast<int32_t*>(smem_raw + kSmallMisc + 16);
@@ -275,8 +263,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     }
     mbar_init(BAR(B_S_FULL0), 1);
     mbar_init(BAR(B_S_FULL1), 1);
-    mbar_init(BAR(B_P_FULL0), kTileThreads / 32);  // one arrival per warp
-    mbar_init(BAR(B_P_FULL1), kTileThreads / 32);
+    mbar_init(BAR(B_S_FREE), kTileThreads / 32);  // one arrival per warp
+    mbar_init(BAR(B_P_FULL), kTileThreads / 32);
     mbar_init(BAR(B_O_DONE0), 1);
     mbar_init(BAR(B_O_DONE1), 1);
     mbar_init(BAR(B_Q_READY), kTileThreads);
@@ -313,10 +301,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     seg_range[0] = sb;
     seg_range[1] = se;
   }
-  // Row-max and row-sum slots start with an impossible tile tag.
-  for (int i = threadIdx.x; i < 4 * kH; i += kThreads) {
-    st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
-    st_shared_v2_volatile(sums + 8u * i, 0u, 0xFFFFFFFFu);
+  // Row-max slots start with an impossible tile tag; the ones tile feeds the
+  // row-sum MMA (written by the generic proxy, read by the tensor core).
+  for (int i = threadIdx.x; i < 4 * kH; i += kThreads) st_shared_v2_volatile(pair + 8u * i, 0u, 0xFFFFFFFFu);
+  if (layout_fits) {
+    uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + kOffOnes);
+    const uint32_t one2 = kF8 ? 0x3C003C00u : 0x3F803F80u;  // f16 / bf16 1.0 pairs
+    for (int i = threadIdx.x; i < kOnesBytes / 4; i += kThreads) ones[i] = one2;
+    fence_proxy_async_smem();
   }
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&kv_map);
@@ -374,8 +366,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
             mbar_arrive_expect_tx(BAR(B_F8_FULL + st), (uint32_t)kF8Payload);
             tma_load_2d(dst, &kv_map, (int)(256 * rank), pid * kPage, BAR(B_F8_FULL + st));
             tma_load_2d(dst + kF8RopeOff, &rope_map, 256 + (int)rank * kRopeHalf, pid * kPage, BAR(B_F8_FULL + st));
-            bulk_load_g2s(base + kOffScale + st * kF8ScaleBytes, a.kv_scales + (size_t)pid * kPage, kF8ScaleBytes,
-                          BAR(B_F8_FULL + st));
+            bulk_load_g2s(dst + kF8ScaleOff, a.kv_scales + (size_t)pid * kPage, kPage * 4, BAR(B_F8_FULL + st));
           } else {
             mbar_arrive_expect_tx(BAR(B_KV_FULL + st), (uint32_t)kStageBytes);
             // latent chunks 4r..4r+3 in one 3D box, then the RoPE half
@@ -394,9 +385,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
   };
   auto role_qk = [&]() {
     // ---------------------------------------------------------------- QK^T issue
-    // S_partial(t) = Q_r · K_r(t)^T into S buffer t mod 2 as soon as page t
-    // has landed and P·V of tile t-2 (whose P sits in that buffer) is
-    // complete.  P·V is issued by its own warp, so a long
+    // S_partial(t) = Q_r · K_r(t)^T as soon as page t has landed and the
+    // softmax has read S(t-1).  P·V is issued by its own warp, so a long
     // QK^T issue (the tensor pipe throttles it) never delays P·V, nor the
     // other way round; the two streams share only the tensor pipe.
     if (lane == 0) {
@@ -407,35 +397,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       // (no carry: shared addresses stay below 2^18).
       const uint64_t kdesc0 = sdesc_sw128(base + kOffKV, 16, 1024);
       const uint64_t rdesc0 = sdesc_sw64(base + kOffKV + 4 * kChunkBytes, 16, 512);
-      const uint64_t qrdesc = sdesc_sw64(base + kOffQR, 16, 512);  // Q's RoPE half, K-major
       for (uint32_t tq = 0; cq.valid(); ++tq) {
         const uint32_t st = tq % kStages;
         if (!wait_phase<false, kIssueSuspend>(BAR(B_KV_FULL + st), (tq / kStages) & 1u, err, abort_flag, a.wait_limit, a.wait_every)) break;
         // FP8: the RoPE half came with the codes (already complete; waited for its TMA visibility)
         if (kF8 && !wait_phase<false, kIssueSuspend>(BAR(B_F8_FULL + st), (tq / kStages) & 1u, err, abort_flag, a.wait_limit, a.wait_every))
           break;
-        if (tq >= 2 && !wait_phase<false, kIssueSuspend>(BAR(B_O_DONE0 + (tq & 1u)), ((tq >> 1) - 1u) & 1u, err, abort_flag,
-                                                          a.wait_limit, a.wait_every))
-          break;
+        if (tq > 0 && !wait_phase<false, kIssueSuspend>(BAR(B_S_FREE), (tq - 1) & 1u, err, abort_flag, a.wait_limit, a.wait_every)) break;
         if (cq.first() &&
             !wait_phase<false, kIssueSuspend>(BAR(B_Q_READY), (uint32_t)(cq.s - s_begin) & 1u, err, abort_flag, a.wait_limit, a.wait_every))
           break;
         tc_fence_after();
         // [128 x 64] += Q_r[128 x 288] · K_r^T, K-major, 16 per step: 4 latent
-        // chunks (128-byte swizzle; Q from TMEM) then the RoPE half (64-byte
-        // swizzle; Q from shared memory).
+        // chunks (128-byte swizzle) then the RoPE half (64-byte swizzle).
         const uint64_t dk = kdesc0 + (uint64_t)((st * kStageBytes) >> 4);
         const uint64_t dr = rdesc0 + (uint64_t)((st * kStageBytes) >> 4);
-        const uint32_t sbuf = tmem + kColS + (tq & 1u) * kSBufCols;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ts(sbuf, tmem + kColQ + i * 32 + kk * 8, dk + (uint64_t)((i * kChunkBytes + kk * 32) >> 4),
+            mma_ts(tmem + kColS, tmem + kColQ + i * 32 + kk * 8, dk + (uint64_t)((i * kChunkBytes + kk * 32) >> 4),
                    kIdescQK, (i | kk) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk)
-          mma_ss(sbuf, qrdesc + (uint64_t)((kk * 32) >> 4), dr + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
+          mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, dr + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
         tc_commit(BAR(B_S_FULL0 + (tq & 1u)));
         cq.next();
       }
@@ -450,28 +435,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     if (lane == 0) {
       TileCursor cp;
       cp.init(a.segs, s_begin, s_end);
-      // The latent chunks read MN-major for P·V.
+      // The latent chunks read MN-major for P·V, and the ones tile.
       const uint64_t vdesc0 = sdesc_sw128(base + kOffKV, 8192, 1024);
+      const uint64_t odesc0 = sdesc_sw128(base + kOffOnes, 16, 1024);
       for (uint32_t tp = 0; cp.valid(); ++tp) {
         const bool first = cp.first();
-        if (!wait_phase<false, kIssueSuspend>(BAR(B_P_FULL0 + (tp & 1u)), (tp >> 1) & 1u, err, abort_flag, a.wait_limit,
-                                              a.wait_every))
-          break;
+        if (!wait_phase<false, kIssueSuspend>(BAR(B_P_FULL), tp & 1u, err, abort_flag, a.wait_limit, a.wait_every)) break;
         if (first && !wait_phase<false, kIssueSuspend>(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u, err, abort_flag, a.wait_limit, a.wait_every))
           break;
         tc_fence_after();
-        // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; P from S buffer tp mod
-        // 2; V_r is MN-major: 4 atoms of 64 columns 8 KB apart (LBO), 8-token
-        // row groups 1 KB apart (SBO).
+        // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
+        // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
+        // l[128 x 16] += P · 1 (every column holds the row sum of P), issued
+        // interleaved so consecutive MMAs never share an accumulator.
         const uint64_t dv = vdesc0 + (uint64_t)(((tp % kStages) * kStageBytes) >> 4);
-        const uint32_t pbuf = tmem + kColS + (tp & 1u) * kSBufCols;
 #pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          mma_ts(tmem + kColO, pbuf + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV,
-                 (first && kk == 0) ? 0u : 1u);
+        for (int kk = 0; kk < 4; ++kk) {
+          const uint32_t acc = (first && kk == 0) ? 0u : 1u;
+          mma_ts(tmem + kColO, tmem + kColP + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, acc);
+          mma_ts(tmem + kColSum, tmem + kColP + kk * 8, odesc0 + (uint64_t)((kk * 32) >> 4), kIdescSum, acc);
+        }
         // QK^T(tp) is complete (its scores were read before P(tp) existed), so
-        // this commit frees the page stage once P·V(tp) has read it; O_DONE
-        // also frees S buffer tp mod 2.
+        // this commit frees the page stage once P·V(tp) has read it.
         tc_commit(BAR(B_KV_EMPTY + tp % kStages));
         tc_commit(BAR(B_O_DONE0 + (tp & 1u)));
         cp.next();
@@ -525,7 +510,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
         const uint32_t r = (uint32_t)(kConvWarps * j + cw);
         code[j] = ld_shared_v2(stage + r * 256u + (uint32_t)lane * 8u);
         bool ok_j;
-        fac[j] = fp8_f16_factor(ld_shared_f32(base + kOffScale + st * kF8ScaleBytes + 4u * r), ok_j);
+        fac[j] = fp8_f16_factor(ld_shared_f32(stage + kF8ScaleOff + 4u * r), ok_j);
         in_range = in_range && ok_j;
       }
       if (!in_range && lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_FP8_RANGE);  // warp-uniform
@@ -591,10 +576,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
     const __half2 c2h = __float2half2_rn(c2);
     __syncwarp();
 
-    // Q_r of a segment's row, this thread's row: the latent half into TMEM
-    // (128 columns), the RoPE half into shared memory (K-major, 64-byte
-    // swizzle: 16-byte chunk c of row h at c ^ ((h >> 1) & 3)), in two rounds
-    // of loads so that at most 20 16-byte values are live.
+    // Q_r of a segment's row into TMEM, this thread's row (144 columns), in
+    // two rounds of loads so that at most 20 16-byte values are live.
     auto load_q = [&](int s) {
       const int row = a.segs[8 * s];
       const uint4* lat = reinterpret_cast<const uint4*>(a.q_abs + ((size_t)row * kH + h) * kDC + rank * 256);
@@ -625,28 +608,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
           tmem_st32(tl + kColQ + half * 64 + ci * 32, r);
         }
         if (half == 0) {
-          const uint32_t qr_row = base + kOffQR + (uint32_t)h * 64u;
+          uint32_t r[16];
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
-            uint32_t x = v[16 + j].x, y = v[16 + j].y, z = v[16 + j].z, w = v[16 + j].w;
-            if constexpr (kF8) {
-              x = bf16x2_to_f16x2(x);
-              y = bf16x2_to_f16x2(y);
-              z = bf16x2_to_f16x2(z);
-              w = bf16x2_to_f16x2(w);
-            }
-            st_shared_v4(qr_row + (((uint32_t)j ^ (((uint32_t)h >> 1) & 3u)) << 4), x, y, z, w);
+            r[4 * j] = v[16 + j].x;
+            r[4 * j + 1] = v[16 + j].y;
+            r[4 * j + 2] = v[16 + j].z;
+            r[4 * j + 3] = v[16 + j].w;
           }
+          if constexpr (kF8) {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) r[j] = bf16x2_to_f16x2(r[j]);
+          }
+          tmem_st16(tl + kColQ + 128, r);
         }
       }
       tmem_st_wait();
-      fence_proxy_async_smem();  // the RoPE half is read by the tensor core
       tc_fence_before();
       mbar_arrive(BAR(B_Q_READY));
     };
 
-    // Read this row's 64 partial scores of tile t, push the fp16 partial to
-    // the peer, and load the next segment's Q if tile
+    // Read this row's 64 partial scores of tile t, free S, push the fp16
+    // partial to the peer, and load the next segment's Q if tile
     // t ends a segment (its QK^T was the segment's last).  `own` keeps the
     // rounded values.
     auto fetch_push = [&](uint32_t t, const TileCursor& c, uint32_t (&own)[kWords]) -> bool {
@@ -655,7 +638,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       tc_fence_after();
       {
         uint32_t r[64];
-        tmem_ld64_sync(tl + kColS + (t & 1u) * kSBufCols, r);
+        tmem_ld64_sync(tl + kColS, r);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_S_FREE));
 #pragma unroll
         for (int j = 0; j < kWords; ++j)
           own[j] = cvt_f16x2_satfinite(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
@@ -745,6 +731,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       const float mt = fmaxf(__low2float(mh), __high2float(mh));
 
       // ---- reference max: tile g-1's (the other warpgroup's) unless this tile starts a segment
+      const uint32_t gp = g - 1;  // the previous tile (the other warpgroup's)
+      const bool od_ready = (g == 0) || mbar_test_wait(BAR(B_O_DONE0 + (gp & 1u)), (gp >> 1) & 1u);
       float m = mt, factor = 1.f;
       bool resc = false;
       if (!cf.first()) {
@@ -772,44 +760,37 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
           m = mp;
         }
       }
-      // Hand m to tile g+1.  Four slots (here and for the row sums below):
-      // the next writer of tile g-1's slot is tile g+3, whose scores need P·V
-      // of tile g+1 complete, hence P of tile g, written by this warpgroup
-      // only after it read both of tile g-1's slots; two slots would not do,
-      // since a tile that starts a segment reads none and may run ahead.
+      // Hand m to tile g+1.  Four slots: the next writer of this one is tile
+      // g+4, and the next writer of tile g-1's is tile g+3, which needs S
+      // freed by tile g+2, fetched by this warpgroup only after this read;
+      // two slots would not do, since a tile that starts a segment reads none
+      // and may run ahead.
       st_shared_v2_volatile(pair + 8u * ((g & 3u) * kH + h), __float_as_uint(m), g);
 
       // ---- P = 2^(c2 (s - m)) in fp16 pairs (one fused multiply-add for the
       //      exponent), stored as bf16 for the tensor core (the FP8 cache's
-      //      f16 operands take the fp16 P as it is), and the row sum of P as
-      //      the tensor core sees it (the rounded values, summed in fp32)
+      //      f16 operands take the fp16 P as it is)
       const __half2 mc2 = __float2half2_rn(-m * c2);
-      float rs0 = 0.f, rs1 = 0.f;
 #pragma unroll
       for (int j = 0; j < kWords; ++j) {
         const uint32_t p16 = ex2_f16x2(as_u32(__hfma2(as_h2(own[j]), c2h, mc2)));
-        const float2 p = __half22float2(as_h2(p16));
         if constexpr (kF8) {
           own[j] = p16;
-          rs0 += p.x;
-          rs1 += p.y;
         } else {
+          const float2 p = __half22float2(as_h2(p16));
           own[j] = pack_bf16x2(p.x, p.y);
-          rs0 += __uint_as_float(own[j] << 16);
-          rs1 += __uint_as_float(own[j] & 0xFFFF0000u);
         }
       }
-      const float rsum = rs0 + rs1;
-      // ---- a rescale (rare) needs P·V of tile g-1 complete; P·V of this
-      //      tile waits for P_FULL below
-      if (__any_sync(0xffffffffu, resc)) {
-        w = wait_phase<false, true>(BAR(B_O_DONE0 + ((g - 1) & 1u)), ((g - 1) >> 1) & 1u, err, abort_flag, a.wait_limit,
-                                    a.wait_every);
+      // Writing P (single TMEM buffer) and a rescale both need P·V of tile g-1 done.
+      if (g > 0) {
+        w = od_ready || wait_phase<false, true>(BAR(B_O_DONE0 + (gp & 1u)), (gp >> 1) & 1u, err, abort_flag, a.wait_limit, a.wait_every);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
         }
         tc_fence_after();
+      }
+      if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll 1
         for (int c = 0; c < 256; c += 32) {
           uint32_t o[32];
@@ -818,36 +799,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * factor);
           tmem_st32(tl + kColO + c, o);
         }
+        tmem_st1(tl + kColSum, __float_as_uint(__uint_as_float(tmem_ld1_sync(tl + kColSum)) * factor));
       }
-      // P over the scores it came from (S buffer g mod 2)
-      tmem_st32(tl + kColS + (g & 1u) * kSBufCols, own);
+      tmem_st32(tl + kColP, own);
       tmem_st_wait();
-      // ---- row sum l(g) = l(g-1) * factor + rowsum(P), l(g-1) from the
-      //      other warpgroup's slot unless this tile starts a segment
-      float lrow = rsum;
-      if (!cf.first()) {
-        const uint32_t slot = sums + 8u * (((g - 1) & 3u) * kH + h);
-        uint2 v = ld_shared_v2_volatile(slot);
-        if (v.y != g - 1) {
-          const uint64_t t0 = cycles();
-          for (uint32_t it = 1; (v = ld_shared_v2_volatile(slot)).y != g - 1; ++it) {
-            if ((it & a.wait_every) == 0u && (*abort_flag || cycles() - t0 > a.wait_limit)) {
-              if (!*abort_flag) atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
-              *abort_flag = 1;
-              break;
-            }
-          }
-        }
-        if (!__all_sync(0xffffffffu, v.y == g - 1)) {
-          ok = false;
-          break;
-        }
-        lrow = fmaf(__uint_as_float(v.x), factor, rsum);
-      }
-      st_shared_v2_volatile(sums + 8u * ((g & 3u) * kH + h), __float_as_uint(lrow), g);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_P_FULL0 + (g & 1u)));
+      if (lane == 0) mbar_arrive(BAR(B_P_FULL));
 
       if (cf.last()) {
         // ---- epilogue of this segment: wait for its last P·V, normalise, store
@@ -858,7 +816,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
           break;
         }
         tc_fence_after();
-        const float lt = lrow;
+        const float lt = __uint_as_float(tmem_ld1_sync(tl + kColSum));
         const float inv = 1.f / lt;
         if (slot < 0) {
           uint4* dst = reinterpret_cast<uint4*>(a.o_lat + ((size_t)row * kH + h) * kDC + rank * 256);

@@ -15,21 +15,13 @@ loads, MMA completions, copies landing in the peer CTA), over random segment
 layouts.  It checks:
   * no deadlock (some role or completion can always make progress);
   * every parity wait passes only when its own phase has completed;
-  * the two TMEM score buffers: QK^T of tile t writes buffer t mod 2 only
-    once P·V of tile t-2 (whose P sits there) is complete; the softmax reads
-    scores QK^T completed and writes P over them; P·V reads that P;
-  * O is rescaled only while no P·V into it is in flight;
   * no exchange buffer region is overwritten while it holds unconsumed
     scores or while a copy out of it is still reading it;
-  * no reference-max or row-sum slot is overwritten before its reader has
-    read it.
-Negative controls re-introduce, one at a time, a single shared score
-barrier, a single shared P barrier, QK^T that does not wait for P·V two
-tiles back, a rescale that does not wait for the previous P·V, two hand-off
-slots instead of four, and a staging offset of one or three buffers; each
-must be caught.  The model is test
-infrastructure for the kernel's control flow only: it computes none of the
-attention arithmetic.
+  * no reference-max slot is overwritten before its reader has read it.
+Negative controls re-introduce, one at a time, a single shared score barrier,
+two hand-off slots instead of four, and a staging offset of one or three
+buffers; each must be caught.  The model is test infrastructure for the
+kernel's control flow only: it computes none of the attention arithmetic.
 """
 import random
 
@@ -75,16 +67,13 @@ class Barrier:
 
 
 def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv_no_barrier=False,
-              conv_skips_f8_full=False, abort_at=None, drain=True, shared_p_full=False, qk_no_s_wait=False,
-              rescale_no_wait=False, rescale_rate=0.3):
+              conv_skips_f8_full=False, abort_at=None, drain=True):
     """fp8: the FP8 layout — the producer's TMA fills stage t mod STAGES with
     codes, the converter warps read all of their codes, meet at a barrier and
     write the bf16 rows over them, and QK^T waits for all converter warps.
     Planted mistakes: converters without the barrier (a warp overwrites codes
     another warp has not read yet) and converters that do not wait for the
     codes to land.
-    rescale_rate: the chance that a tile moves the reference max (the kernel
-    then rescales O, which needs P·V of the previous tile complete).
     abort_at: (cta, step) — that CTA's abort flag goes up after `step` model
     steps (a wait that timed out); every role then leaves at its next wait.
     After the roles, each CTA tells the peer how many score copies each warp
@@ -110,15 +99,12 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             stage=[None] * n_stages,        # (tile, "codes" | "bf16") held by a stage
             codes_read=[set() for _ in range(n_stages)],   # converter warps that have read this tile's codes
             conv=Barrier(WARPS),            # converters' mbarrier: phase t = every warp holds tile t's codes
-            s_full=[Barrier(1), Barrier(1)], p_full=[Barrier(WG_THREADS), Barrier(WG_THREADS)],
+            s_full=[Barrier(1), Barrier(1)], s_free=Barrier(WG_THREADS), p_full=Barrier(WG_THREADS),
             o_done=[Barrier(1), Barrier(1)], q_ready=Barrier(WG_THREADS), o_free=Barrier(WG_THREADS),
-            sbuf=[[None] * WARPS for _ in range(2)],   # TMEM score/P buffer state per (buffer, row block)
-            o_inflight=set(),                          # tiles whose P·V into O has been issued, not completed
             x_full=[Barrier(1) for _ in range(XBUFS)],
             xbuf=[[None] * WARPS for _ in range(XBUFS)],   # region state per (buffer, row block)
             reading=[[False] * WARPS for _ in range(XBUFS)],  # a copy out of this region is in flight
             slot=[[None] * WARPS for _ in range(slots)], slot_unread=[[False] * WARPS for _ in range(slots)],
-            lslot=[[None] * WARPS for _ in range(slots)], lslot_unread=[[False] * WARPS for _ in range(slots)],
             abort=False, pushes=[0] * (2 * WARPS), peer_pushes=None, peer_abort=None,
             armed=[-1] * XBUFS, exited=False,
         ))
@@ -144,9 +130,6 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
 
     def o_done_bar(c, t):
         return (c["o_done"][0], t) if shared_s_full else (c["o_done"][t & 1], t >> 1)
-
-    def p_full_bar(c, t):
-        return (c["p_full"][0], t) if shared_p_full else (c["p_full"][t & 1], t >> 1)
 
     def producer(ci):
         c = ctas[ci]
@@ -189,25 +172,19 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
                     return
                 if c["stage"][t % n_stages] != (t, "bf16"):
                     raise ProtocolError(f"QK^T of tile {t} reads a stage holding {c['stage'][t % n_stages]}")
-            if t >= 2 and not qk_no_s_wait:
-                bar, k = o_done_bar(c, t - 2)   # P·V of tile t-2 has read the P in buffer t mod 2
-                if not (yield from wait(c, lambda: bar.test(k))):
+            if t > 0:
+                if not (yield from wait(c, lambda: c["s_free"].test(t - 1))):
                     return
             seg, first, _ = tiles[t]
             if first:
                 if not (yield from wait(c, lambda: c["q_ready"].test(seg))):
                     return
-            for w in range(WARPS):
-                if c["sbuf"][t & 1][w] is not None:
-                    raise ProtocolError(f"QK^T of tile {t} writes score buffer {t & 1} holding {c['sbuf'][t & 1][w]}")
-                c["sbuf"][t & 1][w] = ("writing", t)
             events.append(("s", ci, t))
 
     def pv(ci):
         c = ctas[ci]
         for t in range(G):
-            bar, k = p_full_bar(c, t)
-            if not (yield from wait(c, lambda: bar.test(k))):
+            if not (yield from wait(c, lambda: c["p_full"].test(t))):
                 return
             seg, first, _ = tiles[t]
             if first:
@@ -215,11 +192,6 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
                     return
             if fp8 and c["stage"][t % n_stages] != (t, "bf16"):
                 raise ProtocolError(f"P·V of tile {t} reads a stage holding {c['stage'][t % n_stages]}")
-            for w in range(WARPS):
-                if c["sbuf"][t & 1][w] != ("p", t):
-                    raise ProtocolError(f"P·V of tile {t} reads buffer {t & 1} holding {c['sbuf'][t & 1][w]}")
-                c["sbuf"][t & 1][w] = ("pv", t)
-            c["o_inflight"].add(t)
             events.append(("o", ci, t))
 
     def softmax_warp(ci, wg, w):
@@ -236,9 +208,7 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             bar, k = s_full_bar(c, t)
             if not (yield from wait(c, lambda: bar.test(k))):
                 return
-            if c["sbuf"][t & 1][w] != ("s", t):
-                raise ProtocolError(f"softmax of tile {t} reads buffer {t & 1} holding {c['sbuf'][t & 1][w]}")
-            c["sbuf"][t & 1][w] = ("read", t)
+            c["s_free"].arrive(per_warp)
             # stage this row block's scores and push them to the peer
             sb = (t + xlead) % XBUFS
             state = c["xbuf"][sb][w]
@@ -275,33 +245,11 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             c["slot"][sl][w] = t
             c["slot_unread"][sl][w] = t + 1 < G and not tiles[t + 1][1]
             yield
-            if not first and rnd.random() < rescale_rate:
-                # the reference max moved: O is rescaled, after P·V of tile t-1
-                if not rescale_no_wait:
-                    bar, k = o_done_bar(c, t - 1)
-                    if not (yield from wait(c, lambda: bar.test(k))):
-                        return
-                if c["o_inflight"]:
-                    raise ProtocolError(f"tile {t} rescales O with P·V of tiles {sorted(c['o_inflight'])} in flight")
-                yield
-            # P over the scores it came from
-            if c["sbuf"][t & 1][w] != ("read", t):
-                raise ProtocolError(f"P of tile {t} written over buffer {t & 1} holding {c['sbuf'][t & 1][w]}")
-            c["sbuf"][t & 1][w] = ("p", t)
-
-            # row sum from tile t-1, then this tile's
-            if not first:
-                sl = (t - 1) % slots
-                if not (yield from wait(c, lambda: c["lslot"][sl][w] == t - 1)):
+            if t > 0:
+                bar, k = o_done_bar(c, t - 1)
+                if not (yield from wait(c, lambda: bar.test(k))):
                     return
-                c["lslot_unread"][sl][w] = False
-            sl = t % slots
-            if c["lslot_unread"][sl][w]:
-                raise ProtocolError(f"tile {t} overwrites tile {c['lslot'][sl][w]}'s row sum before it was read")
-            c["lslot"][sl][w] = t
-            c["lslot_unread"][sl][w] = t + 1 < G and not tiles[t + 1][1]
-            bar, k = p_full_bar(c, t)
-            bar.arrive(per_warp)
+            c["p_full"].arrive(per_warp)
             if last:
                 bar, k = o_done_bar(c, t)
                 if not (yield from wait(c, lambda: bar.test(k))):
@@ -380,17 +328,12 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
                 c["stage"][st] = (t, "codes")
                 c["f8_full"][st].arrive()
             elif kind == "s":
-                for w in range(WARPS):
-                    c["sbuf"][t & 1][w] = ("s", t)
                 bar, _ = s_full_bar(c, t)
                 bar.arrive()
             elif kind == "o":
                 if fp8:
                     c["stage"][t % n_stages] = (t, "free")
                 c["kv_empty"][t % n_stages].arrive()
-                for w in range(WARPS):
-                    c["sbuf"][t & 1][w] = None
-                c["o_inflight"].discard(t)
                 bar, _ = o_done_bar(c, t)
                 bar.arrive()
             else:  # a row block's copy lands in the peer's buffer t mod XBUFS
@@ -441,8 +384,7 @@ def test_protocol_holds_on_single_tile_segments():
         run_model([1, 1, 1, 1, 2, 2, 3, 3, 11], seed)
 
 
-@pytest.mark.parametrize("mistake", [dict(shared_s_full=True), dict(shared_p_full=True), dict(qk_no_s_wait=True),
-                                     dict(rescale_no_wait=True), dict(slots=2), dict(xlead=1), dict(xlead=3)])
+@pytest.mark.parametrize("mistake", [dict(shared_s_full=True), dict(slots=2), dict(xlead=1), dict(xlead=3)])
 def test_planted_protocol_mistakes_are_caught(mistake):
     caught = 0
     for i, segs in enumerate(_layouts(60, 12)):
