@@ -4,11 +4,14 @@
 //   K_c[h, t, :] = c[t, :]·W_UK[h]^T,   V_c[h, t, :] = c[t, :]·W_UV[h]
 // (head-major outputs, one head's rows contiguous for the attention's loads).
 //
-// One CTA = one head and 256 tokens: four 128 x 128 fp32 accumulators in
-// TMEM (K and V for each 128-token half, all 512 columns).  Each 64-wide
-// K-chunk of the latent is loaded once for both outputs and both W tiles
-// once for both token halves, so a CTA moves 512 KB for 67 MFLOP.  Warp 0
-// lane 0 issues TMA, warp 1 lane 0 the MMAs; all four warps run the
+// One CTA = one head and 128 tokens: two 128 x 128 fp32 accumulators in
+// TMEM (K and V, 256 columns), so two CTAs share an SM and one's epilogue
+// runs while the other's MMAs do (with one CTA of 256 tokens per SM, all 512
+// columns in use, the epilogue stalled the tensor pipe: 520 against 470 us
+// on the chunked-prefill expansion).  Each 64-wide K-chunk of the latent is
+// loaded once for both outputs, so a CTA moves 384 KB for 34 MFLOP, the two
+// W tiles coming from L2 for all but the first token block of a head.  Warp
+// 0 lane 0 issues TMA, warp 1 lane 0 the MMAs; all four warps run the
 // epilogue (thread = token row = TMEM lane), which rounds each accumulator
 // to bf16 into the drained ring as two 128-token x 64-column boxes in the
 // TMA's 128-byte-swizzled layout and writes each with one TMA store.
@@ -25,24 +28,27 @@ namespace expand {
 
 using namespace mla::dev;
 
-constexpr int kM = 256, kKCh = 512 / 64;
+constexpr int kHalves = 1;                      // 128-token blocks per CTA
+constexpr int kM = 128 * kHalves, kKCh = 512 / 64;
 constexpr int kTile = 128 * 64 * 2;              // 16 KB: 128 rows x 64, 128-byte swizzle
-constexpr int kStage = 4 * kTile;                // A rows 0-127 | A rows 128-255 | W_UK chunk | W_UV chunk
-constexpr int kStages = 3;
+constexpr int kStage = (kHalves + 2) * kTile;    // A rows of each half | W_UK chunk | W_UV chunk
+constexpr int kStages = 2;
+constexpr int kCtasPerSm = 2;
+constexpr int kTmemCols = 256 * kHalves;         // K and V of each half
 constexpr int kOffBar = kStages * kStage;
 constexpr int kOffMisc = kOffBar + 8 * (2 * kStages + 1);
 constexpr int kSmem = kOffMisc + 16 + 1024;
-static_assert(kSmem <= 232448, "shared memory layout does not fit");
+static_assert(kCtasPerSm * kSmem <= 232448 && kCtasPerSm * kTmemCols <= 512, "the CTAs of an SM do not fit");
 constexpr uint32_t kIdescK = idesc_bf16_f32(128, 128, false, false);  // W_UK read K-major
 constexpr uint32_t kIdescV = idesc_bf16_f32(128, 128, false, true);   // W_UV read MN-major
 
 constexpr int kBoxBytes = 128 * 64 * 2;         // one [128 tokens x 64] bf16 output box
-static_assert(8 * kBoxBytes <= kStages * kStage, "the output boxes are staged in the drained ring");
+static_assert(4 * kHalves * kBoxBytes <= kStages * kStage, "the output boxes are staged in the drained ring");
 
 // a_map: latent rows {512, 1, n} (box 64 x 1 x 128); k_map: W_UK {512, 128, 128 heads}
 // (box 64 x 128 x 1); v_map: W_UV {128, 512, 128 heads} (box 64 x 64 x 1);
 // kc_map / vc_map: K_c and V_c {128, n, 128 heads} (box 64 x 128 x 1, stores).
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(128, kCtasPerSm)
     expand_kv_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap k_map,
                      const __grid_constant__ CUtensorMap v_map, const __grid_constant__ CUtensorMap kc_map,
                      const __grid_constant__ CUtensorMap vc_map, int32_t* err) {
@@ -70,7 +76,7 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (warp == 1) {
     __syncwarp();
-    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -92,11 +98,11 @@ __global__ void __launch_bounds__(128, 1)
         const uint32_t dst = base + st * kStage;
         const uint32_t fb = full0 + 8 * st;
         mbar_arrive_expect_tx(fb, (uint32_t)kStage);
-        tma_load_3d(dst, &a_map, kc * 64, 0, m0, fb);
-        tma_load_3d(dst + kTile, &a_map, kc * 64, 0, m0 + 128, fb);
-        tma_load_3d(dst + 2 * kTile, &k_map, kc * 64, 0, h, fb);
-        tma_load_3d(dst + 3 * kTile, &v_map, 0, kc * 64, h, fb);
-        tma_load_3d(dst + 3 * kTile + 8192, &v_map, 64, kc * 64, h, fb);
+#pragma unroll
+        for (int hf = 0; hf < kHalves; ++hf) tma_load_3d(dst + hf * kTile, &a_map, kc * 64, 0, m0 + 128 * hf, fb);
+        tma_load_3d(dst + kHalves * kTile, &k_map, kc * 64, 0, h, fb);
+        tma_load_3d(dst + (kHalves + 1) * kTile, &v_map, 0, kc * 64, h, fb);
+        tma_load_3d(dst + (kHalves + 1) * kTile + 8192, &v_map, 64, kc * 64, h, fb);
         ++issued;
       }
       for (int k = (issued > kStages ? issued - kStages : 0); k < issued; ++k)
@@ -117,14 +123,14 @@ __global__ void __launch_bounds__(128, 1)
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk) {
           const uint32_t acc = (kc | kk) ? 1u : 0u;
-          const uint64_t a0 = sdesc_sw128(sa + kk * 32, 16, 1024);
-          const uint64_t a1 = sdesc_sw128(sa + kTile + kk * 32, 16, 1024);
-          const uint64_t bk = sdesc_sw128(sa + 2 * kTile + kk * 32, 16, 1024);
-          const uint64_t bv = sdesc_sw128(sa + 3 * kTile + kk * 2048, 8192, 1024);
-          mma_ss(tmem + 0, a0, bk, kIdescK, acc);
-          mma_ss(tmem + 128, a0, bv, kIdescV, acc);
-          mma_ss(tmem + 256, a1, bk, kIdescK, acc);
-          mma_ss(tmem + 384, a1, bv, kIdescV, acc);
+          const uint64_t bk = sdesc_sw128(sa + kHalves * kTile + kk * 32, 16, 1024);
+          const uint64_t bv = sdesc_sw128(sa + (kHalves + 1) * kTile + kk * 2048, 8192, 1024);
+#pragma unroll
+          for (int hf = 0; hf < kHalves; ++hf) {
+            const uint64_t a = sdesc_sw128(sa + hf * kTile + kk * 32, 16, 1024);
+            mma_ss(tmem + 256 * hf, a, bk, kIdescK, acc);
+            mma_ss(tmem + 256 * hf + 128, a, bv, kIdescV, acc);
+          }
         }
         tc_commit(empty0 + 8 * st);
       }
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(128, 1)
     const uint32_t r = (uint32_t)(warp * 32 + lane);
     const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
 #pragma unroll 1
-    for (int q = 0; q < 4; ++q) {              // K rows 0-127, V rows 0-127, K rows 128-255, V rows 128-255
+    for (int q = 0; q < 2 * kHalves; ++q) {    // K rows 0-127, V rows 0-127, K rows 128-255, V rows 128-255
 #pragma unroll
       for (int b = 0; b < 2; ++b) {
         const uint32_t box = base + (q * 2 + b) * kBoxBytes;
@@ -172,7 +178,7 @@ __global__ void __launch_bounds__(128, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, 512);
+    tmem_dealloc(tmem, kTmemCols);
   }
 }
 
