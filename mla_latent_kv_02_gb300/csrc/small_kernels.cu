@@ -28,14 +28,25 @@ __global__ void __launch_bounds__(kWarps * 32)
                      int32_t* err) {
   const int lane = threadIdx.x & 31;
   for (int64_t i = (int64_t)blockIdx.x * kWarps + (threadIdx.x >> 5); i < n; i += (int64_t)gridDim.x * kWarps) {
+    // the row's 72 16-byte pieces (up to three per lane) and its slot are
+    // requested together: one memory round trip before the stores
+    uint4 v[3];
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int k = lane + 32 * j;
+      if (k < kRowVec) v[j] = k < kLatVec ? __ldg(c_new + i * kLatVec + k) : __ldg(k_new + i * kRopeVec + (k - kLatVec));
+    }
     const int64_t slot = __ldg(slots + i);
     if (slot < 0 || slot >= num_slots) {
       if (lane == 0) atomicOr(err, (int32_t)MLA_DEVERR_SLOT_OOB);
       continue;
     }
     uint4* dst = cache + slot * kRowVec;
-    for (int k = lane; k < kRowVec; k += 32)
-      dst[k] = k < kLatVec ? __ldg(c_new + i * kLatVec + k) : __ldg(k_new + i * kRopeVec + (k - kLatVec));
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+      const int k = lane + 32 * j;
+      if (k < kRowVec) dst[k] = v[j];
+    }
   }
 }
 
