@@ -589,6 +589,19 @@ def run_mla(args):
     dec_avg = sum(dec_ms) / len(dec_ms)
     if api.mla_check(dev_err) != 0:
         raise RuntimeError("device error word set during the timed steps")
+    # the step's other kernels, each timed alone after the timed region on
+    # the same inputs (launched back to back, warm as inside the step)
+    step_kernels = {
+        "a1_kv_append_us": round(_time_launches(torch, stream, lambda i: api.mla_kv_append(c_new, k_new, slots_new, kv,
+                                                                                           dev_err), reps=20), 2),
+        "a2_absorb_q_us": round(_time_launches(torch, stream, lambda i: api.mla_absorb_q(q_c, w_uk, q_abs, dev_err),
+                                               reps=20), 2),
+        "a3_a4_decode_us": round(dec_avg * 1e3, 2),
+        "a5_up_v_us": round(_time_launches(torch, stream, lambda i: api.mla_up_v(o_lat, w_uv, out, dev_err), reps=20), 2),
+    }
+    step_kernels["outside_decode_us"] = round(ms_total / K * 1e3 - dec_avg * 1e3, 2)
+    if api.mla_check(dev_err) != 0:
+        raise RuntimeError("device error word set while timing the step's kernels")
 
     # ---- end to end through the API: pinned host inputs in, result out, plan rebuilt each step.
     # Two steps in flight, as a serving loop runs: the host plans and enqueues
@@ -706,6 +719,7 @@ def run_mla(args):
         },
         "kv_tb_per_s": round(st["kv_bytes"] / dec_s / 1e12, 4),
         "decode_us": round(dec_avg * 1e3, 2),
+        "step_kernels": step_kernels,
         "roofline": {
             "kernel": "mla_decode_paged (decode + combine launches)",
             "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
