@@ -169,141 +169,6 @@ __global__ void __launch_bounds__(128, 2)
   }
 }
 
-// A2 with the epilogue pipelined behind the loads.  K = 128 is two 64-wide
-// chunks, so a CTA's whole input (the activation tile, 32 KB, and its 256
-// weight columns as four 64-column blocks of 16 KB) fits in shared memory
-// and is requested at once.  Block j's MMAs (N = 64, into TMEM columns
-// 64j..) start as soon as block j has landed, and its epilogue as soon as
-// they complete: the bf16 box is staged over block j's own weights (no
-// longer read) and stored while later blocks are still loading.
-constexpr int kAqBlocks = 4;                          // 64-column blocks per CTA
-constexpr int kAqA = 2 * 128 * 64 * 2;                // activation tile: 2 K-chunks x [128 x 64]
-constexpr int kAqW = 2 * 64 * 64 * 2;                 // weight block: 2 K-chunks x [64 x 64]
-constexpr int kAqOffBar = kAqA + kAqBlocks * kAqW;    // 96 KB
-constexpr int kAqSmem = kAqOffBar + 8 * (2 + 2 * kAqBlocks) + 16 + 1024;
-static_assert(2 * kAqSmem <= 232448, "two A2 CTAs per SM");
-
-__global__ void __launch_bounds__(128, 2)
-    absorb_q_kernel(const __grid_constant__ CUtensorMap a_map, const __grid_constant__ CUtensorMap w_map,
-                    const __grid_constant__ CUtensorMap c_map, int32_t* err) {
-  constexpr uint32_t kIdesc = idesc_bf16_f32(128, 64, false, true);
-  extern __shared__ uint8_t smem_raw[];
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bars = base + kAqOffBar;
-  // a_full, w_full[j], d_full[j] (block j's MMAs complete), drain
-  const uint32_t a_full = bars, w_full0 = bars + 8, d_full0 = bars + 8 * (1 + kAqBlocks),
-                 drain = bars + 8 * (1 + 2 * kAqBlocks);
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(gbase + kAqOffBar + 8 * (2 + 2 * kAqBlocks));
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gbase + kAqOffBar + 8 * (2 + 2 * kAqBlocks) + 8);
-
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y;
-  const int m0 = blockIdx.x * 128;
-  const int n0 = blockIdx.z * (kAqBlocks * 64);
-
-  if (threadIdx.x == 0) {
-    *abort_flag = 0;
-    mbar_init(a_full, 1);
-    for (int j = 0; j < kAqBlocks; ++j) {
-      mbar_init(w_full0 + 8 * j, 1);
-      mbar_init(d_full0 + 8 * j, 1);
-    }
-    mbar_init(drain, 1);
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    __syncwarp();
-    tmem_alloc(smem_u32(tmem_slot), kAqBlocks * 64);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-
-  if (warp == 0) {
-    if (lane == 0) {
-      prefetch_tmap(&a_map);
-      prefetch_tmap(&w_map);
-      prefetch_tmap(&c_map);
-      mbar_arrive_expect_tx(a_full, (uint32_t)kAqA);
-#pragma unroll
-      for (int kc = 0; kc < 2; ++kc) tma_load_3d(base + kc * 16384, &a_map, kc * 64, h, m0, a_full);
-#pragma unroll
-      for (int j = 0; j < kAqBlocks; ++j) {
-        const uint32_t wb = base + kAqA + j * kAqW;
-        mbar_arrive_expect_tx(w_full0 + 8 * j, (uint32_t)kAqW);
-#pragma unroll
-        for (int kc = 0; kc < 2; ++kc) tma_load_3d(wb + kc * 8192, &w_map, n0 + j * 64, kc * 64, h, w_full0 + 8 * j);
-      }
-      // every load lands before the CTA may exit
-      wait_phase_drain(a_full, 0);
-      for (int j = 0; j < kAqBlocks; ++j) wait_phase_drain(w_full0 + 8 * j, 0);
-    }
-    __syncwarp();
-  } else if (warp == 1) {
-    if (lane == 0) {
-      bool ok = wait_phase(a_full, 0, err, abort_flag);
-      for (int j = 0; j < kAqBlocks && ok; ++j) {
-        if (!wait_phase(w_full0 + 8 * j, 0, err, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t wb = base + kAqA + j * kAqW;
-#pragma unroll
-        for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + j * 64, sdesc_sw128(base + kc * 16384 + kk * 32, 16, 1024),
-                   sdesc_sw128(wb + kc * 8192 + kk * 2048, 8192, 1024), kIdesc, (kc | kk) ? 1u : 0u);
-        tc_commit(d_full0 + 8 * j);
-      }
-      // every MMA of this thread completes before TMEM is released
-      tc_commit(drain);
-      wait_phase_drain(drain, 0);
-    }
-    __syncwarp();
-  }
-
-  // Epilogue: thread = tile row (TMEM lane), all four warps, block by block.
-  // The decision to store a box is the whole CTA's, since it holds every
-  // warp's rows; after a failed wait no further box is stored.
-  const uint32_t r = (uint32_t)(warp * 32 + lane);
-  const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
-#pragma unroll 1
-  for (int j = 0; j < kAqBlocks; ++j) {
-    bool w = wait_phase(d_full0 + 8 * j, 0, err, abort_flag) && !*abort_flag;
-    w = __syncthreads_and(w) != 0;
-    if (!w) break;
-    tc_fence_after();
-    // block j's MMAs are complete: its weights are no longer read
-    const uint32_t box = base + kAqA + j * kAqW;
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-      uint32_t v[32];
-      tmem_ld32_sync(tl + j * 64 + hf * 32, v);
-      stage_row_bf16_sw128(box, r, hf, v);
-    }
-    fence_proxy_async_smem();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      tma_store_3d(&c_map, box, n0 + j * 64, h, m0);
-      bulk_commit_group();
-    }
-  }
-  if (threadIdx.x == 0) bulk_wait_all_read();  // the staged boxes are released at exit
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, kAqBlocks * 64);
-  }
-}
-
 template <int N, int K, int STAGES, int NSPLIT>
 cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, const CUtensorMap& c_map, int32_t T,
                 int32_t* err, cudaStream_t stream) {
@@ -320,14 +185,7 @@ cudaError_t run(const CUtensorMap& a_map, const CUtensorMap& w_map, const CUtens
 
 cudaError_t launch_head_gemm(HeadGemm kind, const CUtensorMap& a_map, const CUtensorMap& w_map,
                              const CUtensorMap& c_map, int32_t T, int32_t* err, cudaStream_t stream) {
-  if (kind == HeadGemm::kAbsorbQ) {
-    cudaError_t e = cudaFuncSetAttribute(gemm::absorb_q_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         gemm::kAqSmem);
-    if (e != cudaSuccess) return e;
-    dim3 grid((T + 127) / 128, 128, 512 / (gemm::kAqBlocks * 64));
-    gemm::absorb_q_kernel<<<grid, 128, gemm::kAqSmem, stream>>>(a_map, w_map, c_map, err);
-    return cudaGetLastError();
-  }
+  if (kind == HeadGemm::kAbsorbQ) return gemm::run<512, 128, 2, 2>(a_map, w_map, c_map, T, err, stream);
   return gemm::run<128, 512, 4, 1>(a_map, w_map, c_map, T, err, stream);
 }
 
