@@ -641,10 +641,11 @@ def run_mla(args):
             dc_new.copy_(h_c_new, non_blocking=True)
             dk_new.copy_(h_k_new, non_blocking=True)
             dslots.copy_(h_slots, non_blocking=True)
+            # the plan is rebuilt every step into its slot's pinned buffer
+            # (that slot's previous step has finished: its result was
+            # collected) and uploaded with the inputs, off the compute stream
+            p = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, into=e2e_plans[sl], stream=in_stream)
             ev_in[sl].record(in_stream)
-        # the plan is rebuilt every step into its slot's pinned buffer: that
-        # slot's previous step has finished (its result was collected)
-        p = api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, into=e2e_plans[sl])
         stream.wait_event(ev_in[sl])
         api.mla_kv_append(dc_new, dk_new, dslots, kv, dev_err)
         api.mla_absorb_q(dq_c, w_uk, q_abs, dev_err)
