@@ -47,26 +47,26 @@ constexpr int kQBytes = 3 * kChunkBytes;           // q_c (2 chunks) | q_r (1 ch
 constexpr int kKBytes = 3 * kChunkBytes;           // K_c (2 chunks) | k_R (1 chunk)
 constexpr int kVBytes = 2 * kChunkBytes;           // V_c (2 chunks of 64 columns)
 constexpr int kStages = 2;                         // depth of the K ring and of the V ring
-constexpr int kOnesBytes = 16 * 64 * 2;            // [16 x 64] bf16 ones
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kStages * kKBytes;
 constexpr int kOffOnes = kOffV + kStages * kVBytes;
-constexpr int kAlignedBytes = kOffOnes + kOnesBytes;
+constexpr int kAlignedBytes = kOffOnes;
 constexpr int kNumBars = 24;
 constexpr int kOffXMax = 8 * kNumBars + 64;         // float [2 tile parities][2 halves][128 rows]
-constexpr int kSmallBytes = kOffXMax + 2 * 2 * 128 * 4;
+constexpr int kOffXSum = kOffXMax + 2 * 2 * 128 * 4; // float [2 halves][128 rows]: the halves' row sums
+constexpr int kSmallBytes = kOffXSum + 2 * 128 * 4;
 constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 
-constexpr uint32_t kColO = 0, kColS = 128, kColP = 384, kColSum = 448, kTmemCols = 512;
+// TMEM: O, two score buffers, two P buffers (tile j's in buffer j mod 2)
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 384, kTmemCols = 512;
 constexpr int kSoftWarp0 = 2;
 constexpr int kSoftWarps = 8;                      // two warps per TMEM lane quarter, 64 key columns each
 constexpr int kPvWarp = kSoftWarp0 + kSoftWarps;
 constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
 constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
-constexpr uint32_t kIdescSum = idesc_bf16_f32(128, 16, false, false);
 
 enum : int {
   B_Q_FULL = 0,
@@ -76,12 +76,13 @@ enum : int {
   B_V_EMPTY = B_V_FULL + kStages,
   B_S_FULL = B_V_EMPTY + kStages,   // 2 (one per S buffer)
   B_S_FREE = B_S_FULL + 2,          // 2, one arrival per softmax warp
-  B_P_FULL = B_S_FREE + 2,          // one arrival per softmax warp
-  B_O_DONE,
-  B_DRAIN,
+  B_P_FULL = B_S_FREE + 2,          // 2 (P buffer), one arrival per softmax warp
+  B_O_DONE = B_P_FULL + 2,          // 2 (tile parity): P·V of tile j complete
+  B_DRAIN = B_O_DONE + 2,
   B_DRAIN_PV,
   B_XMAX,                           // 2 (tile parity), one arrival per softmax warp
-  B_COUNT = B_XMAX + 2
+  B_XSUM = B_XMAX + 2,              // the halves' row sums, one arrival per softmax warp
+  B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier area too small");
 
@@ -129,17 +130,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(BAR(B_S_FREE + i), kSoftWarps);
     }
     mbar_init(BAR(B_P_FULL), kSoftWarps);
+    mbar_init(BAR(B_P_FULL + 1), kSoftWarps);
     mbar_init(BAR(B_O_DONE), 1);
+    mbar_init(BAR(B_O_DONE + 1), 1);
+    mbar_init(BAR(B_XSUM), kSoftWarps);
     mbar_init(BAR(B_DRAIN), 1);
     mbar_init(BAR(B_DRAIN_PV), 1);
     mbar_init(BAR(B_XMAX), kSoftWarps);
     mbar_init(BAR(B_XMAX + 1), kSoftWarps);
     fence_mbar_init();
-  }
-  {
-    uint32_t* ones = reinterpret_cast<uint32_t*>(smem_raw + (base - raw) + kOffOnes);
-    for (int i = threadIdx.x; i < kOnesBytes / 4; i += kThreads) ones[i] = 0x3F803F80u;  // bf16 1.0 pairs
-    fence_proxy_async_smem();
   }
   if (warp == 1) {
     __syncwarp();
@@ -240,14 +239,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == kPvWarp) {
     // ---------------------------------------------------------------- P·V issue
-    // O += P(j)·V(j) and l += P(j)·1 once the softmax has written P(j) and V(j)
-    // has landed.
+    // O += P(j)·V(j) once the softmax has written P(j) (buffer j mod 2) and
+    // V(j) has landed.
     if (lane == 0) {
       const uint64_t vdesc0 = sdesc_sw128(base + kOffV, (uint32_t)kChunkBytes, 1024);
-      const uint64_t odesc = sdesc_sw128(base + kOffOnes, 16, 1024);
       bool ok = true;
       for (int t = 0; ok && t < n_tiles; ++t) {
-        ok = wait_phase<false, false>(BAR(B_P_FULL), t & 1, err, abort_flag) &&
+        ok = wait_phase<false, false>(BAR(B_P_FULL + (t & 1)), (t >> 1) & 1, err, abort_flag) &&
              wait_phase<false, false>(BAR(B_V_FULL + t % kStages), (t / kStages) & 1, err, abort_flag);
         if (!ok) break;
         tc_fence_after();
@@ -255,11 +253,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t acc = (t == 0 && kk == 0) ? 0u : 1u;
-          mma_ts(tmem + kColO, tmem + kColP + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, acc);
-          mma_ts(tmem + kColSum, tmem + kColP + kk * 8, odesc + (uint64_t)(((kk & 3) * 32) >> 4), kIdescSum, acc);
+          mma_ts(tmem + kColO, tmem + kColP + (t & 1) * 64 + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, acc);
         }
         tc_commit(BAR(B_V_EMPTY + t % kStages));
-        tc_commit(BAR(B_O_DONE));
+        tc_commit(BAR(B_O_DONE + (t & 1)));
       }
       tc_commit(BAR(B_DRAIN_PV));
       wait_phase_drain(BAR(B_DRAIN_PV), 0);
@@ -278,6 +275,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float rescale_thr = 8.f / c2;            // lazy rescale: 8 in log2 units
     const __half2 c2h = __float2half2_rn(c2);
     float m = -INFINITY;
+    float l = 0.f;                                 // this half's row sum of P, at the reference max m
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       const int sb = j & 1;
@@ -336,14 +334,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         resc = true;
       }
       const __half2 mc2 = __float2half2_rn(-m * c2);
+      float rs0 = 0.f, rs1 = 0.f;                  // row sum of the bf16 P the tensor core accumulates
 #pragma unroll
       for (int k = 0; k < 32; ++k) {
         const float2 p = __half22float2(as_h2(ex2_f16x2(as_u32(__hfma2(as_h2(own[k]), c2h, mc2)))));
         own[k] = pack_bf16x2(p.x, p.y);
+        rs0 += __uint_as_float(own[k] << 16);
+        rs1 += __uint_as_float(own[k] & 0xFFFF0000u);
       }
-      // the P buffer and a rescale of O both need P·V(j-1) done
-      if (j > 0) {
-        w = wait_phase<false, true>(BAR(B_O_DONE), (j - 1) & 1, err, abort_flag);
+      l = fmaf(l, factor, rs0 + rs1);
+      // P buffer j mod 2 was last read by P·V(j-2); waited first, it also keeps
+      // a rescale's wait for P·V(j-1) below within one phase of its barrier
+      if (j >= 2) {
+        w = wait_phase<false, true>(BAR(B_O_DONE + (j & 1)), ((j >> 1) - 1) & 1, err, abort_flag);
         if (!__all_sync(0xffffffffu, w)) {
           ok = false;
           break;
@@ -351,7 +354,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
       }
       if (__any_sync(0xffffffffu, resc)) {
-        // each half rescales its 64 output columns; half 0 also the row sum
+        // a rescale of O needs P·V(j-1) done (P·V(j) waits for this tile's P)
+        w = wait_phase<false, true>(BAR(B_O_DONE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, err, abort_flag);
+        if (!__all_sync(0xffffffffu, w)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // each half rescales its 64 output columns
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
           uint32_t o[32];
@@ -360,21 +370,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * factor);
           tmem_st32(tl + kColO + c, o);
         }
-        if (half == 0)
-          tmem_st1(tl + kColSum, __float_as_uint(__uint_as_float(tmem_ld1_sync(tl + kColSum)) * factor));
       }
-      tmem_st32(tl + kColP + 32 * half, own);
+      tmem_st32(tl + kColP + (j & 1) * 64 + 32 * half, own);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_P_FULL));
+      if (lane == 0) mbar_arrive(BAR(B_P_FULL + (j & 1)));
     }
-    // ---- epilogue: out[i, h, 64 half : 64 half + 64] = O / l
+    // ---- epilogue: out[i, h, 64 half : 64 half + 64] = O / l, l the sum of
+    //      the two halves' row sums (swapped through shared memory)
     if (ok && n_tiles > 0) {
-      bool w = wait_phase<false, true>(BAR(B_O_DONE), (n_tiles - 1) & 1, err, abort_flag);
+      float* xsum = reinterpret_cast<float*>(smem_raw + kOffXSum);
+      xsum[half * 128 + r] = l;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(B_XSUM));
+      const int nl = n_tiles - 1;
+      bool w = wait_phase<false, true>(BAR(B_XSUM), 0, err, abort_flag) &&
+               wait_phase<false, true>(BAR(B_O_DONE + (nl & 1)), (nl >> 1) & 1, err, abort_flag);
       if (__all_sync(0xffffffffu, w)) {
         tc_fence_after();
-        const float inv = 1.f / __uint_as_float(tmem_ld1_sync(tl + kColSum));
+        const float inv = 1.f / (xsum[r] + xsum[128 + r]);
         uint4* dst = reinterpret_cast<uint4*>(a.out + ((size_t)(sq.q_off + min(i, M - 1)) * 128 + h) * 128);
 #pragma unroll 1
         for (int c = 64 * half; c < 64 * half + 64; c += 32) {
