@@ -17,9 +17,12 @@
 // head-major, so a head's tile is 32 contiguous KB.  tcgen05:
 //   S(j) = Q·K(j)^T   M = 128, N = 128, K = 192   (A = Q from shared memory)
 //   O   += P(j)·V(j)  M = 128, N = 128, K = 128   (A = P from TMEM)
-//   l   += P(j)·1     M = 128, N = 16             (row sums of the bf16 P)
-// S is double-buffered in TMEM so that QK^T(j+1) runs while the softmax
-// works on tile j.  Warps: 0 TMA producer, 1 TMEM allocation + QK^T issue,
+// S and P are double-buffered in TMEM (O 128 + S 2 x 128 + P 2 x 64 = 512
+// columns), so QK^T(j+1) runs while the softmax works on tile j, and P(j)
+// is written while P·V(j-1) still reads the other buffer (P(j) waits for
+// P·V(j-2)).  The row sum l is kept per half by the softmax threads (the
+// rounded bf16 P, summed in fp32) and the halves' sums are added at the end.
+// Warps: 0 TMA producer, 1 TMEM allocation + QK^T issue,
 // 10 P·V issue (an MMA issue blocks while the tensor pipe's queue is full, so
 // one thread issuing both would hold P·V(j) behind QK^T(j+1)),
 // 2-9 softmax and epilogue: two warps per query row (thread = TMEM lane),
