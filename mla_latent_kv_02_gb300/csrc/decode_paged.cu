@@ -103,8 +103,9 @@ constexpr int kSmallMisc = kSmallPair + 4 * kH * 8;
 // misc: +0 abort flag, +8 TMEM address, +16 segment range [2], +32 copies
 // issued per softmax warp [8], +64 the peer's copies [8] (written by the
 // peer), +96 the abort flags of this CTA and the peer [2], +104 the last tile
-// armed on each exchange buffer [4].
-constexpr int kMiscPush = 32, kMiscPeerPush = 64, kMiscAborts = 96, kMiscArmed = 104;
+// armed on each exchange buffer [4], +120 the last tile whose QK^T MMAs are
+// all issued (FP8).
+constexpr int kMiscPush = 32, kMiscPeerPush = 64, kMiscAborts = 96, kMiscArmed = 104, kMiscQkIssued = 120;
 constexpr int kSmallBytes = kSmallMisc + 128;
 
 // The two cache formats.  bf16: the producer's TMA fills a 4-deep ring of
@@ -244,6 +245,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
   volatile uint32_t* peer_push = reinterpret_cast<volatile uint32_t*>(smem_raw + kSmallMisc + kMiscPeerPush);
   volatile int32_t* aborts = reinterpret_cast<volatile int32_t*>(smem_raw + kSmallMisc + kMiscAborts);
   int32_t* armed = reinterpret_cast<int32_t*>(smem_raw + kSmallMisc + kMiscArmed);
+  volatile int32_t* qk_issued = reinterpret_cast<volatile int32_t*>(smem_raw + kSmallMisc + kMiscQkIssued);
   const uint32_t base = (raw + kSmallBytes + 1023u) & ~1023u;
   const bool layout_fits = base + kAlignedBytes <= raw + kSmemBytes;
 #define BAR(i) (bars + 8u * (uint32_t)(i))
@@ -278,6 +280,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       peer_push[i] = 0u;
     }
     aborts[0] = aborts[1] = 0;
+    *qk_issued = -1;
     mbar_init(BAR(B_DRAIN), 1);
     mbar_init(BAR(B_DRAIN_PV), 1);
     fence_mbar_init();
@@ -422,6 +425,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
         for (int kk = 0; kk < 2; ++kk)
           mma_ts(tmem + kColS, tmem + kColQ + 128 + kk * 8, dr + (uint64_t)((kk * 32) >> 4), kIdescQK, 1u);
         tc_commit(BAR(B_S_FULL0 + (tq & 1u)));
+        if (kF8) *qk_issued = (int32_t)tq;
         cq.next();
       }
       // Every MMA of this thread must be finished before TMEM is released.
@@ -438,11 +442,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<kF8>::kThreads, 
       // The latent chunks read MN-major for P·V, and the ones tile.
       const uint64_t vdesc0 = sdesc_sw128(base + kOffKV, 8192, 1024);
       const uint64_t odesc0 = sdesc_sw128(base + kOffOnes, 16, 1024);
+      uint32_t G = 0;  // tiles of this cluster
+      for (int s = s_begin; s < s_end; ++s) G += (uint32_t)(a.segs[8 * s + 3] - a.segs[8 * s + 2]);
       for (uint32_t tp = 0; cp.valid(); ++tp) {
         const bool first = cp.first();
         if (!wait_phase<false, kIssueSuspend>(BAR(B_P_FULL), tp & 1u, err, abort_flag, a.wait_limit, a.wait_every)) break;
         if (first && !wait_phase<false, kIssueSuspend>(BAR(B_O_FREE), (uint32_t)(cp.s - s_begin) & 1u, err, abort_flag, a.wait_limit, a.wait_every))
           break;
+        // FP8: QK^T goes first in the tensor pipe, P·V(tp) being issued only
+        // after every MMA of QK^T(tp+2) is (QK^T(tp+2) needs nothing P·V(tp)
+        // produces); measured 2-4 % faster for FP8 and 10 % slower for bf16.
+        if (kF8 && tp + 2 < G && *qk_issued < (int32_t)(tp + 2)) {
+          const uint64_t t0 = cycles();
+          bool gave_up = false;
+          for (uint32_t it = 1; *qk_issued < (int32_t)(tp + 2); ++it) {
+            if ((it & a.wait_every) == 0u && (*abort_flag || cycles() - t0 > a.wait_limit)) {
+              if (!*abort_flag) atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              gave_up = true;
+              break;
+            }
+          }
+          if (gave_up) break;
+        }
         tc_fence_after();
         // O_r[128 x 256] += P[128 x 64] · V_r[64 x 256]; V_r is MN-major: 4 atoms
         // of 64 columns 8 KB apart (LBO), 8-token row groups 1 KB apart (SBO).
