@@ -18,6 +18,8 @@ layouts.  It checks:
   * no exchange buffer region is overwritten while it holds unconsumed
     scores or while a copy out of it is still reading it;
   * no reference-max slot is overwritten before its reader has read it.
+In the FP8 layout P·V of tile t also waits until QK^T of tile t+2 is
+issued (the kernel orders the tensor pipe that way there).
 Negative controls re-introduce, one at a time, a single shared score barrier,
 two hand-off slots instead of four, and a staging offset of one or three
 buffers; each must be caught.  The model is test infrastructure for the
@@ -106,7 +108,7 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             reading=[[False] * WARPS for _ in range(XBUFS)],  # a copy out of this region is in flight
             slot=[[None] * WARPS for _ in range(slots)], slot_unread=[[False] * WARPS for _ in range(slots)],
             abort=False, pushes=[0] * (2 * WARPS), peer_pushes=None, peer_abort=None,
-            armed=[-1] * XBUFS, exited=False,
+            armed=[-1] * XBUFS, exited=False, qk_issued=-1,
         ))
     events = []
 
@@ -180,6 +182,7 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
                 if not (yield from wait(c, lambda: c["q_ready"].test(seg))):
                     return
             events.append(("s", ci, t))
+            c["qk_issued"] = t
 
     def pv(ci):
         c = ctas[ci]
@@ -189,6 +192,10 @@ def run_model(segs, seed, shared_s_full=False, slots=4, xlead=2, fp8=False, conv
             seg, first, _ = tiles[t]
             if first:
                 if not (yield from wait(c, lambda: c["o_free"].test(seg))):
+                    return
+            # FP8: P·V(t) only after QK^T(t+2) is issued (tensor-pipe order)
+            if fp8 and t + 2 < G:
+                if not (yield from wait(c, lambda: c["qk_issued"] >= t + 2)):
                     return
             if fp8 and c["stage"][t % n_stages] != (t, "bf16"):
                 raise ProtocolError(f"P·V of tile {t} reads a stage holding {c['stage'][t % n_stages]}")
