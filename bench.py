@@ -52,7 +52,7 @@ def workload_stats(case):
 # the sha1 prefix of the decode kernel source it was taken on and the
 # workload.  Captured at half batch and scaled by the query rows (see
 # profiles/decode_kernel_mtp2_b32_ncu.md); any other source reads as null.
-MEASURED_TRAFFIC = {("d9ea1c84f38d", 2): 663.41e6}
+MEASURED_TRAFFIC = {("86c8047d28f0", 2): 664.54e6}
 
 
 def decode_traffic(workload: int, batch):
