@@ -50,6 +50,7 @@ constexpr int kQBytes = 3 * kChunkBytes;           // q_c (2 chunks) | q_r (1 ch
 constexpr int kKBytes = 3 * kChunkBytes;           // K_c (2 chunks) | k_R (1 chunk)
 constexpr int kVBytes = 2 * kChunkBytes;           // V_c (2 chunks of 64 columns)
 constexpr int kStages = 2;                         // depth of the K ring and of the V ring
+constexpr int kPvLag = 2;                          // P·V(j) is issued after every MMA of QK^T(j + kPvLag) (0: no order)
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kQBytes;
 constexpr int kOffV = kOffK + kStages * kKBytes;
@@ -105,6 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t bars = raw;
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(smem_raw + 8 * kNumBars);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 8 * kNumBars + 8);
+  volatile int32_t* qk_issued = reinterpret_cast<volatile int32_t*>(smem_raw + 8 * kNumBars + 16);
   const uint32_t base = (raw + kSmallBytes + 1023u) & ~1023u;
 #define BAR(i) (bars + 8u * (uint32_t)(i))
 
@@ -121,6 +123,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_flag = 0;
+    *qk_issued = -1;
     mbar_init(BAR(B_Q_FULL), 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(BAR(B_K_FULL + i), 1);
@@ -234,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                    dk + (uint64_t)((c * kChunkBytes + kk * 32) >> 4), kIdescQK, (c | kk) ? 1u : 0u);
         tc_commit(BAR(B_S_FULL + sb));
         tc_commit(BAR(B_K_EMPTY + st));
+        *qk_issued = j;
       }
       // every MMA of this thread has finished before TMEM is released
       tc_commit(BAR(B_DRAIN));
@@ -251,6 +255,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = wait_phase<false, false>(BAR(B_P_FULL + (t & 1)), (t >> 1) & 1, err, abort_flag) &&
              wait_phase<false, false>(BAR(B_V_FULL + t % kStages), (t / kStages) & 1, err, abort_flag);
         if (!ok) break;
+        // QK^T first in the tensor pipe: P·V(t) waits until every MMA of
+        // QK^T(t + kPvLag) is issued (which needs nothing P·V(t) produces),
+        // so the key stages free sooner
+        if (kPvLag > 0 && t + kPvLag < n_tiles && *qk_issued < t + kPvLag) {
+          const uint64_t t0 = cycles();
+          for (uint32_t it = 1; *qk_issued < t + kPvLag; ++it) {
+            if ((it & 255u) == 0u && (*abort_flag || cycles() - t0 > kWaitLimitCycles)) {
+              if (!*abort_flag) atomicOr(err, (int32_t)MLA_DEVERR_TIMEOUT);
+              *abort_flag = 1;
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+        }
         tc_fence_after();
         const uint64_t dv = vdesc0 + (uint64_t)(((t % kStages) * kVBytes) >> 4);
 #pragma unroll
