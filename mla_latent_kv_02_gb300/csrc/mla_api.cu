@@ -705,10 +705,10 @@ mla_status mla_expand_kv(const void* rows, int32_t n, const void* w_uk, const vo
   const uint32_t abox[3] = {64, 1, 128};
   mla_status s = make_map(&amap, rows, 3, adims, astr, abox, "latent rows");
   if (s != MLA_OK) return s;
-  // W_UK [128, 128 (d_hc), 512 (d_c)] read K-major: box 64 of d_c x 128 of d_hc x 1 head
+  // W_UK [128, 128 (d_hc), 512 (d_c)] read K-major: box 64 of d_c x 64 of d_hc (one CTA's half) x 1 head
   const uint64_t kdims[3] = {MLA_LATENT_DIM, MLA_HEAD_DIM_C, MLA_NUM_HEADS};
   const uint64_t kstr[2] = {MLA_LATENT_DIM * 2, (uint64_t)MLA_LATENT_DIM * 2 * MLA_HEAD_DIM_C};
-  const uint32_t kbox[3] = {64, 128, 1};
+  const uint32_t kbox[3] = {64, 64, 1};
   s = make_map(&kmap, w_uk, 3, kdims, kstr, kbox, "W_UK (K-major)");
   if (s != MLA_OK) return s;
   // W_UV [128, 512 (d_c), 128 (d_hc)] as in step A5
