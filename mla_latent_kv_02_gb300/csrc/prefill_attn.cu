@@ -11,16 +11,17 @@
 // arrays); query row i sits at position N - M + i and sees keys
 // [0, N - M + i].  Keys of a sequence's last tile that belong to the next
 // sequence are past N - 1 and always masked; query rows past M compute as
-// the last row and are not stored.  Key tiles of 128
-// tokens stream by TMA through two 2-deep rings, K = [K_c[h, ., 0:128] | k_R]
-// (192 columns, K-major) and V = V_c[h, ., :] (MN-major); K_c and V_c are
+// the last row and are not stored.  Key tiles of 128 tokens stream by TMA
+// through a 3-deep ring of K = [K_c[h, ., 0:128] | k_R] (192 columns,
+// K-major) and a 2-deep ring of V = V_c[h, ., :] (MN-major); K_c and V_c are
 // head-major, so a head's tile is 32 contiguous KB.  tcgen05:
-//   S(j) = Q·K(j)^T   M = 128, N = 128, K = 192   (A = Q from shared memory)
+//   S(j) = Q·K(j)^T   M = 128, N = 128, K = 192   (A = Q from TMEM)
 //   O   += P(j)·V(j)  M = 128, N = 128, K = 128   (A = P from TMEM)
-// S and P are double-buffered in TMEM (O 128 + S 2 x 128 + P 2 x 64 = 512
-// columns), so QK^T(j+1) runs while the softmax works on tile j, and P(j)
-// is written while P·V(j-1) still reads the other buffer (P(j) waits for
-// P·V(j-2)).  The row sum l is kept per half by the softmax threads (the
+// TMEM: O 128 | S 128 | P 2 x 64 | Q 96 columns.  QK^T(j+1) waits only
+// until the softmax has read S(j) into registers; P(j) is written while
+// P·V(j-1) still reads the other P buffer (P(j) waits for P·V(j-2)).  Q
+// sits in TMEM (copied from the third K stage, its landing place, before
+// K(2) loads there), which frees shared memory for the third K stage.  The row sum l is kept per half by the softmax threads (the
 // rounded bf16 P, summed in fp32) and the halves' sums are added at the end.
 // Warps: 0 TMA producer, 1 TMEM allocation + QK^T issue,
 // 10 P·V issue (an MMA issue blocks while the tensor pipe's queue is full, so
@@ -46,25 +47,24 @@ using namespace mla::dev;
 
 constexpr int kBM = 128, kBN = 128;                // query rows, key tokens per tile
 constexpr int kChunkBytes = 128 * 64 * 2;          // [128 rows x 64] bf16, 128-byte swizzle: 16 KB
-constexpr int kQBytes = 3 * kChunkBytes;           // q_c (2 chunks) | q_r (1 chunk)
-constexpr int kKBytes = 3 * kChunkBytes;           // K_c (2 chunks) | k_R (1 chunk)
+constexpr int kKBytes = 3 * kChunkBytes;           // K_c (2 chunks) | k_R (1 chunk); q_c | q_r the same way
 constexpr int kVBytes = 2 * kChunkBytes;           // V_c (2 chunks of 64 columns)
-constexpr int kStages = 2;                         // depth of the K ring and of the V ring
+constexpr int kStages = 3;                         // depth of the K ring
+constexpr int kVStages = 2;                        // depth of the V ring
+constexpr int kQStage = 2;                         // the K stage Q lands in (K(2) loads there after Q's copy)
 constexpr int kPvLag = 2;                          // P·V(j) is issued after every MMA of QK^T(j + kPvLag) (0: no order)
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kQBytes;
+constexpr int kOffK = 0;
 constexpr int kOffV = kOffK + kStages * kKBytes;
-constexpr int kOffOnes = kOffV + kStages * kVBytes;
-constexpr int kAlignedBytes = kOffOnes;
-constexpr int kNumBars = 24;
+constexpr int kAlignedBytes = kOffV + kVStages * kVBytes;
+constexpr int kNumBars = 26;
 constexpr int kOffXMax = 8 * kNumBars + 64;         // float [2 tile parities][2 halves][128 rows]
 constexpr int kOffXSum = kOffXMax + 2 * 2 * 128 * 4; // float [2 halves][128 rows]: the halves' row sums
 constexpr int kSmallBytes = kOffXSum + 2 * 128 * 4;
 constexpr int kSmemBytes = kSmallBytes + kAlignedBytes + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory layout does not fit");
 
-// TMEM: O, two score buffers, two P buffers (tile j's in buffer j mod 2)
-constexpr uint32_t kColO = 0, kColS = 128, kColP = 384, kTmemCols = 512;
+// TMEM: O, the score buffer, two P buffers (tile j's in buffer j mod 2), Q
+constexpr uint32_t kColO = 0, kColS = 128, kColP = 256, kColQ = 384, kTmemCols = 512;
 constexpr int kSoftWarp0 = 2;
 constexpr int kSoftWarps = 8;                      // two warps per TMEM lane quarter, 64 key columns each
 constexpr int kPvWarp = kSoftWarp0 + kSoftWarps;
@@ -74,12 +74,13 @@ constexpr uint32_t kIdescPV = idesc_bf16_f32(128, 128, false, true);
 
 enum : int {
   B_Q_FULL = 0,
+  B_Q_TMEM,                         // Q copied into TMEM, one arrival per softmax warp
   B_K_FULL,                         // kStages each: K and V have their own rings, so a K
   B_K_EMPTY = B_K_FULL + kStages,   // stage frees when QK^T is done, before P·V
   B_V_FULL = B_K_EMPTY + kStages,
-  B_V_EMPTY = B_V_FULL + kStages,
-  B_S_FULL = B_V_EMPTY + kStages,   // 2 (one per S buffer)
-  B_S_FREE = B_S_FULL + 2,          // 2, one arrival per softmax warp
+  B_V_EMPTY = B_V_FULL + kVStages,
+  B_S_FULL = B_V_EMPTY + kVStages,  // 2 (tile parity)
+  B_S_FREE = B_S_FULL + 2,          // 2 (tile parity), one arrival per softmax warp
   B_P_FULL = B_S_FREE + 2,          // 2 (P buffer), one arrival per softmax warp
   B_O_DONE = B_P_FULL + 2,          // 2 (tile parity): P·V of tile j complete
   B_DRAIN = B_O_DONE + 2,
@@ -125,9 +126,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     *qk_issued = -1;
     mbar_init(BAR(B_Q_FULL), 1);
+    mbar_init(BAR(B_Q_TMEM), kSoftWarps);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(BAR(B_K_FULL + i), 1);
       mbar_init(BAR(B_K_EMPTY + i), 1);
+    }
+    for (int i = 0; i < kVStages; ++i) {
       mbar_init(BAR(B_V_FULL + i), 1);
       mbar_init(BAR(B_V_EMPTY + i), 1);
     }
@@ -162,19 +166,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       prefetch_tmap(&q_map);
       prefetch_tmap(&k_map);
       prefetch_tmap(&v_map);
-      mbar_arrive_expect_tx(BAR(B_Q_FULL), (uint32_t)kQBytes);
-      tma_load_3d(base + kOffQ, &q_map, 0, h, sq.q_off + i0, BAR(B_Q_FULL));
-      tma_load_3d(base + kOffQ + kChunkBytes, &q_map, 64, h, sq.q_off + i0, BAR(B_Q_FULL));
-      tma_load_3d(base + kOffQ + 2 * kChunkBytes, &r_map, 0, h, sq.q_off + i0, BAR(B_Q_FULL));
-      // K(nk) as soon as its stage is free (QK^T(nk-2) done), V(nv) as soon as
-      // its stage is free (P·V(nv-2) done); a tile's K goes before its V.
+      const uint32_t qdst = base + kOffK + kQStage * kKBytes;
+      mbar_arrive_expect_tx(BAR(B_Q_FULL), (uint32_t)kKBytes);
+      tma_load_3d(qdst, &q_map, 0, h, sq.q_off + i0, BAR(B_Q_FULL));
+      tma_load_3d(qdst + kChunkBytes, &q_map, 64, h, sq.q_off + i0, BAR(B_Q_FULL));
+      tma_load_3d(qdst + 2 * kChunkBytes, &r_map, 0, h, sq.q_off + i0, BAR(B_Q_FULL));
+      // K(nk) as soon as its stage is free (QK^T(nk-3) done; K(2)'s stage once
+      // Q has left it for TMEM), V(nv) as soon as its stage is free (P·V(nv-2)
+      // done); a tile's K goes before its V.
       int nk = 0, nv = 0;
       bool ok = true;
       uint64_t t_last = cycles();
       uint32_t spins = 0;
       while (ok && nv < n_tiles) {
         bool progressed = false;
-        if (nk < n_tiles && (nk < kStages || mbar_test_wait(BAR(B_K_EMPTY + nk % kStages), ((nk - kStages) / kStages) & 1))) {
+        if (nk < n_tiles && (nk < kStages ? (nk != kQStage || mbar_test_wait(BAR(B_Q_TMEM), 0))
+                                          : mbar_test_wait(BAR(B_K_EMPTY + nk % kStages), ((nk - kStages) / kStages) & 1))) {
           const int st = nk % kStages, t0 = sq.kv_off + nk * kBN;
           const uint32_t dst = base + kOffK + st * kKBytes;
           mbar_arrive_expect_tx(BAR(B_K_FULL + st), (uint32_t)kKBytes);
@@ -184,8 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nk;
           progressed = true;
         }
-        if (nv < nk && (nv < kStages || mbar_test_wait(BAR(B_V_EMPTY + nv % kStages), ((nv - kStages) / kStages) & 1))) {
-          const int st = nv % kStages, t0 = sq.kv_off + nv * kBN;
+        if (nv < nk && (nv < kVStages || mbar_test_wait(BAR(B_V_EMPTY + nv % kVStages), ((nv - kVStages) / kVStages) & 1))) {
+          const int st = nv % kVStages, t0 = sq.kv_off + nv * kBN;
           const uint32_t dst = base + kOffV + st * kVBytes;
           mbar_arrive_expect_tx(BAR(B_V_FULL + st), (uint32_t)kVBytes);
           tma_load_3d(dst, &v_map, 0, t0, h, BAR(B_V_FULL + st));
@@ -210,22 +217,21 @@ __global__ void __launch_bounds__(kThreads, 1)
       wait_phase_drain(BAR(B_Q_FULL), 0);
       for (int k = (nk > kStages ? nk - kStages : 0); k < nk; ++k)
         wait_phase_drain(BAR(B_K_FULL + k % kStages), (k / kStages) & 1);
-      for (int k = (nv > kStages ? nv - kStages : 0); k < nv; ++k)
-        wait_phase_drain(BAR(B_V_FULL + k % kStages), (k / kStages) & 1);
+      for (int k = (nv > kVStages ? nv - kVStages : 0); k < nv; ++k)
+        wait_phase_drain(BAR(B_V_FULL + k % kVStages), (k / kVStages) & 1);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ---------------------------------------------------------------- QK^T issue
-    // S(j) = Q·K(j)^T once K(j) has landed and the softmax has read S(j-2)
-    // out of the same buffer.
+    // S(j) = Q·K(j)^T once K(j) has landed and the softmax has read S(j-1)
+    // out of the score buffer.
     if (lane == 0) {
-      const uint64_t qdesc = sdesc_sw128(base + kOffQ, 16, 1024);
       const uint64_t kdesc0 = sdesc_sw128(base + kOffK, 16, 1024);
-      bool ok = wait_phase<false, false>(BAR(B_Q_FULL), 0, err, abort_flag);
+      bool ok = wait_phase<false, false>(BAR(B_Q_TMEM), 0, err, abort_flag);
       for (int j = 0; ok && j < n_tiles; ++j) {
         const int st = j % kStages, sb = j & 1;
         ok = wait_phase<false, false>(BAR(B_K_FULL + st), (j / kStages) & 1, err, abort_flag) &&
-             (j < 2 || wait_phase<false, false>(BAR(B_S_FREE + sb), ((j - 2) >> 1) & 1, err, abort_flag));
+             (j < 1 || wait_phase<false, false>(BAR(B_S_FREE + ((j - 1) & 1)), ((j - 1) >> 1) & 1, err, abort_flag));
         if (!ok) break;
         tc_fence_after();
         const uint64_t dk = kdesc0 + (uint64_t)((st * kKBytes) >> 4);
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int c = 0; c < 3; ++c)
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            mma_ss(tmem + kColS + sb * 128, qdesc + (uint64_t)((c * kChunkBytes + kk * 32) >> 4),
+            mma_ts(tmem + kColS, tmem + kColQ + c * 32 + kk * 8,
                    dk + (uint64_t)((c * kChunkBytes + kk * 32) >> 4), kIdescQK, (c | kk) ? 1u : 0u);
         tc_commit(BAR(B_S_FULL + sb));
         tc_commit(BAR(B_K_EMPTY + st));
@@ -253,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int t = 0; ok && t < n_tiles; ++t) {
         ok = wait_phase<false, false>(BAR(B_P_FULL + (t & 1)), (t >> 1) & 1, err, abort_flag) &&
-             wait_phase<false, false>(BAR(B_V_FULL + t % kStages), (t / kStages) & 1, err, abort_flag);
+             wait_phase<false, false>(BAR(B_V_FULL + t % kVStages), (t / kVStages) & 1, err, abort_flag);
         if (!ok) break;
         // QK^T first in the tensor pipe: P·V(t) waits until every MMA of
         // QK^T(t + kPvLag) is issued (which needs nothing P·V(t) produces),
@@ -271,13 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!ok) break;
         }
         tc_fence_after();
-        const uint64_t dv = vdesc0 + (uint64_t)(((t % kStages) * kVBytes) >> 4);
+        const uint64_t dv = vdesc0 + (uint64_t)(((t % kVStages) * kVBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           const uint32_t acc = (t == 0 && kk == 0) ? 0u : 1u;
           mma_ts(tmem + kColO, tmem + kColP + (t & 1) * 64 + kk * 8, dv + (uint64_t)((kk * 2048) >> 4), kIdescPV, acc);
         }
-        tc_commit(BAR(B_V_EMPTY + t % kStages));
+        tc_commit(BAR(B_V_EMPTY + t % kVStages));
         tc_commit(BAR(B_O_DONE + (t & 1)));
       }
       tc_commit(BAR(B_DRAIN_PV));
@@ -299,7 +305,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     float m = -INFINITY;
     float l = 0.f;                                 // this half's row sum of P, at the reference max m
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
+    {
+      // Q into TMEM: row r's dims in packed pairs, half 0 the q_c chunks, half 1 q_r
+      bool w = wait_phase<false, true>(BAR(B_Q_FULL), 0, err, abort_flag);
+      if (!__all_sync(0xffffffffu, w)) {
+        ok = false;
+      } else {
+        const uint32_t qsrc = base + kOffK + kQStage * kKBytes + (uint32_t)r * 128u;
+#pragma unroll 1
+        for (int cc = 2 * half; cc < 2 + half; ++cc) {
+          uint32_t v[32];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float4 x = ld_shared_v4(qsrc + cc * kChunkBytes + (((uint32_t)u ^ ((uint32_t)r & 7u)) << 4));
+            v[4 * u] = __float_as_uint(x.x);
+            v[4 * u + 1] = __float_as_uint(x.y);
+            v[4 * u + 2] = __float_as_uint(x.z);
+            v[4 * u + 3] = __float_as_uint(x.w);
+          }
+          tmem_st32(tl + kColQ + 32 * cc, v);
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(BAR(B_Q_TMEM));
+      }
+    }
+    for (int j = 0; ok && j < n_tiles; ++j) {
       const int sb = j & 1;
       bool w = wait_phase<false, true>(BAR(B_S_FULL + sb), (j >> 1) & 1, err, abort_flag);
       if (!__all_sync(0xffffffffu, w)) {
@@ -310,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t own[32];                            // raw scores as fp16 pairs, then P as bf16 pairs
       {
         uint32_t s[64];
-        tmem_ld64_sync(tl + kColS + sb * 128 + half * 64, s);
+        tmem_ld64_sync(tl + kColS + half * 64, s);
 #pragma unroll
         for (int k = 0; k < 32; ++k)
           own[k] = cvt_f16x2_satfinite(__uint_as_float(s[2 * k]), __uint_as_float(s[2 * k + 1]));
