@@ -133,6 +133,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       prefetch_tmap(&k_map);
       prefetch_tmap(&v_map);
       const uint32_t lead_afull = mapa(BAR(kBarAFull), 0);
+      const uint64_t wpol = l2_policy_evict_last();  // W: read by every pair, kept in L2 past the output stream
       int g = 0, na = 0, cur = -1;
       bool ok = true;
       for (int64_t u = u0; u < u1 && ok; ++u) {
@@ -153,8 +154,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
           }
           if (even) mbar_arrive_expect_tx(BAR(kBarFull + s), 2u * kStage);
           const uint32_t dst = base + kOffB + s * kStage, lead_full = mapa(BAR(kBarFull + s), 0);
-          tma_load_3d_pair(dst, &k_map, kc * 64, 64 * (int)rank, h, lead_full);
-          tma_load_3d_pair(dst + kBHalf, &v_map, 64 * (int)rank, kc * 64, h, lead_full);
+          tma_load_3d_pair_hint(dst, &k_map, kc * 64, 64 * (int)rank, h, lead_full, wpol);
+          tma_load_3d_pair_hint(dst + kBHalf, &v_map, 64 * (int)rank, kc * 64, h, lead_full, wpol);
           *w_issued = g + 1;
         }
       }
@@ -206,6 +207,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t tl = tmem + ((uint32_t)(q * 32) << 16);
     const uint32_t lead_empty[2] = {mapa(BAR(kBarAccEmpty), 0), mapa(BAR(kBarAccEmpty + 1), 0)};
     const bool issuer = warp == 2 && lane == 0;
+    const uint64_t opol = l2_policy_evict_first();  // K_c / V_c: written once, read by the next kernel
     int j = 0, nbox = 0;
     for (int64_t u = u0; u < u1; ++u, ++j) {
       const int tb = (int)(u >> 7), h = (int)(u & 127);
@@ -233,7 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         named_bar_sync(kEpiBar, 128);
         if (issuer && m0 < n) {
-          tma_store_3d(bx < 2 ? &kc_map : &vc_map, box, (bx & 1) * 64, m0, h);
+          tma_store_3d_hint(bx < 2 ? &kc_map : &vc_map, box, (bx & 1) * 64, m0, h, opol);
           bulk_commit_group();
         }
       }

@@ -293,6 +293,14 @@ __device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int
                "r"(src), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// TMA tensor store with an L2 eviction-priority policy for the written lines.
+__device__ __forceinline__ void tma_store_3d_hint(const void* tmap, uint32_t src, int32_t x, int32_t y, int32_t z,
+                                                  uint64_t policy) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%2, %3, %4}], [%1], %5;" ::"l"(
+                   reinterpret_cast<uint64_t>(tmap)),
+               "r"(src), "r"(x), "r"(y), "r"(z), "l"(policy)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Every bulk store this thread committed has read its shared-memory source
 // (the source may be reused or released; the global writes complete before
@@ -395,6 +403,15 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const void* tmap,
       "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, "
       "%4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+// The same with an L2 eviction-priority policy (createpolicy) for the read.
+__device__ __forceinline__ void tma_load_3d_pair_hint(uint32_t dst, const void* tmap, int32_t x, int32_t y, int32_t z,
+                                                      uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], "
+      "[%1, {%2, %3, %4}], [%5], %6;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar), "l"(policy)
       : "memory");
 }
 // Arrive once on the barrier at shared::cluster address `bar` (this CTA's or
