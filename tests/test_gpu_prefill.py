@@ -36,7 +36,7 @@ def test_branch_threshold(api):
     assert api.mla_branch_for(255) == 0 and api.mla_branch_for(256) == 1 and api.mla_branch_for(1) == 0
 
 
-@pytest.mark.parametrize("n", [1, 130, 300, 2600])
+@pytest.mark.parametrize("n", [1, 130, 256, 257, 300, 2600])
 def test_expand_kv(api, n):
     case = wl.make_case([n], [1], seed=80 + n)
     rows = torch.cat([to_bf16(case.c_kv, "cuda"), to_bf16(case.k_r, "cuda")], dim=1).contiguous()
