@@ -85,8 +85,7 @@ enum : int {
   B_O_DONE = B_P_FULL + 2,          // 2 (tile parity): P·V of tile j complete
   B_DRAIN = B_O_DONE + 2,
   B_DRAIN_PV,
-  B_XMAX,                           // 2 (tile parity), one arrival per softmax warp
-  B_XSUM = B_XMAX + 2,              // the halves' row sums, one arrival per softmax warp
+  B_XSUM,                           // the halves' row sums, one arrival per softmax warp
   B_COUNT
 };
 static_assert(B_COUNT <= kNumBars, "barrier area too small");
@@ -146,8 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(BAR(B_XSUM), kSoftWarps);
     mbar_init(BAR(B_DRAIN), 1);
     mbar_init(BAR(B_DRAIN_PV), 1);
-    mbar_init(BAR(B_XMAX), kSoftWarps);
-    mbar_init(BAR(B_XMAX + 1), kSoftWarps);
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -366,17 +363,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 8; k < 32; ++k) mx[k & 7] = __hmax2(mx[k & 7], as_h2(own[k]));
       const __half2 mh = __hmax2(__hmax2(__hmax2(mx[0], mx[1]), __hmax2(mx[2], mx[3])),
                                  __hmax2(__hmax2(mx[4], mx[5]), __hmax2(mx[6], mx[7])));
-      // swap the halves' maxima through a tile-parity buffer and mbarrier: a
-      // warp writes tile j+2's value only after passing tile j+1's barrier,
-      // which every warp reaches after reading tile j's values
+      // swap the halves' maxima through a tile-parity buffer and the named
+      // barrier of this lane quarter's two warps: a warp writes tile j+2's
+      // value only after passing tile j+1's barrier, which its partner
+      // reaches after reading tile j's values.  A warp that leaves the loop
+      // early arrives once (below), which releases its partner's current or
+      // next sync; the partner then sees the abort flag before its next one.
       xmax[(sb * 2 + half) * 128 + r] = fmaxf(__low2float(mh), __high2float(mh));
-      __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(B_XMAX + sb));
-      w = wait_phase<false, true>(BAR(B_XMAX + sb), (j >> 1) & 1, err, abort_flag);
-      if (!__all_sync(0xffffffffu, w)) {
+      if (*abort_flag) {
         ok = false;
         break;
       }
+      named_bar_sync(1 + q4, 64);
       const float mt = fmaxf(xmax[(sb * 2) * 128 + r], xmax[(sb * 2 + 1) * 128 + r]);
       float factor = 1.f;
       bool resc = false;
@@ -431,6 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(B_P_FULL + (j & 1)));
     }
+    if (!ok) named_bar_arrive(1 + q4, 64);
     // ---- epilogue: out[i, h, 64 half : 64 half + 64] = O / l, l the sum of
     //      the two halves' row sums (swapped through shared memory)
     if (ok && n_tiles > 0) {
