@@ -17,7 +17,7 @@
 // Work unit = (256-token block, head); the pairs take contiguous ranges of
 // units in block-major order, so a pair reloads its rows once or twice.
 // Warps: 0 TMA producer (both CTAs: rows, then per head the W halves through
-// a 4-stage ring, every copy completing on the even CTA's barriers);
+// a 5-stage ring, every copy completing on the even CTA's barriers);
 // 1 TMEM allocation and, in the even CTA, the MMA issue; 2-5 the epilogue
 // (thread = token row = TMEM lane): two 256-column accumulators in TMEM
 // (K_c and V_c of one head) alternate, so the epilogue of head h — bf16
@@ -41,9 +41,9 @@ constexpr int kAChunk = 128 * 64 * 2;           // 16 KB: 128 rows x 64, 128-byt
 constexpr int kABytes = kKCh * kAChunk;         // 128 KB: this CTA's rows, resident
 constexpr int kBHalf = 64 * 64 * 2;             // 8 KB: this CTA's half of one W chunk
 constexpr int kStage = 2 * kBHalf;              // W_UK half | W_UV half
-constexpr int kStages = 4;
+constexpr int kStages = 5;
 constexpr int kBoxBytes = 128 * 64 * 2;         // one [128 tokens x 64] bf16 output box
-constexpr int kOutBufs = 2;
+constexpr int kOutBufs = 1;
 constexpr int kOffB = kABytes;
 constexpr int kOffOut = kOffB + kStages * kStage;
 constexpr int kOffBar = kOffOut + kOutBufs * kBoxBytes;
@@ -218,8 +218,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       const int m0 = tb * kTokBlock + 128 * (int)rank;
 #pragma unroll 1
       for (int bx = 0; bx < 4; ++bx, ++nbox) {  // K_c columns 0-63, 64-127, then V_c
-        const uint32_t box = base + kOffOut + (nbox & 1) * kBoxBytes;
-        if (issuer) bulk_wait_read<1>();  // the store from this buffer two boxes back has read it
+        const uint32_t box = base + kOffOut + (nbox % kOutBufs) * kBoxBytes;
+        if (issuer) bulk_wait_read<kOutBufs - 1>();  // the store from this buffer kOutBufs boxes back has read it
         named_bar_sync(kEpiBar, 128);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {

@@ -33,7 +33,7 @@ import random
 
 import pytest
 
-STAGES = 4
+STAGES = 5
 CHUNKS = 8          # W stages per unit (the latent's 512 columns in 64-wide chunks)
 STAGE, ROWS = 16, 128   # bytes a CTA's copy counts on the even CTA's barrier (model units)
 
