@@ -112,7 +112,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     *w_issued = 0;
     *a_issued = 0;
-
     for (int i = 0; i < kNumBars; ++i) mbar_init(BAR(i), i == kBarAccEmpty || i == kBarAccEmpty + 1 ? 8u : 1u);
     fence_mbar_init();
   }
