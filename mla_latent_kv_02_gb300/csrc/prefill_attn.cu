@@ -368,7 +368,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // value only after passing tile j+1's barrier, which its partner
       // reaches after reading tile j's values.  A warp that leaves the loop
       // early arrives once (below), which releases its partner's current or
-      // next sync; the partner then sees the abort flag before its next one.
+      // next sync; the partner cannot reach a second one, since QK^T of the
+      // tile after needs both warps' score reads (the abort check before the
+      // sync only makes it leave sooner).
       xmax[(sb * 2 + half) * 128 + r] = fmaxf(__low2float(mh), __high2float(mh));
       if (*abort_flag) {
         ok = false;
