@@ -91,7 +91,7 @@ def retire(bar, mine, peer, nbytes):
 
 
 def run_model(units, seed, abort_at=None, odd_arms=False, single_release=False, no_retire=False,
-              reload_unguarded=False):
+              reload_unguarded=False, slow_mma=False):
     """units: the pair's (token block, head) list in order.
     abort_at: (cta, step) — that CTA's abort flag goes up after `step` model
     steps (a wait that timed out); its roles leave at their next wait."""
@@ -227,6 +227,8 @@ def run_model(units, seed, abort_at=None, odd_arms=False, single_release=False, 
                sum(b.phase for b in full), a_full.phase, sum(b.phase for b in acc_empty),
                sum(b.phase for r in acc_full for b in r), len(released[0]) + len(released[1]))
         c = rng.choice(list(live) + ["copy lands"] * (len(in_flight) > 0) + ["MMA completes"] * (len(mma_queue) > 0))
+        if c == "MMA completes" and slow_mma and rng.random() < 0.9:
+            c = rng.choice(list(live))    # a slow tensor pipe: completions lag far behind issue
         if c == "copy lands":
             land(rng.randrange(len(in_flight)))
         elif c == "MMA completes":
@@ -240,7 +242,7 @@ def run_model(units, seed, abort_at=None, odd_arms=False, single_release=False, 
                sum(b.phase for b in full), a_full.phase, sum(b.phase for b in acc_empty),
                sum(b.phase for r in acc_full for b in r), len(released[0]) + len(released[1]))
         idle = idle + 1 if new == sig else 0
-        if idle > 400:
+        if idle > 5000:
             if not any(abort):
                 raise ProtocolError("deadlock: no role or completion makes progress")
             abort[0] = abort[1] = True   # the other CTA's bounded waits expire too
@@ -283,7 +285,7 @@ def random_units(rng):
 @pytest.mark.parametrize("seed", range(150))
 def test_pair_protocol_random(seed):
     rng = random.Random(1000 + seed)
-    run_model(random_units(rng), seed)
+    run_model(random_units(rng), seed, slow_mma=seed % 2 == 1)
 
 
 def test_pair_protocol_row_reloads():
