@@ -21,14 +21,18 @@
 // until the softmax has read S(j) into registers; P(j) is written while
 // P·V(j-1) still reads the other P buffer (P(j) waits for P·V(j-2)).  Q
 // sits in TMEM (copied from the third K stage, its landing place, before
-// K(2) loads there), which frees shared memory for the third K stage.  The row sum l is kept per half by the softmax threads (the
-// rounded bf16 P, summed in fp32) and the halves' sums are added at the end.
+// K(2) loads there), which frees shared memory for the third K stage.  The
+// row sum l is kept per half by the softmax threads (the rounded bf16 P,
+// summed in fp32) and the halves' sums are added at the end.
 // Warps: 0 TMA producer, 1 TMEM allocation + QK^T issue,
 // 10 P·V issue (an MMA issue blocks while the tensor pipe's queue is full, so
 // one thread issuing both would hold P·V(j) behind QK^T(j+1)),
 // 2-9 softmax and epilogue: two warps per query row (thread = TMEM lane),
 // each with 64 of a tile's 128 key columns; the two halves of a row swap
-// their maxima through shared memory once per tile.  The softmax
+// their maxima through shared memory and the named barrier of their lane
+// quarter once per tile.  P·V(j) is issued only after every MMA of
+// QK^T(j + 2) (QK^T first in the tensor pipe, so the key stages free
+// sooner).  The softmax
 // follows the decode kernel's: fp16 raw scores, a lazily moved reference max
 // (8 log2 units), P = 2^(c2 (s - m)) with one fused multiply-add, bf16 P.
 #include <cuda.h>
