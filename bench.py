@@ -29,6 +29,7 @@ sys.path.insert(0, ROOT)
 
 from mla_latent_kv_02_gb300 import workloads as wl  # noqa: E402
 
+E2E_SLOTS = 2     # steps in flight in the end-to-end loop (3 measured the same)
 METRIC = "MLA decode tokens/s and achieved KV HBM TB/s (% roofline), B=64 ctx 8K"
 SCALE = 1.0 / math.sqrt(192)
 FLOPS_PER_VISIBLE = 128 * (2 * 576 + 2 * 512)   # per (query row, visible token), all heads
@@ -604,8 +605,8 @@ def run_mla(args):
         raise RuntimeError("device error word set while timing the step's kernels")
 
     # ---- end to end through the API: pinned host inputs in, result out, plan rebuilt each step.
-    # Two steps in flight, as a serving loop runs: the host plans and enqueues
-    # step i+1 before it waits for step i's result and reads it; the copies
+    # E2E_SLOTS steps in flight, as a serving loop runs: the host plans and
+    # enqueues the next steps before it waits for step i's result and reads it; the copies
     # in and the copies out run on two streams of their own (double-buffered
     # device inputs and outputs), so that step i+1's inputs never queue behind
     # step i's result and both overlap the neighbouring steps' kernels.
@@ -614,25 +615,25 @@ def run_mla(args):
     h_c_new = c_new.cpu().pin_memory()
     h_k_new = k_new.cpu().pin_memory()
     h_slots = slots_new.cpu().pin_memory()
-    h_out = [torch.empty((T, 128, 128), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    h_out = [torch.empty((T, 128, 128), dtype=torch.bfloat16).pin_memory() for _ in range(E2E_SLOTS)]
     d_in = [(torch.empty_like(q_c), torch.empty_like(q_r), torch.empty_like(c_new), torch.empty_like(k_new),
-             torch.empty_like(slots_new)) for _ in range(2)]
-    d_out = [torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev) for _ in range(2)]
+             torch.empty_like(slots_new)) for _ in range(E2E_SLOTS)]
+    d_out = [torch.empty((T, 128, 128), dtype=torch.bfloat16, device=dev) for _ in range(E2E_SLOTS)]
     h2d = sum(t.numel() * t.element_size() for t in (h_q_c, h_q_r, h_c_new, h_k_new, h_slots))
     d2h = h_out[0].numel() * h_out[0].element_size()
     in_stream = torch.cuda.Stream(device=dev)
     out_stream = torch.cuda.Stream(device=dev)
-    ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of slot s landed
-    ev_used = [torch.cuda.Event() for _ in range(2)]   # the kernels of slot s are done with its buffers
-    ev_done = [torch.cuda.Event() for _ in range(2)]   # slot s's result is on the host
+    ev_in = [torch.cuda.Event() for _ in range(E2E_SLOTS)]     # inputs of slot s landed
+    ev_used = [torch.cuda.Event() for _ in range(E2E_SLOTS)]   # the kernels of slot s are done with its buffers
+    ev_done = [torch.cuda.Event() for _ in range(E2E_SLOTS)]   # slot s's result is on the host
     for e in ev_used:
         e.record(stream)
     checksum = [0.0]
     e2e_plans = [api.mla_decode_plan(case.seq_lens, case.q_lens, device=dev, num_clusters=plan.num_clusters)
-                 for _ in range(2)]
+                 for _ in range(E2E_SLOTS)]
 
     def e2e_issue(i):
-        sl = i % 2
+        sl = i % E2E_SLOTS
         dq_c, dq_r, dc_new, dk_new, dslots = d_in[sl]
         with torch.cuda.stream(in_stream):
             in_stream.wait_event(ev_used[sl])
@@ -658,17 +659,18 @@ def run_mla(args):
             ev_done[sl].record(out_stream)
 
     def e2e_collect(i):
-        ev_done[i % 2].synchronize()
-        checksum[0] += float(h_out[i % 2][0, 0, 0])   # the host reads this step's result
+        ev_done[i % E2E_SLOTS].synchronize()
+        checksum[0] += float(h_out[i % E2E_SLOTS][0, 0, 0])   # the host reads this step's result
 
     def e2e_run(n):
         for i in range(n):
             e2e_issue(i)
-            if i > 0:
-                e2e_collect(i - 1)
-        e2e_collect(n - 1)
+            if i >= E2E_SLOTS - 1:
+                e2e_collect(i - (E2E_SLOTS - 1))
+        for i in range(max(0, n - (E2E_SLOTS - 1)), n):
+            e2e_collect(i)
 
-    e2e_run(max(2, args.warmup))
+    e2e_run(max(E2E_SLOTS, args.warmup))
     barrier(ws)
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
@@ -731,7 +733,7 @@ def run_mla(args):
             "algorithmic": {"flops": st["flops"], "bytes": st["bytes"]},
         },
         "e2e": {"value": round(tokens * K / e2e_s, 1), "unit": "tokens/s", "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h), "steps_in_flight": 2},
+                "d2h_bytes_per_step": int(d2h), "steps_in_flight": E2E_SLOTS},
         "gpu_launches": launches_per_step * K,
         "clocks": clk,
         "parity": None,
